@@ -1,0 +1,71 @@
+"""Work and traffic accounting for attention forward (pure Python, no GPU).
+
+These are the measurement definitions the benchmark divides by:
+
+* FLOPs of one forward call: the two matrix products QK^T and PV cost
+  2 * Tq * Tk * d each per (batch, head), 4 * B * Hq * Tq * Tk * d in all
+  ("Attention from scratch + roofline", section "FLOPs / bytes / arithmetic
+  intensity"); under a causal mask half of that is counted (its exercise 3,
+  and the causal skip in "4.2 FlashAttention I", section "FlashAttention
+  forward").
+* Compulsory bytes: every input read once and every output written once,
+  Q + K + V + O in bf16 plus the fp32 row log-sum-exp.
+* The logical access model of "Explain tiled attention and verify its
+  output" (lab.py, estimate_hbm_bytes): the standard method's Q, K, V, O plus
+  four T x T passes (write S, read S, write P, read P), against the causal
+  outer-Q tiled loop that rereads the visible K/V rows once per query block.
+"""
+from __future__ import annotations
+
+import math
+
+BF16_BYTES = 2
+LSE_BYTES = 4
+
+
+def attention_flops(B: int, Hq: int, Tq: int, Tk: int, d: int, causal: bool) -> float:
+    """4*B*Hq*Tq*Tk*d, halved for a causal mask."""
+    f = 4.0 * B * Hq * Tq * Tk * d
+    return f / 2.0 if causal else f
+
+
+def prefill_compulsory_bytes(B: int, Hq: int, Hkv: int, Tq: int, Tk: int, d: int) -> int:
+    """Read Q, K, V once and write O (bf16) and LSE (fp32) once."""
+    q = B * Hq * Tq * d * BF16_BYTES
+    kv = 2 * B * Hkv * Tk * d * BF16_BYTES
+    o = B * Hq * Tq * d * BF16_BYTES
+    lse = B * Hq * Tq * LSE_BYTES
+    return q + kv + o + lse
+
+
+def decode_bytes(B: int, Hq: int, Hkv: int, Tk: int, d: int) -> int:
+    """Algorithmic bytes of one decode call: the KV cache read once, q read,
+    o and lse written.  Split-KV partials are not counted (they are an
+    implementation choice, reported separately)."""
+    return prefill_compulsory_bytes(B, Hq, Hkv, 1, Tk, d)
+
+
+def decode_flops(B: int, Hq: int, Tk: int, d: int) -> float:
+    return attention_flops(B, Hq, 1, Tk, d, causal=False)
+
+
+def logical_access_model(seq_len: int, num_heads: int = 32, head_dim: int = 128,
+                         bytes_per_elem: int = 2, block_q: int = 128) -> dict:
+    """Logical (not measured) HBM access counts for one layer, in bytes.
+
+    standard: Q, K, V, O plus S and P each written and read once (4 T^2 per head).
+    tiled_causal: Q and O once, plus K and V rows [0, min(T, q0 + block_q))
+    for every query block starting at q0 (no reuse between blocks assumed).
+    """
+    qkvo = 4 * num_heads * seq_len * head_dim * bytes_per_elem
+    nxn = 4 * num_heads * seq_len * seq_len * bytes_per_elem
+    kv_rows = sum(min(seq_len, q0 + block_q) for q0 in range(0, seq_len, block_q))
+    tiled = (2 * num_heads * seq_len * head_dim
+             + 2 * num_heads * kv_rows * head_dim) * bytes_per_elem
+    return {
+        "qkvo_bytes": qkvo,
+        "standard_nxn_bytes": nxn,
+        "standard_total_bytes": qkvo + nxn,
+        "tiled_causal_bytes": tiled,
+        "num_q_blocks": math.ceil(seq_len / block_q),
+    }

@@ -1,0 +1,35 @@
+"""Pins for the work/traffic accounting the benchmark divides by."""
+import json
+import os
+
+from online_softmax_03_gb300 import accounting as acc
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def test_logical_access_model_matches_recorded_sweep():
+    """'Explain tiled attention and verify its output', recorded
+    hbm_traffic_sweep (MB = 1e6 bytes, two decimals)."""
+    with open(os.path.join(GOLDEN, "p2_hbm_sweep.json")) as f:
+        gold = json.load(f)
+    for row in gold["rows"]:
+        m = acc.logical_access_model(row["seq_len"], 32, 128, 2, 128)
+        assert round(m["qkvo_bytes"] / 1e6, 2) == row["standard_qkv_o_mb"]
+        assert round(m["standard_nxn_bytes"] / 1e6, 2) == row["standard_nxn_matrix_hbm_mb"]
+        assert round(m["standard_total_bytes"] / 1e6, 2) == row["standard_total_hbm_mb"]
+        assert (round(m["tiled_causal_bytes"] / 1e6, 2)
+                == row["tiled_logical_access_mb_no_cache_reuse"])
+        assert m["num_q_blocks"] == row["num_q_blocks"]
+
+
+def test_flops_and_intensity():
+    """'Attention from scratch + roofline': 4*B*H*T*T*D FLOPs over Q+K+V+O
+    bytes; intensity doubles with T; decode stays memory-bound."""
+    def ai(T):
+        return acc.attention_flops(1, 32, T, T, 128, False) / (2 * 32 * 128 * 4 * T)
+    assert 1.8 <= ai(2048) / ai(1024) <= 2.2
+    assert acc.attention_flops(4, 32, 4096, 4096, 128, True) == 4 * 32 * 4096 * 4096 * 128 * 2
+    assert acc.decode_bytes(64, 32, 8, 8192, 128) == 2147483648 + 2 * 64 * 32 * 128 * 2 + 64 * 32 * 4
+    # GQA decode: 4 query heads share each K/V head, AI about 4 FLOP/byte
+    ai_dec = acc.decode_flops(64, 32, 8192, 128) / acc.decode_bytes(64, 32, 8, 8192, 128)
+    assert 3.9 < ai_dec < 4.1

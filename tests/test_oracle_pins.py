@@ -1,0 +1,303 @@
+"""Pins for the fp64 CPU oracle, against what the pages and mathematics fix.
+
+Each test ties the oracle to something other than itself: values printed on
+the pages, closed forms, invariants, library routines on special cases, or
+the agreement of two independently written algorithms (dense and blocked).
+Every plausible slip in the oracle (a dropped rescale, a wrong causal index,
+a transposed operand, a wrong GQA map, a missing max shift, a wrong LSE base)
+fails at least one of them.
+"""
+import json
+import math
+import os
+import random
+
+import numpy as np
+import pytest
+import scipy.special
+
+from oracle import oracle as ora
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _bhtd(x):
+    """[T, d] list/array -> [1, 1, T, d] float64."""
+    return np.asarray(x, dtype=np.float64)[None, None]
+
+
+def _lab_qkv(seq_len, head_dim, seed):
+    """The lab's input recipe: one random.Random stream, q then k then v,
+    row-major, each entry uniform on (-0.8, 0.8)."""
+    rng = random.Random(seed)
+    out = []
+    for _ in range(3):
+        out.append([[rng.uniform(-0.8, 0.8) for _ in range(head_dim)]
+                    for _ in range(seq_len)])
+    return out
+
+
+# --- values printed on the pages -------------------------------------------
+
+def test_p2_recorded_run_sample_rows_and_counts():
+    """'Explain tiled attention and verify its output': recorded result."""
+    gold = _golden("p2_lab_recorded.json")
+    q, k, v = _lab_qkv(gold["seq_len"], gold["head_dim"], gold["seed"])
+    q, k, v = _bhtd(q), _bhtd(k), _bhtd(v)
+    o, lse, ex = ora.attention_dense(q, k, v, causal=True)
+    half_ulp = 0.5 * 10.0 ** -gold["printed_decimals"] + 1e-12
+    np.testing.assert_allclose(o[0, 0, 0, :4], gold["sample_row0_first4"], rtol=0,
+                               atol=half_ulp)
+    np.testing.assert_allclose(o[0, 0, -1, :4], gold["sample_last_row_first4"],
+                               rtol=0, atol=half_ulp)
+    # the standard method keeps one score and one probability per visible pair
+    assert 2 * ex["visible_pairs"] == gold["standard_materialized_elements"]
+    ob, lseb, visited = ora.attention_blocked(q, k, v, gold["block_q"],
+                                              gold["block_kv"], causal=True)
+    assert visited == gold["flash_tiles_visited"]
+    assert np.abs(ob - o).max() < 1e-12
+    assert np.abs(lseb - lse).max() < 1e-12
+
+
+def test_p3_exercise2_online_softmax_trace():
+    """'4.2 FlashAttention I', Exercise 2: x=[3,1,6,2], block 2."""
+    gold = _golden("p3_exercise2.json")
+    p, lse, tr = ora.online_softmax_1d(gold["x"], gold["block"])
+    tol = gold["tolerance"]
+    assert tr["m"][0] == gold["m_after_block1"]
+    assert abs(tr["l"][0] - gold["l_after_block1"]) < tol
+    assert abs(tr["alpha"][1] - gold["alpha_block2"]) < tol
+    assert tr["m"][1] == gold["m_final"]
+    assert abs(tr["l"][1] - gold["l_final"]) < tol
+    assert abs(lse - gold["lse"]) < tol
+    # (a): the streamed denominator equals the two-pass one
+    x = np.asarray(gold["x"])
+    assert abs(tr["l"][1] - np.exp(x - x.max()).sum()) < 1e-15
+    assert abs(p.sum() - 1.0) < 1e-15
+
+
+def test_hand_example_t4_d2():
+    gold = _golden("hand_t4_d2.json")
+    q = _bhtd([[math.sqrt(2.0), 0.0]] * 4)
+    k = _bhtd([[math.log(j + 1.0), 0.0] for j in range(4)])
+    v = _bhtd(gold["v"])
+    scale = 1.0 / math.sqrt(2.0)
+    o, lse, _ = ora.attention_dense(q, k, v, causal=True, scale=scale)
+    np.testing.assert_allclose(o[0, 0], gold["causal_o"], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lse[0, 0], gold["causal_lse"], rtol=0, atol=1e-14)
+    o, lse, _ = ora.attention_dense(q, k, v, causal=False, scale=scale)
+    for i in range(4):
+        np.testing.assert_allclose(o[0, 0, i], gold["noncausal_o_every_row"], rtol=0,
+                                   atol=1e-14)
+        assert abs(lse[0, 0, i] - gold["noncausal_lse_every_row"]) < 1e-14
+    ob, lseb, _ = ora.attention_blocked(q, k, v, 3, 3, causal=True, scale=scale)
+    np.testing.assert_allclose(ob[0, 0], gold["causal_o"], rtol=0, atol=1e-14)
+
+
+# --- closed forms and invariants ---------------------------------------------
+
+def _rand(shape, seed, scale=1.0):
+    return np.random.default_rng(seed).standard_normal(shape) * scale
+
+
+def test_causal_row0_is_v0_and_lse0_is_s00():
+    q, k, v = _rand((2, 3, 9, 8), 1), _rand((2, 3, 9, 8), 2), _rand((2, 3, 9, 8), 3)
+    o, lse, _ = ora.attention_dense(q, k, v, causal=True)
+    np.testing.assert_allclose(o[:, :, 0], v[:, :, 0], rtol=0, atol=1e-15)
+    s00 = (q[:, :, 0] * k[:, :, 0]).sum(-1) / math.sqrt(8)
+    np.testing.assert_allclose(lse[:, :, 0], s00, rtol=0, atol=1e-14)
+
+
+def test_equal_keys_give_prefix_mean():
+    T, d = 37, 8
+    q = _rand((1, 2, T, d), 4)
+    k = np.broadcast_to(_rand((1, 2, 1, d), 5), (1, 2, T, d)).copy()
+    v = _rand((1, 2, T, d), 6)
+    s = (q * k).sum(-1) / math.sqrt(d)  # every key scores the same per row
+    o, lse, _ = ora.attention_dense(q, k, v, causal=True)
+    prefix_mean = np.cumsum(v, axis=2) / np.arange(1, T + 1)[None, None, :, None]
+    np.testing.assert_allclose(o, prefix_mean, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse, s + np.log(np.arange(1, T + 1)), rtol=0,
+                               atol=1e-13)
+    o, lse, _ = ora.attention_dense(q, k, v, causal=False)
+    np.testing.assert_allclose(o, np.broadcast_to(v.mean(2, keepdims=True), o.shape),
+                               rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse, s + math.log(T), rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_p_rows_sum_to_one_and_equal_exp_s_minus_lse(causal):
+    """Rows of P sum to 1; P_ij = exp(s_ij - L_i) on visible entries
+    ('4.2 FlashAttention I', Exercise 5; 'Efficient attention & KV cache',
+    exercise 3)."""
+    T, d = 23, 16
+    q, k, v = _rand((1, 2, T, d), 7), _rand((1, 2, T, d), 8), _rand((1, 2, T, d), 9)
+    o, lse, ex = ora.attention_dense(q, k, v, causal=causal, return_p=True)
+    p = ex["p"]
+    np.testing.assert_allclose(p.sum(-1), 1.0, rtol=0, atol=1e-14)
+    s = np.einsum("bhid,bhjd->bhij", q, k) / math.sqrt(d)
+    vis = np.tril(np.ones((T, T), bool)) if causal else np.ones((T, T), bool)
+    ref = np.where(vis, np.exp(s - lse[..., None]), 0.0)
+    np.testing.assert_allclose(p, ref, rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(o, np.einsum("bhij,bhjd->bhid", p, v), rtol=0,
+                               atol=1e-13)
+    assert ex["visible_pairs"] == 2 * (T * (T + 1) // 2 if causal else T * T)
+
+
+def test_special_case_single_row_matches_scipy_softmax_and_logsumexp():
+    """With one query row the method is softmax(s) @ V; scipy supplies both
+    the softmax and the log-sum-exp."""
+    Tk, d = 50, 12
+    q, k, v = _rand((1, 1, 1, d), 10, 3.0), _rand((1, 1, Tk, d), 11), _rand((1, 1, Tk, d), 12)
+    s = (k[0, 0] @ q[0, 0, 0]) * 0.37
+    o, lse, _ = ora.attention_dense(q, k, v, causal=False, scale=0.37)
+    assert abs(lse[0, 0, 0] - scipy.special.logsumexp(s)) < 1e-13
+    np.testing.assert_allclose(o[0, 0, 0], scipy.special.softmax(s) @ v[0, 0], rtol=0,
+                               atol=1e-14)
+
+
+def test_online_softmax_1d_matches_scipy():
+    """'Efficient attention & KV cache', section 3: online_softmax against the
+    library softmax and logsumexp, for chunks that do not divide the length."""
+    x = _rand((101,), 13, 5.0)
+    for chunk in (1, 4, 7, 101, 200):
+        p, lse, _ = ora.online_softmax_1d(x, chunk)
+        np.testing.assert_allclose(p, scipy.special.softmax(x), rtol=1e-13, atol=0)
+        assert abs(lse - scipy.special.logsumexp(x)) < 1e-13
+
+
+def test_gqa_head_map_is_consecutive_grouping():
+    """Query head h reads K/V head h // (Hq/Hkv): the same as repeating every
+    K/V head Hq/Hkv times in place (enable_gqa)."""
+    q = _rand((2, 8, 11, 8), 14)
+    k, v = _rand((2, 2, 13, 8), 15), _rand((2, 2, 13, 8), 16)
+    o, lse, _ = ora.attention_dense(q, k, v, causal=True)
+    kr, vr = np.repeat(k, 4, axis=1), np.repeat(v, 4, axis=1)
+    o2, lse2, _ = ora.attention_dense(q, kr, vr, causal=True)
+    np.testing.assert_array_equal(o, o2)
+    np.testing.assert_array_equal(lse, lse2)
+    # the other map (h % Hkv) would differ
+    kt, vt = np.tile(k, (1, 4, 1, 1)), np.tile(v, (1, 4, 1, 1))
+    o3, _, _ = ora.attention_dense(q, kt, vt, causal=True)
+    assert np.abs(o3 - o).max() > 1e-3
+
+
+def test_causal_alignment_is_bottom_right():
+    """Query i of Tq sits at key position i + Tk - Tq; with Tq = 1 causal is
+    attention over the whole cache."""
+    Tq, Tk, d = 3, 7, 4
+    q, k, v = _rand((1, 1, Tq, d), 17), _rand((1, 1, Tk, d), 18), _rand((1, 1, Tk, d), 19)
+    o, lse, _ = ora.attention_dense(q, k, v, causal=True)
+    for i in range(Tq):
+        last = i + Tk - Tq
+        oi, li, _ = ora.attention_dense(q[:, :, i:i + 1], k[:, :, :last + 1],
+                                        v[:, :, :last + 1], causal=False)
+        np.testing.assert_allclose(o[:, :, i], oi[:, :, 0], rtol=0, atol=1e-15)
+        np.testing.assert_allclose(lse[:, :, i], li[:, :, 0], rtol=0, atol=1e-15)
+    o1, l1, _ = ora.attention_dense(q[:, :, :1], k, v, causal=True)
+    o0, l0, _ = ora.attention_dense(q[:, :, :1], k, v, causal=False)
+    np.testing.assert_array_equal(o1, o0)
+    with pytest.raises(ValueError):
+        ora.attention_dense(k, q, q, causal=True)  # Tq > Tk under causal
+
+
+def test_bf16_inputs_are_upcast_exactly():
+    rng = np.random.default_rng(20)
+    bits = [rng.integers(0x3000, 0x4000, size=(1, 2, 9, 8), dtype=np.uint16) for _ in range(3)]
+    bits = [b | (rng.integers(0, 2, size=b.shape, dtype=np.uint16) << 15) for b in bits]
+    f64 = [(b.astype(np.uint32) << 16).view(np.float32).astype(np.float64) for b in bits]
+    o, lse, _ = ora.attention_dense(*bits, causal=True)
+    o2, lse2, _ = ora.attention_dense(*f64, causal=True)
+    np.testing.assert_array_equal(o, o2)
+    np.testing.assert_array_equal(lse, lse2)
+
+
+def test_rows_entry_point_matches_dense():
+    q, k, v = _rand((2, 4, 19, 8), 21), _rand((2, 2, 23, 8), 22), _rand((2, 2, 23, 8), 23)
+    for causal in (False, True):
+        o, lse, _ = ora.attention_dense(q, k, v, causal=causal)
+        rb, rh, ri = [0, 1, 1, 0, 1], [0, 3, 2, 1, 0], [0, 18, 7, 5, 12]
+        orow, lrow = ora.attention_rows(q, k, v, rb, rh, ri, causal=causal)
+        np.testing.assert_allclose(orow, o[rb, rh, ri], rtol=0, atol=1e-14)
+        np.testing.assert_allclose(lrow, lse[rb, rh, ri], rtol=0, atol=1e-14)
+
+
+# --- blocked online softmax against dense ------------------------------------
+
+@pytest.mark.parametrize("bq,bk", [(8, 8), (16, 16), (13, 19), (32, 8), (1, 1), (64, 64)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_blocked_equals_dense_any_tile(bq, bk, causal):
+    """Tile pairs from the lab's unit test, (1, 1), and a ragged T = 61."""
+    q, k, v = _rand((1, 2, 61, 16), 24), _rand((1, 2, 61, 16), 25), _rand((1, 2, 61, 16), 26)
+    o, lse, _ = ora.attention_dense(q, k, v, causal=causal)
+    ob, lseb, _ = ora.attention_blocked(q, k, v, bq, bk, causal=causal)
+    assert np.abs(ob - o).max() < 1e-12
+    assert np.abs(lseb - lse).max() < 1e-12
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_blocked_random_block_order_with_scores_times_20(causal):
+    """'Efficient attention & KV cache', failure modes: scores scaled x20 and
+    random block orders must not change the result."""
+    T, d, bk = 70, 8, 9
+    q, k, v = _rand((1, 3, T, d), 27, 20.0), _rand((1, 3, T, d), 28), _rand((1, 3, T, d), 29)
+    o, lse, _ = ora.attention_dense(q, k, v, causal=causal)
+    rng = np.random.default_rng(30)
+    for _ in range(4):
+        order = rng.permutation((T + bk - 1) // bk)
+        ob, lseb, _ = ora.attention_blocked(q, k, v, 16, bk, causal=causal,
+                                            kv_order=order)
+        assert np.abs(ob - o).max() < 1e-12
+        assert np.abs(lseb - lse).max() < 1e-11
+
+
+def test_blocked_gqa_and_tq_lt_tk():
+    q = _rand((2, 6, 20, 8), 31)
+    k, v = _rand((2, 3, 45, 8), 32), _rand((2, 3, 45, 8), 33)
+    for causal in (False, True):
+        o, lse, _ = ora.attention_dense(q, k, v, causal=causal)
+        ob, lseb, _ = ora.attention_blocked(q, k, v, 7, 10, causal=causal)
+        assert np.abs(ob - o).max() < 1e-12
+        assert np.abs(lseb - lse).max() < 1e-12
+
+
+def test_mutation_without_accumulator_rescale_is_caught():
+    """The lab's failure-boundary test: emphasise a late key so the running
+    max grows on a later tile; dropping the rescale of acc is then wrong by
+    more than 0.1 while the correct variant agrees to 1e-12."""
+    q, k, v = _lab_qkv(32, 8, 99)
+    k[-1] = [4.0] * 8
+    q, k, v = _bhtd(q), _bhtd(k), _bhtd(v)
+    o, _, _ = ora.attention_dense(q, k, v, causal=True)
+    good, _, _ = ora.attention_blocked(q, k, v, 8, 8, causal=True, rescale_acc=True)
+    bad, _, _ = ora.attention_blocked(q, k, v, 8, 8, causal=True, rescale_acc=False)
+    assert np.abs(good - o).max() < 1e-12
+    assert np.abs(bad - o).max() > 0.1
+
+
+def test_unshifted_softmax_overflows_while_stable_forms_agree():
+    """The lab's overflow test: logits near 1414 overflow exp() without the
+    max shift; the shifted dense form and the 1x1-blocked form agree."""
+    q = _bhtd([[500.0, 500.0], [500.0, 500.0]])
+    k = _bhtd([[1.0, 1.0], [2.0, 2.0]])
+    v = _bhtd([[1.0, 0.0], [0.0, 1.0]])
+    with pytest.raises(ora.OracleOverflow):
+        ora.attention_dense(q, k, v, causal=False, subtract_max=False)
+    o, lse, _ = ora.attention_dense(q, k, v, causal=False)
+    ob, lseb, _ = ora.attention_blocked(q, k, v, 1, 1, causal=False)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
+    assert np.abs(ob - o).max() < 1e-12
+
+
+def test_causal_tiles_visited_half_the_grid():
+    """Causal skipping visits only blocks at or below the diagonal."""
+    q = k = v = _rand((1, 1, 64, 4), 34)
+    _, _, visited = ora.attention_blocked(q, k, v, 16, 16, causal=True)
+    assert visited == 1 + 2 + 3 + 4
+    _, _, visited = ora.attention_blocked(q, k, v, 16, 16, causal=False)
+    assert visited == 16
