@@ -1,0 +1,472 @@
+"""Benchmark: exact attention forward on GB300.
+
+One step = one pass of the whole path over one batch of synthetic input:
+  1. causal prefill, B=4, H=32, T=4096, d=128 (attn_fwd, tensor cores), then
+  2. GQA decode, B=64, Hq=32, Hkv=8, Tk=8192, d=128 (attn_decode: split + combine).
+
+Printed (rank 0, one JSON line):
+  value     prefill TFLOP/s (causal FLOPs = 2*B*H*T^2*d), summed over ranks
+  decode    decode HBM GB/s (K+V+q+o+lse bytes), with its own roofline
+  e2e       the same metrics through the public API with pinned host buffers,
+            host->device inputs and device->host outputs inside the timed region
+  roofline  prefill kernel: achieved TFLOP/s vs the measured bf16 peak
+  cpu_baseline  the fp64 oracle timed on the host cores on a bounded sample
+
+`--impl reference` times the fp64 CPU oracle instead (the only reference that
+exists for this path), on the same metric and workload, one bounded sample
+per step.  Under torchrun only rank 0 runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+from online_softmax_03_gb300 import accounting as acct  # noqa: E402
+
+METRIC = "attn fwd TFLOP/s (causal-adjusted) & % bf16 peak; decode HBM GB/s & % of 8TB/s"
+PREFILL = synth.PREFILL_4K
+DECODE = synth.DECODE_GQA
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_sha(*names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "online_softmax_03_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+PREFILL_SOURCES = ("ptx.cuh", "prefill_kernel.cuh", "prefill.cu")
+DECODE_SOURCES = ("ptx.cuh", "decode_kernel.cuh", "decode.cu")
+
+
+def ncu_traffic(kernel_key, sha):
+    """DRAM bytes per launch recorded from an ncu capture, or None when the
+    kernel source changed since the capture."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(kernel_key)
+    if not e or e.get("source_sha") != sha:
+        return None
+    return e["dram_bytes_per_launch"]
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons in the background."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu_index), "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        self.proc.wait(timeout=10)
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, mx, reasons = [], [], set()
+        for r in rows:
+            r = [x.strip() for x in r]
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except (ValueError, IndexError):
+                continue
+            for n, val in zip(names, r[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ CPU legs
+
+def oracle_prefill_sample(q, k, v, n_heads):
+    """Time the fp64 oracle on the first n_heads heads of batch 0 (prefill)."""
+    from oracle import oracle as ora
+
+    qs, ks, vs = (synth.bf16_bits(t[:1, :n_heads]) for t in (q, k, v))
+    t0 = time.perf_counter()
+    ora.attention_dense(qs, ks, vs, causal=PREFILL.causal, scale=PREFILL.scale)
+    dt = time.perf_counter() - t0
+    flops = acct.attention_flops(1, n_heads, PREFILL.Tq, PREFILL.Tk, PREFILL.d, PREFILL.causal)
+    return flops, dt
+
+
+def oracle_decode_sample(q, k, v, n_batch):
+    from oracle import oracle as ora
+
+    qs, ks, vs = (synth.bf16_bits(t[:n_batch]) for t in (q, k, v))
+    t0 = time.perf_counter()
+    ora.attention_dense(qs, ks, vs, causal=False, scale=DECODE.scale)
+    dt = time.perf_counter() - t0
+    nbytes = acct.decode_bytes(n_batch, DECODE.Hq, DECODE.Hkv, DECODE.Tk, DECODE.d)
+    return nbytes, dt
+
+
+def omp_threads():
+    try:
+        return int(os.environ.get("OMP_NUM_THREADS", "")) or os.cpu_count()
+    except ValueError:
+        return os.cpu_count()
+
+
+PREFILL_SAMPLE_HEADS = 16
+DECODE_SAMPLE_BATCH = 8
+
+
+def cpu_baseline(qp, kp, vp, qd, kd, vd):
+    flops, dt = oracle_prefill_sample(qp, kp, vp, PREFILL_SAMPLE_HEADS)
+    nbytes, dtd = oracle_decode_sample(qd, kd, vd, DECODE_SAMPLE_BATCH)
+    return {
+        "value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": omp_threads(),
+        "kind": "oracle",
+        "sample": (f"fp64 dense oracle on {PREFILL_SAMPLE_HEADS} of {PREFILL.B * PREFILL.Hq} "
+                   f"heads of the prefill workload ({dt:.2f} s)"),
+        "decode": {"value": nbytes / dtd / 1e9, "unit": "GB/s",
+                   "sample": (f"fp64 dense oracle on {DECODE_SAMPLE_BATCH} of {DECODE.B} "
+                              f"sequences of the decode workload ({dtd:.2f} s)")},
+    }
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    from online_softmax_03_gb300 import binding
+    from online_softmax_03_gb300 import build as cuda_build
+
+    cuda_build.build()
+    binding.load_library()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    peaks, peak_src = load_peaks()
+
+    qp, kp, vp = synth.make_inputs(PREFILL, dev)
+    qd, kd, vd = synth.make_inputs(DECODE, dev)
+    op = torch.empty_like(qp)
+    lp = torch.empty((PREFILL.B, PREFILL.Hq, PREFILL.Tq), dtype=torch.float32, device=dev)
+    od = torch.empty_like(qd)
+    ld = torch.empty((DECODE.B, DECODE.Hq, 1), dtype=torch.float32, device=dev)
+    ws = binding.decode_workspace(kd, DECODE.Hq)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        binding.fwd(qp, kp, vp, causal=True, out=op, lse=lp)
+        binding.decode(qd, kd, vd, workspace=ws, out=od, lse=ld)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_start.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        binding.fwd(qp, kp, vp, causal=True, out=op, lse=lp)
+        ev[i][1].record(stream)
+        binding.decode(qd, kd, vd, workspace=ws, out=od, lse=ld)
+        ev[i][2].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    pre_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    dec_ms = [e[1].elapsed_time(e[2]) for e in ev]
+
+    # ---- end to end through the public API with pinned host buffers
+    E = max(3, min(args.e2e_steps, K))
+    hq, hk, hv = (t.cpu().pin_memory() for t in (qp, kp, vp))
+    hqd, hkd, hvd = (t.cpu().pin_memory() for t in (qd, kd, vd))
+    ho, hl = torch.empty_like(op, device="cpu").pin_memory(), torch.empty_like(lp, device="cpu").pin_memory()
+    hod, hld = torch.empty_like(od, device="cpu").pin_memory(), torch.empty_like(ld, device="cpu").pin_memory()
+    eve = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(E + 1)]
+
+    def e2e_step(i):
+        eve[i][0].record(stream)
+        qp.copy_(hq, non_blocking=True)
+        kp.copy_(hk, non_blocking=True)
+        vp.copy_(hv, non_blocking=True)
+        binding.fwd(qp, kp, vp, causal=True, out=op, lse=lp)
+        ho.copy_(op, non_blocking=True)
+        hl.copy_(lp, non_blocking=True)
+        eve[i][1].record(stream)
+        qd.copy_(hqd, non_blocking=True)
+        kd.copy_(hkd, non_blocking=True)
+        vd.copy_(hvd, non_blocking=True)
+        binding.decode(qd, kd, vd, workspace=ws, out=od, lse=ld)
+        hod.copy_(od, non_blocking=True)
+        hld.copy_(ld, non_blocking=True)
+        eve[i][2].record(stream)
+
+    e2e_step(E)  # warm-up of the copy path
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    for i in range(E):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e2e_pre_ms = sum(eve[i][0].elapsed_time(eve[i][1]) for i in range(E)) / E
+    e2e_dec_ms = sum(eve[i][1].elapsed_time(eve[i][2]) for i in range(E)) / E
+
+    pre_flops = acct.attention_flops(PREFILL.B, PREFILL.Hq, PREFILL.Tq, PREFILL.Tk, PREFILL.d,
+                                     PREFILL.causal)
+    dec_bytes = acct.decode_bytes(DECODE.B, DECODE.Hq, DECODE.Hkv, DECODE.Tk, DECODE.d)
+    pre_s = sum(pre_ms) / 1e3
+    dec_s = sum(dec_ms) / 1e3
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+
+    pre_s, dec_s = max_over_ranks(pre_s), max_over_ranks(dec_s)
+    total_ms = max_over_ranks(total_ms)
+    e2e_pre_ms, e2e_dec_ms = max_over_ranks(e2e_pre_ms), max_over_ranks(e2e_dec_ms)
+
+    pre_tflops = world * K * pre_flops / pre_s / 1e12
+    dec_gbs = world * K * dec_bytes / dec_s / 1e9
+    per_launch_tflops = pre_flops / (pre_s / K) / 1e12
+    per_launch_gbs = dec_bytes / (dec_s / K) / 1e9
+    peak_tf = peaks["bf16_tflops_sustained"]
+    peak_bw = peaks["hbm_gbs"]
+    h2d_pre = sum(t.numel() * t.element_size() for t in (qp, kp, vp))
+    d2h_pre = op.numel() * 2 + lp.numel() * 4
+    h2d_dec = sum(t.numel() * t.element_size() for t in (qd, kd, vd))
+    d2h_dec = od.numel() * 2 + ld.numel() * 4
+
+    if rank != 0:
+        return
+    result = {
+        "metric": METRIC,
+        "value": round(pre_tflops, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms / K, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": f"{PREFILL.name} + {DECODE.name}",
+            "prefill": {"B": PREFILL.B, "Hq": PREFILL.Hq, "Hkv": PREFILL.Hkv, "Tq": PREFILL.Tq,
+                        "Tk": PREFILL.Tk, "d": PREFILL.d, "causal": PREFILL.causal,
+                        "dist": PREFILL.dist, "seed": PREFILL.seed},
+            "decode": {"B": DECODE.B, "Hq": DECODE.Hq, "Hkv": DECODE.Hkv, "Tq": 1,
+                       "Tk": DECODE.Tk, "d": DECODE.d, "causal": False,
+                       "dist": DECODE.dist, "seed": DECODE.seed},
+            "l2": "no flush: inputs exceed the 129 MB L2 (prefill q+k+v 403 MB, decode cache 2.1 GB)",
+            "parallelism": f"replicas x{world} (each rank runs the full workload)",
+        },
+        "prefill_ms": round(pre_s * 1e3 / K, 4),
+        "roofline": {
+            "kernel": "prefill_fwd_kernel<128>",
+            "bound": "tensor",
+            "achieved": round(per_launch_tflops, 2),
+            "peak": peak_tf,
+            "unit": "TFLOP/s",
+            "frac": round(per_launch_tflops / peak_tf, 4),
+            "peak_source": f"{peak_src} bf16_tflops_sustained (the loop runs for seconds)",
+            "frac_of_burst_peak": round(per_launch_tflops / peaks["bf16_tflops"], 4),
+            "traffic": ncu_traffic("prefill_fwd_kernel<128>/" + PREFILL.name,
+                                   source_sha(*PREFILL_SOURCES)),
+            "algorithmic_flops_per_launch": pre_flops,
+        },
+        "decode": {
+            "value": round(dec_gbs, 1),
+            "unit": "GB/s",
+            "ms": round(dec_s * 1e3 / K, 4),
+            "frac_of_8TBs": round(per_launch_gbs / 8000.0, 4),
+            "roofline": {
+                "kernel": "decode_split_kernel<128,4> + decode_combine_kernel<128>",
+                "bound": "hbm",
+                "achieved": round(per_launch_gbs, 1),
+                "peak": peak_bw,
+                "unit": "GB/s",
+                "frac": round(per_launch_gbs / peak_bw, 4),
+                "peak_source": f"{peak_src} hbm_gbs",
+                "traffic": ncu_traffic("decode_split_kernel<128,4>/" + DECODE.name,
+                                       source_sha(*DECODE_SOURCES)),
+                "algorithmic_bytes_per_launch": dec_bytes,
+            },
+            "e2e": {"value": round(world * dec_bytes / (e2e_dec_ms / 1e3) / 1e9, 1),
+                    "unit": "GB/s", "h2d_bytes_per_step": h2d_dec,
+                    "d2h_bytes_per_step": d2h_dec},
+        },
+        "e2e": {
+            "value": round(world * pre_flops / (e2e_pre_ms / 1e3) / 1e12, 2),
+            "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d_pre,
+            "d2h_bytes_per_step": d2h_pre,
+            "steps": E,
+            "note": "prefill leg; the decode leg's e2e is under decode.e2e",
+        },
+        "gpu_launches": K * 3,
+        "clocks": clk,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(qp, kp, vp, qd, kd, vd)
+    print(json.dumps(result), flush=True)
+
+
+# --------------------------------------------------------- reference arm
+
+def _reference_rows(n, T, heads, offset):
+    """n (h, i) rows spread evenly over the heads and the causal row range."""
+    import numpy as np
+
+    idx = (np.arange(n, dtype=np.int64) * 7919 + offset) % (heads * T)
+    return np.zeros(n, np.int32), (idx // T).astype(np.int32), (idx % T).astype(np.int32)
+
+
+def run_reference(args, rank, world):
+    """Time the fp64 oracle (the only reference for this path) on the host
+    cores: each step evaluates a bounded, evenly spread sample of rows of the
+    causal prefill workload; FLOPs count 4*d per visible (row, key) pair."""
+    from oracle import oracle as ora
+
+    if rank != 0:
+        return
+    heads = 4
+    w = PREFILL.with_(B=1, Hq=heads, Hkv=heads)
+    q, k, v = (synth.bf16_bits(t) for t in synth.make_inputs(w, "cpu"))
+    budget = min(2.0, 150.0 / (args.steps + args.warmup))
+
+    def one(n, offset):
+        rb, rh, ri = _reference_rows(n, w.Tq, heads, offset)
+        t0 = time.perf_counter()
+        ora.attention_rows(q, k, v, rb, rh, ri, causal=True, scale=w.scale)
+        dt = time.perf_counter() - t0
+        flops = float(4 * w.d * (ri.astype("int64") + 1).sum())
+        return flops, dt
+
+    f, dt = one(256, 0)
+    n_rows = int(max(32, min(heads * w.Tq, 256 * budget / max(dt, 1e-6))))
+    flops_total, t_total = 0.0, 0.0
+    for step in range(args.warmup + args.steps):
+        flops, dt = one(n_rows, step * 104729)
+        if step >= args.warmup:
+            flops_total += flops
+            t_total += dt
+    value = flops_total / t_total / 1e12
+    sample = (f"each step: fp64 oracle on {n_rows} rows spread over {heads} causal heads "
+              f"of the prefill workload (T=4096, d=128); inputs drawn on the CPU")
+    result = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": t_total * 1e3 / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"{PREFILL.name} (sampled rows)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": omp_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(result), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        print(f"warning: --gpus {args.gpus} but WORLD_SIZE={world}", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch
+
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

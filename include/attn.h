@@ -1,0 +1,153 @@
+/*
+ * attn.h -- C ABI of the GB300 (sm_103a) exact attention forward library.
+ *
+ * The operation is exact scaled-dot-product attention with the row
+ * log-sum-exp, O = softmax(scale * Q K^T [+ causal mask]) V, computed with the
+ * online softmax: K/V tiles stream past a resident Q tile while a running
+ * row max m, running sum l and unnormalised accumulator acc are kept and
+ * rescaled by exp(m - m') whenever the max grows; O = acc / l and
+ * LSE = m + ln l.  Sources: "Efficient attention & KV cache", sections 2.1
+ * (online softmax, boxed recurrence) and 3 (blockwise forward with lse and
+ * the causal kv_end stop); "4.2 FlashAttention I: IO-Awareness & The Online
+ * Softmax", section "FlashAttention forward: tiling + online softmax fused
+ * into one pass" (the -inf guards, LSE = m + log l).  The argument list
+ * follows the fused attention signature quoted in "SDPA and
+ * FlashAttention's tiling" (query, key, value, is_causal, scale,
+ * enable_gqa) in the (batch, heads, seq, head_dim) layout.
+ *
+ * Conventions shared by every entry point
+ * --------------------------------------
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *    library never allocates, frees or retains them.
+ *  - bf16 tensors are dense and row-major:
+ *        q [B, Hq, Tq, d]      k, v [B, Hkv, Tk, d]      o [B, Hq, Tq, d]
+ *    lse is fp32 [B, Hq, Tq] and holds the natural-log log-sum-exp of the
+ *    scaled, masked scores of each row.
+ *  - q, k, v and o must be 16-byte aligned, lse 4-byte aligned.
+ *  - d (head_dim) must be 32, 64 or 128.
+ *  - Grouped-query attention: Hq % Hkv == 0 and query head h reads K/V
+ *    head h / (Hq / Hkv).
+ *  - Causal masking is aligned to the bottom-right corner: query row i sits
+ *    at key position i + (Tk - Tq) and sees keys j <= i + (Tk - Tq).  With
+ *    Tq == Tk this is the usual lower-triangular mask; causal with Tq > Tk
+ *    is rejected.
+ *  - scale must be finite and > 0; 0.0f selects 1/sqrt(d).
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *    default stream) and return after enqueueing.  Argument errors are
+ *    detected on the host before any CUDA call and leave every buffer
+ *    untouched.  Launch failures return ATTN_ERR_CUDA.  Faults inside a
+ *    kernel surface at the caller's next synchronisation; a kernel that
+ *    gives up on a bounded wait records ATTN_ERR_DEVICE_TIMEOUT in a device
+ *    status word read by attn_device_status().
+ *  - The entry points keep no per-call state and may be called from several
+ *    host threads.
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,    /* null pointer, bad size, bad scale, ...      */
+  ATTN_ERR_UNSUPPORTED = 2,    /* d not in {32,64,128}, or not an sm_103 GPU  */
+  ATTN_ERR_MISALIGNED = 3,     /* a pointer breaks the alignment rule         */
+  ATTN_ERR_WORKSPACE = 4,      /* decode workspace missing or too small       */
+  ATTN_ERR_CUDA = 5,           /* a CUDA runtime/driver call failed           */
+  ATTN_ERR_DEVICE_TIMEOUT = 6  /* a kernel gave up waiting (see below)        */
+} attn_status;
+
+/*
+ * attn_fwd -- prefill / general forward pass.
+ *
+ *   q, k, v   inputs as described above (device, bf16, read only)
+ *   o         output [B, Hq, Tq, d] bf16 (device, written)
+ *   lse       output [B, Hq, Tq] fp32 (device, written)
+ *   B, Hq, Hkv, Tq, Tk, d   sizes (all >= 1)
+ *   causal    0 = full attention, 1 = bottom-right causal mask
+ *   scale     softmax scale (0.0f = 1/sqrt(d))
+ *   stream    cudaStream_t to enqueue on
+ *
+ * The kernel keeps per query tile of 128 rows the running (m, l, acc) in
+ * fp32 (acc in tensor memory), computes both products on the tensor cores
+ * from bf16 operands with fp32 accumulation, and never writes a score or
+ * probability to global memory.  Under causal masking, K/V tiles wholly
+ * above the diagonal are not visited.
+ *
+ * Returns ATTN_OK or an attn_status code.
+ */
+int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+             int B, int Hq, int Hkv, int Tq, int Tk, int d, int causal,
+             float scale, void *stream);
+
+/*
+ * attn_decode_workspace_bytes -- scratch needed by attn_decode.
+ *
+ * Depends only on the sizes (not on the GPU), so it may be called before any
+ * device exists.  Returns 0 for invalid sizes.
+ */
+size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Tk, int d);
+
+/*
+ * attn_decode -- one query token per sequence against a KV cache (Tq = 1).
+ *
+ *   q         [B, Hq, 1, d] bf16      k_cache, v_cache [B, Hkv, Tk, d] bf16
+ *   o         [B, Hq, 1, d] bf16      lse [B, Hq, 1] fp32
+ *   scale     as for attn_fwd
+ *   workspace device scratch of at least attn_decode_workspace_bytes(...)
+ *             bytes, 16-byte aligned, owned by the caller; its contents on
+ *             entry do not matter and are overwritten.
+ *
+ * The cache is split along Tk into chunks processed in parallel; each chunk
+ * produces a partial (m, l, acc) per query head, and a second kernel merges
+ * the partials with the same rescaling the online softmax uses
+ * (m* = max m_s, l = sum e^(m_s - m*) l_s, O = sum e^(m_s - m*) acc_s / l).
+ * The merge rule follows from the associativity of the recurrence
+ * ("Efficient attention & KV cache", section 2.1: any running max gives the
+ * same final ratio); the pages show only sequential blocks.  Every query
+ * token sees the whole cache (the causal reading above with Tq = 1).
+ *
+ * Returns ATTN_OK or an attn_status code (ATTN_ERR_WORKSPACE if the
+ * workspace is NULL, misaligned or too small).
+ */
+int attn_decode(const void *q, const void *k_cache, const void *v_cache,
+                void *o, float *lse, int B, int Hq, int Hkv, int Tk, int d,
+                float scale, void *workspace, size_t workspace_bytes,
+                void *stream);
+
+/* Human-readable name of a status code (never NULL). */
+const char *attn_status_string(int status);
+
+/*
+ * attn_device_status -- read and clear the device-side status word of the
+ * current device.
+ *
+ * Every wait inside the kernels is bounded in time.  A kernel that gives up
+ * stops its work, drains its own copies and tensor-core operations, frees
+ * its tensor memory, records ATTN_ERR_DEVICE_TIMEOUT here and returns, so
+ * the CUDA context stays usable.  This call synchronises `stream`, copies
+ * the word to *status (ATTN_OK when nothing was recorded) and resets it.
+ * Returns ATTN_OK, or ATTN_ERR_CUDA if the copy fails.
+ */
+int attn_device_status(void *stream, int *status);
+
+/*
+ * attn_debug_set -- test hooks (process-wide; not for production use).
+ *
+ *   wait_limit_ns  time a kernel waits on one barrier before giving up
+ *                  (0 restores the default of 1 s)
+ *   inject         0 = none; 1 = the prefill kernel withholds the first V
+ *                  tile load, so a bounded wait must expire and report
+ *                  ATTN_ERR_DEVICE_TIMEOUT
+ */
+void attn_debug_set(unsigned long long wait_limit_ns, int inject);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H */

@@ -1,0 +1,180 @@
+"""Thin ctypes binding over libattn.so (the C ABI in include/attn.h).
+
+The functions named like the C entry points (attn_fwd, attn_decode, ...)
+take raw integers and pointers exactly as the C ABI does.  `fwd` and
+`decode` marshal torch CUDA tensors into those calls: they check dtype,
+device, layout and shapes, allocate the outputs with torch, and pass the
+current CUDA stream.  All attention arithmetic runs in the library's
+kernels; if the library is missing these functions raise instead of
+computing anything elsewhere.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libattn.so")
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_MISALIGNED = 3
+ATTN_ERR_WORKSPACE = 4
+ATTN_ERR_CUDA = 5
+ATTN_ERR_DEVICE_TIMEOUT = 6
+STATUS_CODES = (ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_MISALIGNED,
+                ATTN_ERR_WORKSPACE, ATTN_ERR_CUDA, ATTN_ERR_DEVICE_TIMEOUT)
+
+_lock = threading.Lock()
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {attn_status_string(status)}")
+
+
+def load_library():
+    """Load libattn.so (built by __graft_entry__.build()); raise if absent."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build the CUDA library first "
+                    "(python -c 'import __graft_entry__ as g; g.build()')")
+            lib = ctypes.CDLL(LIB_PATH)
+            vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+            lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+            lib.attn_fwd.restype = i
+            lib.attn_decode_workspace_bytes.argtypes = [i, i, i, i, i]
+            lib.attn_decode_workspace_bytes.restype = ctypes.c_size_t
+            lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp,
+                                        ctypes.c_size_t, vp]
+            lib.attn_decode.restype = i
+            lib.attn_status_string.argtypes = [i]
+            lib.attn_status_string.restype = ctypes.c_char_p
+            lib.attn_device_status.argtypes = [vp, ctypes.POINTER(i)]
+            lib.attn_device_status.restype = i
+            lib.attn_debug_set.argtypes = [ctypes.c_ulonglong, i]
+            lib.attn_debug_set.restype = None
+            _lib = lib
+    return _lib
+
+
+# ---------------------------------------------------------------- raw C ABI
+
+def attn_fwd(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, causal, scale, stream) -> int:
+    return load_library().attn_fwd(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, causal,
+                                   scale, stream)
+
+
+def attn_decode_workspace_bytes(B, Hq, Hkv, Tk, d) -> int:
+    return load_library().attn_decode_workspace_bytes(B, Hq, Hkv, Tk, d)
+
+
+def attn_decode(q, k_cache, v_cache, o, lse, B, Hq, Hkv, Tk, d, scale, workspace,
+                workspace_bytes, stream) -> int:
+    return load_library().attn_decode(q, k_cache, v_cache, o, lse, B, Hq, Hkv, Tk, d,
+                                      scale, workspace, workspace_bytes, stream)
+
+
+def attn_status_string(status: int) -> str:
+    return load_library().attn_status_string(status).decode()
+
+
+def attn_device_status(stream=None) -> int:
+    out = ctypes.c_int(0)
+    rc = load_library().attn_device_status(stream, ctypes.byref(out))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_device_status")
+    return out.value
+
+
+def attn_debug_set(wait_limit_ns: int = 0, inject: int = 0) -> None:
+    load_library().attn_debug_set(wait_limit_ns, inject)
+
+
+# ------------------------------------------------------- torch marshalling
+
+def _check_tensor(t, name, ndim):
+    import torch
+
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be on a CUDA device")
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16")
+    if t.dim() != ndim or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {ndim}-d tensor")
+
+
+def _stream_handle(stream):
+    import torch
+
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None,
+        lse=None, stream=None):
+    """O, LSE = attention(q [B,Hq,Tq,d], k/v [B,Hkv,Tk,d]) through attn_fwd."""
+    import torch
+
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check_tensor(t, n, 4)
+    B, Hq, Tq, d = q.shape
+    Bk, Hkv, Tk, dk = k.shape
+    if (Bk, dk) != (B, d) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("inconsistent q/k/v shapes")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Tq), dtype=torch.float32, device=q.device)
+    rc = attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                  B, Hq, Hkv, Tq, Tk, d, int(bool(causal)),
+                  0.0 if scale is None else float(scale), _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd")
+    return out, lse
+
+
+def decode_workspace(k_cache, q_heads: int):
+    """Allocate the scratch attn_decode needs for this cache shape."""
+    import torch
+
+    B, Hkv, Tk, d = k_cache.shape
+    n = attn_decode_workspace_bytes(B, q_heads, Hkv, Tk, d)
+    if n == 0:
+        raise ValueError("invalid decode sizes")
+    return torch.empty((n + 15) // 16 * 16, dtype=torch.uint8, device=k_cache.device)
+
+
+def decode(q, k_cache, v_cache, scale: float | None = None, workspace=None, out=None,
+           lse=None, stream=None):
+    """O, LSE for one query token per sequence: q [B,Hq,1,d] against the cache."""
+    import torch
+
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _check_tensor(t, n, 4)
+    B, Hq, Tq, d = q.shape
+    Bk, Hkv, Tk, dk = k_cache.shape
+    if Tq != 1 or (Bk, dk) != (B, d) or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("decode expects q [B,Hq,1,d] and caches [B,Hkv,Tk,d]")
+    if workspace is None:
+        workspace = decode_workspace(k_cache, Hq)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, 1), dtype=torch.float32, device=q.device)
+    rc = attn_decode(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), out.data_ptr(),
+                     lse.data_ptr(), B, Hq, Hkv, Tk, d,
+                     0.0 if scale is None else float(scale), workspace.data_ptr(),
+                     workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_decode")
+    return out, lse

@@ -1,0 +1,183 @@
+// api.cu -- the C ABI: argument validation (before any CUDA call), device
+// checks, TMA descriptor encoding, and dispatch to the kernel launchers.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/attn.h"
+#include "internal.h"
+
+#define ATTN_API extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+constexpr unsigned long long kDefaultWaitNs = 1000000000ull;  // 1 s
+std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};
+std::atomic<int> g_inject{0};
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *,
+                                   const cuuint32_t *, const cuuint32_t *,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Shared argument checks of attn_fwd / attn_decode.  No CUDA call.
+int validate(const void *q, const void *k, const void *v, const void *o,
+             const float *lse, int B, int Hq, int Hkv, int Tq, int Tk, int d,
+             int causal, float scale, float *scale_out) {
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Tq < 1 || Tk < 1) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (causal && Tq > Tk) return ATTN_ERR_INVALID_ARG;
+  if (!(std::isfinite(scale) && scale >= 0.f)) return ATTN_ERR_INVALID_ARG;
+  if (d != 32 && d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) ||
+      !aligned(lse, 4))
+    return ATTN_ERR_MISALIGNED;
+  *scale_out = (scale == 0.f) ? 1.f / std::sqrt((float)d) : scale;
+  return ATTN_OK;
+}
+
+}  // namespace
+
+namespace attn_host {
+
+int check_device_sm103(int *num_sms) {
+  int dev = 0, major = 0, minor = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (major != 10 || minor != 3) return ATTN_ERR_UNSUPPORTED;
+  if (num_sms) *num_sms = sms;
+  return ATTN_OK;
+}
+
+bool encode_tmap_3d_bf16(CUtensorMap *map, const void *base, uint64_t inner,
+                         uint64_t rows, uint64_t planes, uint32_t box_inner,
+                         uint32_t box_rows, int swizzle_bytes) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {inner, rows, planes};
+  const cuuint64_t strides[2] = {inner * 2, inner * rows * 2};
+  const cuuint32_t box[3] = {box_inner, box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapSwizzle sw =
+      swizzle_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
+            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace attn_host
+
+ATTN_API int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                      int B, int Hq, int Hkv, int Tq, int Tk, int d, int causal,
+                      float scale, void *stream) {
+  float sc = 0.f;
+  int rc = validate(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, causal, scale, &sc);
+  if (rc != ATTN_OK) return rc;
+  rc = attn_host::check_device_sm103(nullptr);
+  if (rc != ATTN_OK) return rc;
+  attn_host::PrefillArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.Tq = Tq;
+  a.Tk = Tk;
+  a.d = d;
+  a.causal = causal;
+  a.scale = sc;
+  a.stream = static_cast<cudaStream_t>(stream);
+  a.wait_ns = g_wait_ns.load();
+  a.inject = g_inject.load();
+  return attn_host::prefill_launch(a);
+}
+
+ATTN_API size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Tk, int d) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Tk < 1 || Hq % Hkv != 0) return 0;
+  if (d != 32 && d != 64 && d != 128) return 0;
+  return attn_host::decode_workspace_bytes_for(B, Hq, Tk, d);
+}
+
+ATTN_API int attn_decode(const void *q, const void *k_cache, const void *v_cache, void *o,
+                         float *lse, int B, int Hq, int Hkv, int Tk, int d, float scale,
+                         void *workspace, size_t workspace_bytes, void *stream) {
+  float sc = 0.f;
+  int rc = validate(q, k_cache, v_cache, o, lse, B, Hq, Hkv, 1, Tk, d, 0, scale, &sc);
+  if (rc != ATTN_OK) return rc;
+  if (!workspace || !aligned(workspace, 16) ||
+      workspace_bytes < attn_decode_workspace_bytes(B, Hq, Hkv, Tk, d))
+    return ATTN_ERR_WORKSPACE;
+  attn_host::DecodeArgs a;
+  a.q = q;
+  a.k = k_cache;
+  a.v = v_cache;
+  a.o = o;
+  a.lse = lse;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.Tk = Tk;
+  a.d = d;
+  a.scale = sc;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  a.stream = static_cast<cudaStream_t>(stream);
+  a.wait_ns = g_wait_ns.load();
+  return attn_host::decode_launch(a);
+}
+
+ATTN_API const char *attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG: invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED: unsupported head dim or GPU";
+    case ATTN_ERR_MISALIGNED: return "ATTN_ERR_MISALIGNED: pointer alignment";
+    case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE: workspace missing or too small";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA: CUDA call failed";
+    case ATTN_ERR_DEVICE_TIMEOUT: return "ATTN_ERR_DEVICE_TIMEOUT: kernel wait expired";
+    default: return "ATTN_ERR_UNKNOWN";
+  }
+}
+
+ATTN_API int attn_device_status(void *stream, int *status) {
+  if (!status) return ATTN_ERR_INVALID_ARG;
+  unsigned int a = 0, b = 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (attn_host::prefill_take_status(st, &a) != ATTN_OK ||
+      attn_host::decode_take_status(st, &b) != ATTN_OK)
+    return ATTN_ERR_CUDA;
+  *status = (int)(a > b ? a : b);
+  return ATTN_OK;
+}
+
+ATTN_API void attn_debug_set(unsigned long long wait_limit_ns, int inject) {
+  g_wait_ns.store(wait_limit_ns ? wait_limit_ns : kDefaultWaitNs);
+  g_inject.store(inject);
+}

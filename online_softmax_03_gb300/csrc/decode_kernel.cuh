@@ -1,0 +1,344 @@
+// decode_kernel.cuh -- one query token per sequence against a KV cache.
+//
+// Decode attention reads the whole cache once per step and does about one
+// multiply-add per cached element per query head, so it is bound by HBM
+// bandwidth, not arithmetic ("Attention from scratch + roofline", section
+// "Classify prefill vs decode"; "Efficient attention & KV cache", section
+// 2.4).  The kernels therefore run on the CUDA cores and are organised
+// around moving the cache once, coalesced:
+//
+//  * decode_split_kernel: grid (split, KV head x head chunk, batch).  One CTA
+//    streams a contiguous chunk of keys of one K/V head through shared memory
+//    with 1-D bulk copies (a ring of STAGES tiles of 32 keys, filled by one
+//    producer thread), and serves all query heads that share that K/V head
+//    (grouped-query attention), so each cache byte is read once per group.
+//    Each consumer warp takes groups of KG = 32/GP keys: a lane owns D/32
+//    head-dim columns, forms partial dot products for GP heads x KG keys,
+//    and one reduce-scatter across the warp leaves lane l with the full
+//    score of (head l / KG, key l % KG).  The online-softmax update of
+//    "Efficient attention & KV cache", section 2.1 then runs per head over
+//    those lanes, and the value accumulation again with lanes over head-dim
+//    columns.  The warps' partial (m, l, acc) are merged in shared memory
+//    and written to the workspace.
+//  * decode_combine_kernel: one warp per (batch, query head) merges the
+//    splits with the same rescaling (m* = max m_s, weights e^(m_s - m*)),
+//    writes O as bf16 and LSE in natural log.
+//
+// Scores are pre-scaled by scale*log2(e) so exponentials run in base 2.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "ptx.cuh"
+
+namespace attn_dev {
+
+constexpr unsigned int kDecodeStatusTimeout = 6;  // ATTN_ERR_DEVICE_TIMEOUT
+
+struct DecodeParams {
+  const __nv_bfloat16 *q;   // [B, Hq, 1, D]
+  const __nv_bfloat16 *k;   // [B, Hkv, Tk, D]
+  const __nv_bfloat16 *v;   // [B, Hkv, Tk, D]
+  float *part_acc;          // [B*Hq, nsplit, D]
+  float *part_ml;           // [B*Hq, nsplit, 2]  (m in log2 units, l)
+  unsigned int *status;
+  int Hq, Hkv, group, Tk;
+  int nsplit, chunk;        // keys per split (multiple of 32)
+  int n_hc;                 // head chunks of GP per K/V head
+  float scale_log2;
+  unsigned long long wait_ns;
+};
+
+template <int D, int GP>
+struct DecodeCfg {
+  static constexpr int CW = 4;                  // consumer warps
+  static constexpr int THREADS = (CW + 1) * 32;
+  static constexpr int TILE = 32;               // keys per stage
+  static constexpr int STAGES = 4;
+  static constexpr int KG = 32 / GP;            // keys per reduce-scatter
+  static constexpr int NGRP = TILE / KG;
+  static constexpr int VEC = D / 32;            // head-dim columns per lane
+  static constexpr uint32_t ROW_BYTES = D * 2;
+  static constexpr uint32_t TILE_BYTES = TILE * ROW_BYTES;
+  static constexpr uint32_t OFF_K = 0;
+  static constexpr uint32_t OFF_V = OFF_K + STAGES * TILE_BYTES;
+  static constexpr uint32_t OFF_P = OFF_V + STAGES * TILE_BYTES;   // [CW][32]
+  static constexpr uint32_t OFF_A = OFF_P + CW * 32 * 4;           // [CW][GP]
+  static constexpr uint32_t OFF_BAR = OFF_A + CW * GP * 4;
+  static constexpr uint32_t SMEM_BYTES = OFF_BAR + 2 * STAGES * 8 + 128;
+  // merge scratch, aliased on the (drained) K/V ring after the main loop
+  static constexpr uint32_t OFF_MM = 0;                            // [CW][GP]
+  static constexpr uint32_t OFF_LL = OFF_MM + CW * GP * 4;         // [CW][GP]
+  static constexpr uint32_t OFF_AA = OFF_LL + CW * GP * 4;         // [CW][GP][D]
+  static_assert(OFF_AA + CW * GP * D * 4 <= OFF_P, "merge scratch fits the ring");
+  static_assert(GP * KG == 32 && NGRP % CW == 0, "one value per lane");
+};
+
+// Lane l ends with the warp-wide sum of v[l] (the transpose-and-add network:
+// at each step a lane keeps one half of its values and sends the other).
+__device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    const bool up = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < off; ++i) {
+      const float send = up ? v[i] : v[i + off];
+      const float keep = up ? v[i + off] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+  return v[0];
+}
+
+template <int VEC>
+__device__ __forceinline__ void load_bf16_row(const uint8_t *src, float (&f)[VEC]) {
+  if constexpr (VEC == 4) {
+    const uint2 w = *reinterpret_cast<const uint2 *>(src);
+    f[0] = __uint_as_float(w.x << 16);
+    f[1] = __uint_as_float(w.x & 0xffff0000u);
+    f[2] = __uint_as_float(w.y << 16);
+    f[3] = __uint_as_float(w.y & 0xffff0000u);
+  } else if constexpr (VEC == 2) {
+    const uint32_t w = *reinterpret_cast<const uint32_t *>(src);
+    f[0] = __uint_as_float(w << 16);
+    f[1] = __uint_as_float(w & 0xffff0000u);
+  } else {
+    const uint32_t w = *reinterpret_cast<const uint16_t *>(src);
+    f[0] = __uint_as_float(w << 16);
+  }
+}
+
+template <int D, int GP>
+__global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS)
+    decode_split_kernel(const DecodeParams p) {
+  using C = DecodeCfg<D, GP>;
+  constexpr int ST = C::STAGES;
+  constexpr int KG = C::KG;
+  constexpr int VEC = C::VEC;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+  uint64_t *empty = full + ST;
+  float *pbuf = reinterpret_cast<float *>(smem + C::OFF_P);
+  float *abuf = reinterpret_cast<float *>(smem + C::OFF_A);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int sidx = blockIdx.x;
+  const int hk = blockIdx.y / p.n_hc;
+  const int hc = blockIdx.y - hk * p.n_hc;
+  const int b = blockIdx.z;
+  const int h0 = hk * p.group + hc * GP;          // first query head served
+  const int nh = min(GP, p.group - hc * GP);      // query heads served
+  const int k0 = sidx * p.chunk;
+  const int len = min(p.Tk, k0 + p.chunk) - k0;   // >= 1 (host guarantees)
+  const int ntiles = (len + C::TILE - 1) / C::TILE;
+  const size_t kv_off = ((size_t)(b * p.Hkv + hk) * p.Tk + k0) * D;
+  const uint8_t *kg = reinterpret_cast<const uint8_t *>(p.k + kv_off);
+  const uint8_t *vg = reinterpret_cast<const uint8_t *>(p.v + kv_off);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], C::CW);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == C::CW) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int last[ST];
+      for (int s = 0; s < ST; ++s) last[s] = -1;
+      for (int t = 0; t < ntiles; ++t) {
+        const int s = t % ST, u = t / ST;
+        if (t >= ST && !mbar_wait(&empty[s], (u - 1) & 1, p.wait_ns)) {
+          atomicExch(p.status, kDecodeStatusTimeout);
+          break;
+        }
+        const int rows = min(C::TILE, len - t * C::TILE);
+        const uint32_t bytes = rows * C::ROW_BYTES;
+        mbar_arrive_expect_tx(&full[s], 2 * bytes);
+        bulk_load(smem + C::OFF_K + s * C::TILE_BYTES, kg + (size_t)t * C::TILE_BYTES,
+                  bytes, &full[s]);
+        bulk_load(smem + C::OFF_V + s * C::TILE_BYTES, vg + (size_t)t * C::TILE_BYTES,
+                  bytes, &full[s]);
+        last[s] = t;
+      }
+      for (int s = 0; s < ST; ++s)
+        if (last[s] >= 0) mbar_wait(&full[s], (last[s] / ST) & 1, p.wait_ns);
+    }
+    __syncwarp();
+    return;  // the producer warp takes no part in the merge below
+  }
+
+  // -------------------------------------------------------------- consumers
+  float qv[GP][VEC];
+#pragma unroll
+  for (int hh = 0; hh < GP; ++hh) {
+    if (hh < nh) {
+      const uint8_t *qrow = reinterpret_cast<const uint8_t *>(
+          p.q + ((size_t)b * p.Hq + h0 + hh) * D);
+      float f[VEC];
+      load_bf16_row<VEC>(qrow + lane * VEC * 2, f);
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) qv[hh][e] = f[e] * p.scale_log2;
+    } else {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) qv[hh][e] = 0.f;
+    }
+  }
+  float acc[GP][VEC];
+#pragma unroll
+  for (int hh = 0; hh < GP; ++hh)
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) acc[hh][e] = 0.f;
+  float m = -INFINITY;  // for head lane / KG
+  float l = 0.f;
+  bool ok = true;
+  float *pw = pbuf + warp * 32;
+  float *aw = abuf + warp * GP;
+
+  for (int t = 0; t < ntiles; ++t) {
+    const int s = t % ST, u = t / ST;
+    ok = __all_sync(0xffffffffu, mbar_wait(&full[s], u & 1, p.wait_ns));
+    if (!ok) break;
+    const int rows_valid = min(C::TILE, len - t * C::TILE);
+    const uint8_t *ks = smem + C::OFF_K + s * C::TILE_BYTES;
+    const uint8_t *vs = smem + C::OFF_V + s * C::TILE_BYTES;
+#pragma unroll
+    for (int gi = warp; gi < C::NGRP; gi += C::CW) {
+      const int key0 = gi * KG;
+      float part[32];
+#pragma unroll
+      for (int kk = 0; kk < KG; ++kk) {
+        float kf[VEC];
+        load_bf16_row<VEC>(ks + (key0 + kk) * C::ROW_BYTES + lane * VEC * 2, kf);
+#pragma unroll
+        for (int hh = 0; hh < GP; ++hh) {
+          float a = 0.f;
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) a = fmaf(qv[hh][e], kf[e], a);
+          part[hh * KG + kk] = a;
+        }
+      }
+      float sc = warp_reduce_scatter32(part, lane);
+      const bool valid = key0 + (lane % KG) < rows_valid;
+      sc = valid ? sc : -INFINITY;
+      float mx = sc;
+#pragma unroll
+      for (int off = 1; off < KG; off <<= 1)
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      const float m_new = fmaxf(m, mx);
+      const float alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_new);
+      const float m_ref = (m_new == -INFINITY) ? 0.f : m_new;
+      const float pv = ex2_approx(sc - m_ref);
+      float ps = pv;
+#pragma unroll
+      for (int off = 1; off < KG; off <<= 1)
+        ps += __shfl_xor_sync(0xffffffffu, ps, off);
+      l = fmaf(l, alpha, ps);
+      m = m_new;
+      pw[lane] = pv;
+      if ((lane % KG) == 0) aw[lane / KG] = alpha;
+      __syncwarp();
+#pragma unroll
+      for (int hh = 0; hh < GP; ++hh) {
+        const float a = aw[hh];
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) acc[hh][e] *= a;
+      }
+#pragma unroll
+      for (int kk = 0; kk < KG; ++kk) {
+        if (key0 + kk < rows_valid) {
+          float vf[VEC];
+          load_bf16_row<VEC>(vs + (key0 + kk) * C::ROW_BYTES + lane * VEC * 2, vf);
+#pragma unroll
+          for (int hh = 0; hh < GP; ++hh) {
+            const float pk = pw[hh * KG + kk];
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) acc[hh][e] = fmaf(pk, vf[e], acc[hh][e]);
+          }
+        }
+      }
+      __syncwarp();
+    }
+    if (lane == 0) mbar_arrive(&empty[s]);
+  }
+  if (!ok) atomicExch(p.status, kDecodeStatusTimeout);
+
+  // ---- merge the consumer warps' states (the K/V ring is free now: every
+  // tile was waited for above).
+  named_barrier_sync(1, C::CW * 32);
+  float *mm = reinterpret_cast<float *>(smem + C::OFF_MM);
+  float *ll = reinterpret_cast<float *>(smem + C::OFF_LL);
+  float *aa = reinterpret_cast<float *>(smem + C::OFF_AA);
+  if ((lane % KG) == 0) {
+    mm[warp * GP + lane / KG] = m;
+    ll[warp * GP + lane / KG] = l;
+  }
+#pragma unroll
+  for (int hh = 0; hh < GP; ++hh)
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) aa[(warp * GP + hh) * D + lane * VEC + e] = acc[hh][e];
+  named_barrier_sync(1, C::CW * 32);
+  if (ok) {
+    for (int idx = threadIdx.x; idx < nh * D; idx += C::CW * 32) {
+      const int hh = idx / D, col = idx - hh * D;
+      float ms = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < C::CW; ++w) ms = fmaxf(ms, mm[w * GP + hh]);
+      float a = 0.f, ls = 0.f;
+#pragma unroll
+      for (int w = 0; w < C::CW; ++w) {
+        const float mw = mm[w * GP + hh];
+        const float wt = (mw == -INFINITY) ? 0.f : ex2_approx(mw - ms);
+        a = fmaf(wt, aa[(w * GP + hh) * D + col], a);
+        ls = fmaf(wt, ll[w * GP + hh], ls);
+      }
+      const size_t row = (size_t)b * p.Hq + h0 + hh;
+      p.part_acc[(row * p.nsplit + sidx) * D + col] = a;
+      if (col == 0) {
+        p.part_ml[(row * p.nsplit + sidx) * 2 + 0] = ms;
+        p.part_ml[(row * p.nsplit + sidx) * 2 + 1] = ls;
+      }
+    }
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(128)
+    decode_combine_kernel(const float *__restrict__ part_acc,
+                          const float *__restrict__ part_ml,
+                          __nv_bfloat16 *__restrict__ o, float *__restrict__ lse,
+                          int rows, int nsplit) {
+  constexpr int VEC = D / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 4 + warp;
+  if (row >= rows) return;
+  const float *ml = part_ml + (size_t)row * nsplit * 2;
+  const float *pa = part_acc + (size_t)row * nsplit * D;
+  float ms = -INFINITY;
+  for (int s = lane; s < nsplit; s += 32) ms = fmaxf(ms, ml[2 * s]);
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1)
+    ms = fmaxf(ms, __shfl_xor_sync(0xffffffffu, ms, off));
+  float acc[VEC];
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
+  float ls = 0.f;
+  for (int s = 0; s < nsplit; ++s) {
+    const float mw = ml[2 * s];
+    const float wt = (mw == -INFINITY) ? 0.f : ex2_approx(mw - ms);
+    ls = fmaf(wt, ml[2 * s + 1], ls);
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) acc[e] = fmaf(wt, pa[(size_t)s * D + lane * VEC + e], acc[e]);
+  }
+  const float inv = (ls > 0.f) ? 1.f / ls : 0.f;
+  __nv_bfloat16 *orow = o + (size_t)row * D + lane * VEC;
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) orow[e] = __float2bfloat16_rn(acc[e] * inv);
+  if (lane == 0) lse[row] = (ls > 0.f) ? (ms + log2f(ls)) * 0.6931471805599453f : 0.f;
+}
+
+}  // namespace attn_dev

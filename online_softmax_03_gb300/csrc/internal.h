@@ -1,0 +1,51 @@
+// internal.h -- declarations shared by the library's translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace attn_host {
+
+struct PrefillArgs {
+  const void *q, *k, *v;
+  void *o;
+  float *lse;
+  int B, Hq, Hkv, Tq, Tk, d, causal;
+  float scale;
+  cudaStream_t stream;
+  unsigned long long wait_ns;
+  int inject;
+};
+
+struct DecodeArgs {
+  const void *q, *k, *v;
+  void *o;
+  float *lse;
+  int B, Hq, Hkv, Tk, d;
+  float scale;
+  void *workspace;
+  size_t workspace_bytes;
+  cudaStream_t stream;
+  unsigned long long wait_ns;
+};
+
+// Return an attn_status code.
+int prefill_launch(const PrefillArgs &a);
+int decode_launch(const DecodeArgs &a);
+int prefill_take_status(cudaStream_t s, unsigned int *out);
+int decode_take_status(cudaStream_t s, unsigned int *out);
+
+// Shared helpers (api.cu).
+int check_device_sm103(int *num_sms);
+bool encode_tmap_3d_bf16(CUtensorMap *map, const void *base, uint64_t inner,
+                         uint64_t rows, uint64_t planes, uint32_t box_inner,
+                         uint32_t box_rows, int swizzle_bytes);
+
+// Decode split plan: depends only on sizes (and the SM count for the chosen
+// split, bounded above by the size-only maximum).
+int decode_max_splits(int Tk);
+size_t decode_workspace_bytes_for(int B, int Hq, int Tk, int d);
+
+}  // namespace attn_host
