@@ -27,7 +27,7 @@ int launch_d(const attn_host::PrefillArgs &a, unsigned int *status) {
   p.group = a.Hq / a.Hkv;
   p.Tq = a.Tq;
   p.Tk = a.Tk;
-  p.n_qt = (a.Tq + C::BM - 1) / C::BM;
+  p.n_qt = (a.Tq + C::NQ * C::BM - 1) / (C::NQ * C::BM);
   p.causal = a.causal;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.wait_ns = a.wait_ns;
