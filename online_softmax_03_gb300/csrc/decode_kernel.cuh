@@ -13,13 +13,16 @@
 //    producer thread), and serves all query heads that share that K/V head
 //    (grouped-query attention), so each cache byte is read once per group.
 //    Each consumer warp takes groups of KG = 32/GP keys: a lane owns D/32
-//    head-dim columns, forms partial dot products for GP heads x KG keys,
-//    and one reduce-scatter across the warp leaves lane l with the full
-//    score of (head l / KG, key l % KG).  The online-softmax update of
-//    "Efficient attention & KV cache", section 2.1 then runs per head over
-//    those lanes, and the value accumulation again with lanes over head-dim
-//    columns.  The warps' partial (m, l, acc) are merged in shared memory
-//    and written to the workspace.
+//    head-dim columns and forms partial dot products for the GP x KG
+//    (head, key) pairs.  Lane l keeps the partial of pair j at position
+//    j XOR l (its query heads and key rows are permuted accordingly), which
+//    makes the transpose-and-add network that leaves lane l with the full
+//    score of pair l free of selects: 31 shuffles and 31 adds for 32 pairs.
+//    The online-softmax update of "Efficient attention & KV cache", section
+//    2.1 then runs per head over those lanes, and the value accumulation with
+//    lanes over head-dim columns.  Products use packed fp32x2 FMAs.  The
+//    warps' partial (m, l, acc) are merged in shared memory and written to
+//    the workspace.
 //  * decode_combine_kernel: one warp per (batch, query head) merges the
 //    splits with the same rescaling (m* = max m_s, weights e^(m_s - m*)),
 //    writes O as bf16 and LSE in natural log.
@@ -62,8 +65,8 @@ struct DecodeCfg {
   static constexpr uint32_t TILE_BYTES = TILE * ROW_BYTES;
   static constexpr uint32_t OFF_K = 0;
   static constexpr uint32_t OFF_V = OFF_K + STAGES * TILE_BYTES;
-  static constexpr uint32_t OFF_P = OFF_V + STAGES * TILE_BYTES;   // [CW][32]
-  static constexpr uint32_t OFF_A = OFF_P + CW * 32 * 4;           // [CW][GP]
+  static constexpr uint32_t OFF_P = OFF_V + STAGES * TILE_BYTES;   // [CW][32] float2
+  static constexpr uint32_t OFF_A = OFF_P + CW * 32 * 8;           // [CW][GP]
   static constexpr uint32_t OFF_BAR = OFF_A + CW * GP * 4;
   static constexpr uint32_t SMEM_BYTES = OFF_BAR + 2 * STAGES * 8 + 128;
   // merge scratch, aliased on the (drained) K/V ring after the main loop
@@ -74,18 +77,16 @@ struct DecodeCfg {
   static_assert(GP * KG == 32 && NGRP % CW == 0, "one value per lane");
 };
 
-// Lane l ends with the warp-wide sum of v[l] (the transpose-and-add network:
-// at each step a lane keeps one half of its values and sends the other).
-__device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32], int lane) {
+// Transpose-and-add across the warp.  On entry lane l holds at position j
+// its partial for pair j XOR l; on exit v[0] is the warp-wide sum for pair l.
+// At the step with offset o a lane keeps positions [0, o) and adds what its
+// partner l ^ o holds at positions [o, 2o), which is the partner's partial
+// for the same pairs, so no lane-dependent select is needed.
+__device__ __forceinline__ float warp_reduce_scatter32_xor(float (&v)[32]) {
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) {
-    const bool up = (lane & off) != 0;
 #pragma unroll
-    for (int i = 0; i < off; ++i) {
-      const float send = up ? v[i] : v[i + off];
-      const float keep = up ? v[i + off] : v[i];
-      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-    }
+    for (int i = 0; i < off; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i + off], off);
   }
   return v[0];
 }
@@ -173,21 +174,29 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS)
   }
 
   // -------------------------------------------------------------- consumers
-  float qv[GP][VEC];
+  // Lane l's view of the 32 (head, key) pairs is permuted by XOR with l (see
+  // warp_reduce_scatter32_xor): position j holds head (j / KG) ^ hsel and key
+  // (j % KG) ^ ksel.  The query vectors are loaded in that permuted head
+  // order, pre-scaled by scale * log2(e) and duplicated into fp32x2 pairs.
+  const int hsel = lane / KG;
+  const int ksel = lane % KG;
+  float2 qd[GP][VEC];
 #pragma unroll
-  for (int hh = 0; hh < GP; ++hh) {
+  for (int hp = 0; hp < GP; ++hp) {
+    const int hh = hp ^ hsel;
     if (hh < nh) {
       const uint8_t *qrow = reinterpret_cast<const uint8_t *>(
           p.q + ((size_t)b * p.Hq + h0 + hh) * D);
       float f[VEC];
       load_bf16_row<VEC>(qrow + lane * VEC * 2, f);
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) qv[hh][e] = f[e] * p.scale_log2;
+      for (int e = 0; e < VEC; ++e) qd[hp][e] = make_float2(f[e] * p.scale_log2, f[e] * p.scale_log2);
     } else {
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) qv[hh][e] = 0.f;
+      for (int e = 0; e < VEC; ++e) qd[hp][e] = make_float2(0.f, 0.f);
     }
   }
+  // acc[h][e] for the natural head order, lanes over head-dim columns.
   float acc[GP][VEC];
 #pragma unroll
   for (int hh = 0; hh < GP; ++hh)
@@ -196,7 +205,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS)
   float m = -INFINITY;  // for head lane / KG
   float l = 0.f;
   bool ok = true;
-  float *pw = pbuf + warp * 32;
+  float2 *pw = reinterpret_cast<float2 *>(pbuf) + warp * 32;
   float *aw = abuf + warp * GP;
 
   for (int t = 0; t < ntiles; ++t) {
@@ -209,21 +218,26 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS)
 #pragma unroll
     for (int gi = warp; gi < C::NGRP; gi += C::CW) {
       const int key0 = gi * KG;
+      // K rows of this group in the lane's permuted key order.
+      float kf[KG][VEC];
+#pragma unroll
+      for (int jj = 0; jj < KG; ++jj)
+        load_bf16_row<VEC>(ks + (key0 + (jj ^ ksel)) * C::ROW_BYTES + lane * VEC * 2, kf[jj]);
       float part[32];
 #pragma unroll
-      for (int kk = 0; kk < KG; ++kk) {
-        float kf[VEC];
-        load_bf16_row<VEC>(ks + (key0 + kk) * C::ROW_BYTES + lane * VEC * 2, kf);
+      for (int hp = 0; hp < GP; ++hp) {
 #pragma unroll
-        for (int hh = 0; hh < GP; ++hh) {
-          float a = 0.f;
+        for (int jj = 0; jj < KG; jj += 2) {
+          float2 a = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int e = 0; e < VEC; ++e) a = fmaf(qv[hh][e], kf[e], a);
-          part[hh * KG + kk] = a;
+          for (int e = 0; e < VEC; ++e)
+            a = __ffma2_rn(qd[hp][e], make_float2(kf[jj][e], kf[jj + 1][e]), a);
+          part[hp * KG + jj] = a.x;
+          part[hp * KG + jj + 1] = a.y;
         }
       }
-      float sc = warp_reduce_scatter32(part, lane);
-      const bool valid = key0 + (lane % KG) < rows_valid;
+      float sc = warp_reduce_scatter32_xor(part);
+      const bool valid = key0 + ksel < rows_valid;
       sc = valid ? sc : -INFINITY;
       float mx = sc;
 #pragma unroll
@@ -239,14 +253,23 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS)
         ps += __shfl_xor_sync(0xffffffffu, ps, off);
       l = fmaf(l, alpha, ps);
       m = m_new;
-      pw[lane] = pv;
-      if ((lane % KG) == 0) aw[lane / KG] = alpha;
+      pw[lane] = make_float2(pv, pv);
+      if (ksel == 0) aw[hsel] = alpha;
       __syncwarp();
 #pragma unroll
       for (int hh = 0; hh < GP; ++hh) {
         const float a = aw[hh];
+        if constexpr (VEC % 2 == 0) {
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) acc[hh][e] *= a;
+          for (int e = 0; e < VEC; e += 2) {
+            const float2 y = __fmul2_rn(make_float2(acc[hh][e], acc[hh][e + 1]), make_float2(a, a));
+            acc[hh][e] = y.x;
+            acc[hh][e + 1] = y.y;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) acc[hh][e] *= a;
+        }
       }
 #pragma unroll
       for (int kk = 0; kk < KG; ++kk) {
@@ -255,9 +278,19 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS)
           load_bf16_row<VEC>(vs + (key0 + kk) * C::ROW_BYTES + lane * VEC * 2, vf);
 #pragma unroll
           for (int hh = 0; hh < GP; ++hh) {
-            const float pk = pw[hh * KG + kk];
+            const float2 pk = pw[hh * KG + kk];
+            if constexpr (VEC % 2 == 0) {
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) acc[hh][e] = fmaf(pk, vf[e], acc[hh][e]);
+              for (int e = 0; e < VEC; e += 2) {
+                const float2 y = __ffma2_rn(pk, make_float2(vf[e], vf[e + 1]),
+                                            make_float2(acc[hh][e], acc[hh][e + 1]));
+                acc[hh][e] = y.x;
+                acc[hh][e + 1] = y.y;
+              }
+            } else {
+#pragma unroll
+              for (int e = 0; e < VEC; ++e) acc[hh][e] = fmaf(pk.x, vf[e], acc[hh][e]);
+            }
           }
         }
       }
