@@ -119,6 +119,37 @@ int attn_decode(const void *q, const void *k_cache, const void *v_cache,
                 float scale, void *workspace, size_t workspace_bytes,
                 void *stream);
 
+/*
+ * attn_decode_noalloc -- attn_decode for callers that cannot allocate.
+ *
+ * The pages have no counterpart: this is a deployment variant of
+ * attn_decode.  It exists for callers that cannot call cudaMalloc where they
+ * decode -- code running inside a host framework that owns every device
+ * allocation, serving loops that cannot afford cudaMalloc's implicit device
+ * synchronisation, or deployments whose memory plan is fixed at start-up.
+ * Instead of a caller workspace it uses a scratch array that is part of the
+ * library image: ATTN_DECODE_NOALLOC_MAX_BYTES (16 MiB) of device memory on
+ * every GPU where the library is loaded, held until the process exits.
+ *
+ * Arguments, layouts and results are those of attn_decode, without the
+ * workspace.  The call allocates nothing (no cudaMalloc, cudaFree or
+ * allocating library routine).
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) for that device, so make that first call before
+ *    any stream capture begins.
+ *  - Problems whose split plan needs more than ATTN_DECODE_NOALLOC_MAX_BYTES
+ *    of partial results (B * Hq * splits * (d + 2) * 4 bytes) are rejected
+ *    with ATTN_ERR_WORKSPACE before anything is launched.
+ *  - Every call uses the same array.  Calls that overlap on the GPU (other
+ *    streams, other host threads) race on it and must be ordered by the
+ *    caller.  The array keeps the last call's contents; no call depends on
+ *    them, since every partial is written before it is read.
+ */
+#define ATTN_DECODE_NOALLOC_MAX_BYTES ((size_t)16 << 20)
+int attn_decode_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                        void *o, float *lse, int B, int Hq, int Hkv, int Tk, int d,
+                        float scale, void *stream);
+
 /* Human-readable name of a status code (never NULL). */
 const char *attn_status_string(int status);
 

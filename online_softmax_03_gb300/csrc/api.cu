@@ -89,6 +89,14 @@ bool encode_tmap_3d_bf16(CUtensorMap *map, const void *base, uint64_t inner,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Argument checks of attn_decode (Tq = 1, no mask), for entry points that
+// supply their own scratch.  No CUDA call.
+int validate_decode_args(const void *q, const void *k, const void *v, const void *o,
+                         const float *lse, int B, int Hq, int Hkv, int Tk, int d,
+                         float scale, float *scale_out) {
+  return validate(q, k, v, o, lse, B, Hq, Hkv, 1, Tk, d, 0, scale, scale_out);
+}
+
 }  // namespace attn_host
 
 ATTN_API int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,

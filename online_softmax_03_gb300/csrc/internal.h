@@ -38,6 +38,9 @@ int prefill_take_status(cudaStream_t s, unsigned int *out);
 int decode_take_status(cudaStream_t s, unsigned int *out);
 
 // Shared helpers (api.cu).
+int validate_decode_args(const void *q, const void *k, const void *v, const void *o,
+                         const float *lse, int B, int Hq, int Hkv, int Tk, int d,
+                         float scale, float *scale_out);
 int check_device_sm103(int *num_sms);
 bool encode_tmap_3d_bf16(CUtensorMap *map, const void *base, uint64_t inner,
                          uint64_t rows, uint64_t planes, uint32_t box_inner,

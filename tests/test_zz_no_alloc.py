@@ -1,0 +1,84 @@
+"""attn_decode_noalloc: decode for callers that cannot allocate device memory.
+
+Some callers cannot call cudaMalloc where they decode (a host framework owns
+all device allocations, a serving loop cannot afford the implicit device
+synchronisation, or the memory plan is frozen at start-up).  The library
+gives them an entry point whose scratch is a fixed 16 MiB array inside the
+library image.  These tests call it through the C ABI and check it against
+attn_decode (which takes a caller workspace), on two different problems in
+a row so the second call runs on whatever the first left in the shared
+array.  The file is named to be collected last.
+"""
+import ctypes
+import re
+import os
+
+import pytest
+import torch
+
+import synth
+from online_softmax_03_gb300 import binding
+from online_softmax_03_gb300 import build as cuda_build
+from parity import TOL_MAX_LSE, TOL_MAX_O, TOL_MEAN_O
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _entry():
+    cuda_build.build()
+    lib = binding.load_library()
+    f = lib.attn_decode_noalloc
+    vp, i = ctypes.c_void_p, ctypes.c_int
+    f.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.c_float, vp]
+    f.restype = i
+    return f
+
+
+def _max_bytes():
+    with open(os.path.join(ROOT, "include", "attn.h")) as fh:
+        m = re.search(r"#define ATTN_DECODE_NOALLOC_MAX_BYTES \(\(size_t\)(\d+) << (\d+)\)", fh.read())
+    return int(m.group(1)) << int(m.group(2))
+
+
+def _call(f, q, k, v):
+    B, Hq, _, d = q.shape
+    _, Hkv, Tk, _ = k.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, 1), dtype=torch.float32, device=q.device)
+    rc = f(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+           B, Hq, Hkv, Tk, d, 0.0, torch.cuda.current_stream().cuda_stream)
+    return rc, o, lse
+
+
+def test_noalloc_decode_matches_attn_decode_on_two_calls_in_a_row():
+    f = _entry()
+    problems = [
+        synth.DECODE_GQA,  # B=64 Hq=32 Hkv=8 Tk=8192 d=128
+        synth.Workload("dec_b4_hq16_hkv2_tk1500_d64", 4, 16, 2, 1, 1500, 64, False,
+                       "normal", 21, decode=True),
+    ]
+    for w in problems:
+        q, k, v = synth.make_inputs(w, "cuda")
+        o_ref, lse_ref = binding.decode(q, k, v)
+        rc, o, lse = _call(f, q, k, v)
+        assert rc == binding.ATTN_OK, binding.attn_status_string(rc)
+        torch.cuda.synchronize()
+        do = (o.float() - o_ref.float()).abs()
+        dl = (lse - lse_ref).abs()
+        assert do.max().item() <= TOL_MAX_O and do.mean().item() <= TOL_MEAN_O, w.name
+        assert dl.max().item() <= TOL_MAX_LSE, w.name
+        del q, k, v
+    assert binding.attn_device_status() == binding.ATTN_OK
+
+
+def test_noalloc_decode_rejects_plans_beyond_its_scratch():
+    f = _entry()
+    # 1024 x 32 rows, one split (Tk = 1), (128 + 2) floats each: just over 16 MiB
+    w = synth.Workload("dec_oversize", 1024, 32, 32, 1, 1, 128, False, "normal", 22,
+                       decode=True)
+    assert w.B * w.Hq * (w.d + 2) * 4 > _max_bytes()
+    q, k, v = synth.make_inputs(w, "cuda")
+    rc, _, _ = _call(f, q, k, v)
+    assert rc == binding.ATTN_ERR_WORKSPACE
