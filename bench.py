@@ -173,6 +173,27 @@ def cpu_baseline(qp, kp, vp, qd, kd, vd):
     }
 
 
+# ------------------------------------------------------- multi-rank timing
+
+def aggregate_ranks(local: dict, world: int, device) -> dict:
+    """Max over ranks of every timing in `local` (each rank runs a full
+    replica, so the slowest rank bounds the whole job)."""
+    if world == 1:
+        return dict(local)
+    import torch
+    import torch.distributed as dist
+
+    keys = sorted(local)
+    t = torch.tensor([float(local[k]) for k in keys], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return {k: float(x) for k, x in zip(keys, t.tolist())}
+
+
+def whole_job_rate(units_per_rank: float, seconds_max: float, world: int) -> float:
+    """Units processed by all ranks divided by the slowest rank's time."""
+    return world * units_per_rank / seconds_max
+
+
 # ------------------------------------------------------------------ GPU arm
 
 def run_ours(args, rank, world, local_rank):
@@ -267,22 +288,15 @@ def run_ours(args, rank, world, local_rank):
     pre_flops = acct.attention_flops(PREFILL.B, PREFILL.Hq, PREFILL.Tq, PREFILL.Tk, PREFILL.d,
                                      PREFILL.causal)
     dec_bytes = acct.decode_bytes(DECODE.B, DECODE.Hq, DECODE.Hkv, DECODE.Tk, DECODE.d)
-    pre_s = sum(pre_ms) / 1e3
-    dec_s = sum(dec_ms) / 1e3
+    agg = aggregate_ranks(
+        {"pre_s": sum(pre_ms) / 1e3, "dec_s": sum(dec_ms) / 1e3, "total_ms": total_ms,
+         "e2e_pre_ms": e2e_pre_ms, "e2e_dec_ms": e2e_dec_ms},
+        world, dev)
+    pre_s, dec_s, total_ms = agg["pre_s"], agg["dec_s"], agg["total_ms"]
+    e2e_pre_ms, e2e_dec_ms = agg["e2e_pre_ms"], agg["e2e_dec_ms"]
 
-    def max_over_ranks(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        return float(t.item())
-
-    pre_s, dec_s = max_over_ranks(pre_s), max_over_ranks(dec_s)
-    total_ms = max_over_ranks(total_ms)
-    e2e_pre_ms, e2e_dec_ms = max_over_ranks(e2e_pre_ms), max_over_ranks(e2e_dec_ms)
-
-    pre_tflops = world * K * pre_flops / pre_s / 1e12
-    dec_gbs = world * K * dec_bytes / dec_s / 1e9
+    pre_tflops = whole_job_rate(K * pre_flops, pre_s, world) / 1e12
+    dec_gbs = whole_job_rate(K * dec_bytes, dec_s, world) / 1e9
     per_launch_tflops = pre_flops / (pre_s / K) / 1e12
     per_launch_gbs = dec_bytes / (dec_s / K) / 1e9
     peak_tf = peaks["bf16_tflops_sustained"]
@@ -349,12 +363,12 @@ def run_ours(args, rank, world, local_rank):
                                        source_sha(*DECODE_SOURCES)),
                 "algorithmic_bytes_per_launch": dec_bytes,
             },
-            "e2e": {"value": round(world * dec_bytes / (e2e_dec_ms / 1e3) / 1e9, 1),
+            "e2e": {"value": round(whole_job_rate(dec_bytes, e2e_dec_ms / 1e3, world) / 1e9, 1),
                     "unit": "GB/s", "h2d_bytes_per_step": h2d_dec,
                     "d2h_bytes_per_step": d2h_dec},
         },
         "e2e": {
-            "value": round(world * pre_flops / (e2e_pre_ms / 1e3) / 1e12, 2),
+            "value": round(whole_job_rate(pre_flops, e2e_pre_ms / 1e3, world) / 1e12, 2),
             "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d_pre,
             "d2h_bytes_per_step": d2h_pre,

@@ -178,6 +178,8 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS)
   // warp_reduce_scatter32_xor): position j holds head (j / KG) ^ hsel and key
   // (j % KG) ^ ksel.  The query vectors are loaded in that permuted head
   // order, pre-scaled by scale * log2(e) and duplicated into fp32x2 pairs.
+  static_assert(VEC % 2 == 0 || VEC == 1, "head-dim columns per lane");
+  constexpr int VP = (VEC + 1) / 2;  // fp32x2 pairs of head-dim columns
   const int hsel = lane / KG;
   const int ksel = lane % KG;
   float2 qd[GP][VEC];
@@ -196,17 +198,22 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS)
       for (int e = 0; e < VEC; ++e) qd[hp][e] = make_float2(0.f, 0.f);
     }
   }
-  // acc[h][e] for the natural head order, lanes over head-dim columns.
-  float acc[GP][VEC];
+  // Byte offsets of the lane's permuted K rows inside a key group.
+  uint32_t koff[KG];
+#pragma unroll
+  for (int jj = 0; jj < KG; ++jj) koff[jj] = (uint32_t)((jj ^ ksel) * C::ROW_BYTES + lane * VEC * 2);
+  // acc2[h][.] for the natural head order, lanes over head-dim columns.
+  float2 acc2[GP][VP];
 #pragma unroll
   for (int hh = 0; hh < GP; ++hh)
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) acc[hh][e] = 0.f;
-  float m = -INFINITY;  // for head lane / KG
+    for (int e = 0; e < VP; ++e) acc2[hh][e] = make_float2(0.f, 0.f);
+  float m = -INFINITY;  // reference max for head lane / KG (log2 units)
   float l = 0.f;
   bool ok = true;
   float2 *pw = reinterpret_cast<float2 *>(pbuf) + warp * 32;
   float *aw = abuf + warp * GP;
+  constexpr float kRescale = 8.0f;  // lazy rescale threshold, log2 units
 
   for (int t = 0; t < ntiles; ++t) {
     const int s = t % ST, u = t / ST;
@@ -218,78 +225,81 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS)
 #pragma unroll
     for (int gi = warp; gi < C::NGRP; gi += C::CW) {
       const int key0 = gi * KG;
-      // K rows of this group in the lane's permuted key order.
-      float kf[KG][VEC];
+      const uint8_t *kg0 = ks + key0 * C::ROW_BYTES;
+      // ---- scores: fp32x2 over key pairs, then the select-free transpose-add
+      float2 part2[GP * KG / 2];
 #pragma unroll
-      for (int jj = 0; jj < KG; ++jj)
-        load_bf16_row<VEC>(ks + (key0 + (jj ^ ksel)) * C::ROW_BYTES + lane * VEC * 2, kf[jj]);
-      float part[32];
+      for (int jj = 0; jj < KG; jj += 2) {
+        float ka[VEC], kb[VEC];
+        load_bf16_row<VEC>(kg0 + koff[jj], ka);
+        load_bf16_row<VEC>(kg0 + koff[jj + 1], kb);
 #pragma unroll
-      for (int hp = 0; hp < GP; ++hp) {
+        for (int hp = 0; hp < GP; ++hp) {
+          float2 a = __fmul2_rn(qd[hp][0], make_float2(ka[0], kb[0]));
 #pragma unroll
-        for (int jj = 0; jj < KG; jj += 2) {
-          float2 a = make_float2(0.f, 0.f);
-#pragma unroll
-          for (int e = 0; e < VEC; ++e)
-            a = __ffma2_rn(qd[hp][e], make_float2(kf[jj][e], kf[jj + 1][e]), a);
-          part[hp * KG + jj] = a.x;
-          part[hp * KG + jj + 1] = a.y;
+          for (int e = 1; e < VEC; ++e) a = __ffma2_rn(qd[hp][e], make_float2(ka[e], kb[e]), a);
+          part2[(hp * KG + jj) / 2] = a;
         }
       }
-      float sc = warp_reduce_scatter32_xor(part);
-      const bool valid = key0 + ksel < rows_valid;
-      sc = valid ? sc : -INFINITY;
+#pragma unroll
+      for (int off = 8; off >= 1; off >>= 1) {
+#pragma unroll
+        for (int i = 0; i < off; ++i) {
+          const float2 r = make_float2(__shfl_xor_sync(0xffffffffu, part2[i + off].x, 2 * off),
+                                       __shfl_xor_sync(0xffffffffu, part2[i + off].y, 2 * off));
+          part2[i] = __fadd2_rn(part2[i], r);
+        }
+      }
+      float sc = part2[0].x + __shfl_xor_sync(0xffffffffu, part2[0].y, 1);
+      const bool full_group = key0 + KG <= rows_valid;
+      if (!full_group && key0 + ksel >= rows_valid) sc = -INFINITY;
+      // ---- online update per head over its KG lanes
       float mx = sc;
 #pragma unroll
       for (int off = 1; off < KG; off <<= 1)
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-      const float m_new = fmaxf(m, mx);
-      const float alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_new);
-      const float m_ref = (m_new == -INFINITY) ? 0.f : m_new;
+      const bool resc = mx > m + kRescale;  // true on the first group (m = -inf)
+      if (__any_sync(0xffffffffu, resc)) {
+        // move the reference max only where it grew; scale acc and l by alpha
+        const float m_new = resc ? mx : m;
+        const float alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_new);
+        l *= alpha;
+        m = m_new;
+        if (ksel == 0) aw[hsel] = alpha;
+        __syncwarp();
+#pragma unroll
+        for (int hh = 0; hh < GP; ++hh) {
+          const float a = aw[hh];
+#pragma unroll
+          for (int e = 0; e < VP; ++e) acc2[hh][e] = __fmul2_rn(acc2[hh][e], make_float2(a, a));
+        }
+      }
+      const float m_ref = (m == -INFINITY) ? 0.f : m;
       const float pv = ex2_approx(sc - m_ref);
       float ps = pv;
 #pragma unroll
       for (int off = 1; off < KG; off <<= 1)
         ps += __shfl_xor_sync(0xffffffffu, ps, off);
-      l = fmaf(l, alpha, ps);
-      m = m_new;
+      l += ps;
       pw[lane] = make_float2(pv, pv);
-      if (ksel == 0) aw[hsel] = alpha;
       __syncwarp();
-#pragma unroll
-      for (int hh = 0; hh < GP; ++hh) {
-        const float a = aw[hh];
-        if constexpr (VEC % 2 == 0) {
-#pragma unroll
-          for (int e = 0; e < VEC; e += 2) {
-            const float2 y = __fmul2_rn(make_float2(acc[hh][e], acc[hh][e + 1]), make_float2(a, a));
-            acc[hh][e] = y.x;
-            acc[hh][e + 1] = y.y;
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < VEC; ++e) acc[hh][e] *= a;
-        }
-      }
+      // ---- values: lanes over head-dim columns, fp32x2 over column pairs
+      const uint8_t *vg0 = vs + key0 * C::ROW_BYTES + lane * VEC * 2;
+      const int kmax = full_group ? KG : max(0, rows_valid - key0);
 #pragma unroll
       for (int kk = 0; kk < KG; ++kk) {
-        if (key0 + kk < rows_valid) {
+        if (full_group || kk < kmax) {
           float vf[VEC];
-          load_bf16_row<VEC>(vs + (key0 + kk) * C::ROW_BYTES + lane * VEC * 2, vf);
+          load_bf16_row<VEC>(vg0 + kk * C::ROW_BYTES, vf);
 #pragma unroll
           for (int hh = 0; hh < GP; ++hh) {
             const float2 pk = pw[hh * KG + kk];
-            if constexpr (VEC % 2 == 0) {
-#pragma unroll
-              for (int e = 0; e < VEC; e += 2) {
-                const float2 y = __ffma2_rn(pk, make_float2(vf[e], vf[e + 1]),
-                                            make_float2(acc[hh][e], acc[hh][e + 1]));
-                acc[hh][e] = y.x;
-                acc[hh][e + 1] = y.y;
-              }
+            if constexpr (VEC == 1) {
+              acc2[hh][0].x = fmaf(pk.x, vf[0], acc2[hh][0].x);
             } else {
 #pragma unroll
-              for (int e = 0; e < VEC; ++e) acc[hh][e] = fmaf(pk.x, vf[e], acc[hh][e]);
+              for (int e = 0; e < VP; ++e)
+                acc2[hh][e] = __ffma2_rn(pk, make_float2(vf[2 * e], vf[2 * e + 1]), acc2[hh][e]);
             }
           }
         }
@@ -299,6 +309,19 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS)
     if (lane == 0) mbar_arrive(&empty[s]);
   }
   if (!ok) atomicExch(p.status, kDecodeStatusTimeout);
+  float acc[GP][VEC];
+#pragma unroll
+  for (int hh = 0; hh < GP; ++hh) {
+    if constexpr (VEC == 1) {
+      acc[hh][0] = acc2[hh][0].x;
+    } else {
+#pragma unroll
+      for (int e = 0; e < VP; ++e) {
+        acc[hh][2 * e] = acc2[hh][e].x;
+        acc[hh][2 * e + 1] = acc2[hh][e].y;
+      }
+    }
+  }
 
   // ---- merge the consumer warps' states (the K/V ring is free now: every
   // tile was waited for above).
