@@ -1,7 +1,7 @@
 // prefill_kernel.cuh -- exact attention forward on sm_103a tensor cores.
 //
-// One CTA owns two tiles of 128 query rows (256 consecutive rows) of one
-// (batch, head) and streams the K/V tiles of its K/V head past them: the
+// A work item is two tiles of 128 query rows (256 consecutive rows) of one
+// (batch, head); the K/V tiles of its K/V head stream past them: the
 // outer-Q / inner-KV loop order of "4.2 FlashAttention I: IO-Awareness & The
 // Online Softmax", section "FlashAttention forward: tiling + online softmax
 // fused into one pass", and of "Efficient attention & KV cache", section 3.
@@ -12,28 +12,37 @@
 //   m' = max(m, rowmax S_j),  l' = e^(m-m') l + rowsum e^(S_j-m'),
 //   acc' = e^(m-m') acc + e^(S_j-m') V_j,  O = acc / l,  LSE = m + ln l.
 //
-// GB300 mapping (warp-specialised, 320 threads, one CTA per SM):
+// GB300 mapping: a persistent kernel, one CTA of 320 threads per SM.  The
+// producer thread takes work items from a launch-wide atomic counter (so
+// faster CTAs take more of the unequal causal items) and publishes each one
+// to the other roles through a two-entry shared-memory ring.
+// Every role runs ahead into the next item, so one item's tail (last PV,
+// epilogue) overlaps the next item's loads and first products.
 //   warps 0-3, 4-7  two softmax warpgroups, one per query tile t.  Thread r
 //              of group t owns row r of tile t = TMEM lane r.  It reads its
-//              row of S_t from tensor memory, masks, updates (m, l), writes P
-//              as bf16 back into the first 64 columns of S_t's tensor memory,
-//              rescales its row of the O_t accumulator when needed, and at the
-//              end writes O_t (through shared memory and a TMA store) and LSE.
-//   warp 8     TMA producer: both Q tiles once, then K and V tiles into a
-//              ring of STAGES shared-memory slots (swizzled boxes).
+//              row of S_t from tensor memory, masks, updates (m, l), rescales
+//              its row of O_t when needed, and writes P as bf16 back into the
+//              first 64 columns of S_t.  At the end of an item it reads O_t, normalises
+//              and stores its row of O straight to global memory, and LSE.
+//   warp 8     TMA producer: Q tiles (as soon as the previous item's last
+//              S_t no longer needs them) and K and V tiles into a ring of
+//              STAGES shared-memory slots (swizzled boxes), across items.
 //   warp 9     MMA issuer (one thread), tcgen05.mma kind::f16, bf16 operands,
 //              fp32 accumulation in tensor memory:
 //                S_t = Q_t K_j^T    A and B from shared memory,
 //                O_t += P_t V_j     A = P_t from tensor memory, B = V_j.
 //              The two tiles ping-pong: while group 0 turns S_0 into P_0 the
-//              tensor core runs PV_1 and S_1 of the next K tile, and the
-//              other way round, so exponentials and MMAs overlap.
+//              tensor core runs PV_1 and S_1 of the next K tile, and the other
+//              way round, so exponentials and MMAs overlap.
 //
 // Tensor memory (512 columns): S_0 [0,128), S_1 [128,256), O_0 [256,256+D),
-// O_1 [256+D, 256+2D).  P_t aliases S_t: the MMAs of one thread execute in
-// issue order, so S_t(j+1) (issued after PV_t(j)) overwrites P_t(j) only
-// after PV_t(j) has read it, and the commit that signals S_t(j+1) also
-// covers PV_t(j), so a softmax group that sees S_t(j+1) may rescale O_t.
+// O_1 [256+D, 256+2D).  P_t aliases S_t.  The MMAs of one thread execute in
+// issue order, so S_t(j+1) (issued after PV_t(j)) overwrites P_t(j) only after
+// PV_t(j) has read it, and the commit that signals S_t(j+1) also covers
+// PV_t(j), so a softmax group that sees S_t(j+1) may rescale O_t.  Across
+// items, a softmax group reads O_t of item i before it publishes any P_t of
+// item i+1, and the first PV_t of item i+1 (which overwrites O_t) waits for
+// that P_t.
 //
 // Exponentials run in base 2 on scores pre-multiplied by scale*log2(e); m is
 // kept in those units and LSE is converted back to natural log.  The
@@ -45,6 +54,8 @@
 // Causal masking is bottom-right aligned (query i sees keys j <= i + Tk - Tq);
 // K/V tiles wholly above the diagonal are never loaded, and only tiles that
 // cross the diagonal or the ragged end of K are masked element by element.
+// Work items are ordered by groups of heads whose K/V fit in L2, heaviest
+// query tiles first within a group.
 //
 // Every barrier wait is bounded in time; on expiry the kernel records
 // ATTN_ERR_DEVICE_TIMEOUT, stops issuing work, drains its own copies and
@@ -62,11 +73,16 @@ constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 struct PrefillParams {
+  __nv_bfloat16 *o;        // [B, Hq, Tq, D]
   float *lse;              // [B, Hq, Tq]
   unsigned int *status;   // device status word
   int Hq, Hkv, group;     // group = Hq / Hkv
   int Tq, Tk;
   int n_qt;               // ceil(Tq / 256): query-tile pairs per head
+  int n_bh;               // B * Hq
+  int head_group;         // heads per scheduling group (K/V working set in L2)
+  int n_items;            // n_bh * n_qt
+  unsigned int *work;     // {next item, finished CTAs}: zero on entry, zero on exit
   int causal;
   float scale_log2;       // scale * log2(e)
   unsigned long long wait_ns;
@@ -76,7 +92,7 @@ struct PrefillParams {
 template <int D>
 struct PrefillCfg {
   static constexpr int BM = 128;                      // query rows per tile
-  static constexpr int NQ = 2;                        // query tiles per CTA
+  static constexpr int NQ = 2;                        // query tiles per item
   static constexpr int BN = 128;                      // keys per K/V tile
   static constexpr int SPAN = (D >= 64) ? 128 : 64;   // swizzle span, bytes
   static constexpr int CHUNK = SPAN / 2;              // bf16 columns per box
@@ -89,11 +105,11 @@ struct PrefillCfg {
   static constexpr uint32_t OFF_K = OFF_Q + NQ * Q_BYTES;
   static constexpr uint32_t OFF_V = OFF_K + STAGES * KV_BYTES;
   static constexpr uint32_t OFF_BAR = OFF_V + STAGES * KV_BYTES;
-  // q_full, drain, s_full[2], p_full[2], o_done[2], then per stage
-  // k_full, v_full, k_empty, v_empty
-  static constexpr int NBAR = 8 + 4 * STAGES;
+  // drain, q_full[2], q_empty[2], s_full[2], p_full[2], o_done[2],
+  // item_full[2], item_empty[2], then per stage k_full, v_full, k_empty, v_empty
+  static constexpr int NBAR = 15 + 4 * STAGES;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr uint32_t SMEM_USED = OFF_MISC + 16 + 1024;  // + align slack
+  static constexpr uint32_t SMEM_USED = OFF_MISC + 32 + 1024;  // + align slack
   // At least ~116 KB so that only one CTA (which holds all 512 TMEM
   // columns) is resident per SM.
   static constexpr uint32_t SMEM_BYTES = SMEM_USED > 118784u ? SMEM_USED : 118784u;
@@ -108,12 +124,60 @@ struct PrefillCfg {
   static_assert(256 + 2 * D <= 512, "tensor memory budget");
 };
 
+// Geometry of one work item, computed identically by every role.
+struct PrefillItem {
+  int bh, bh_kv, q0;
+  int n0, n1;  // K/V tiles visited by query tile 0 and 1 (0 = tile empty)
+  __device__ __forceinline__ int n(int t) const { return t == 0 ? n0 : n1; }
+  __device__ __forceinline__ int n_max() const { return n0 > n1 ? n0 : n1; }
+};
+
+__device__ __forceinline__ PrefillItem prefill_item(const PrefillParams &p, int idx) {
+  // Heads are taken in groups of head_group; inside a group the heaviest
+  // query-tile pairs of every head come first, so the items in flight share
+  // the K/V of one group in L2 and the light items that end a group fill in.
+  const int per_full = p.head_group * p.n_qt;
+  const int n_full = p.n_bh / p.head_group;
+  int g0, gsize, r;
+  if (idx < n_full * per_full) {
+    g0 = (idx / per_full) * p.head_group;
+    gsize = p.head_group;
+    r = idx % per_full;
+  } else {
+    g0 = n_full * p.head_group;
+    gsize = p.n_bh - g0;
+    r = idx - n_full * per_full;
+  }
+  PrefillItem it;
+  const int qt = p.n_qt - 1 - r / gsize;
+  it.bh = g0 + r % gsize;
+  const int b = it.bh / p.Hq;
+  const int h = it.bh - b * p.Hq;
+  it.bh_kv = b * p.Hkv + h / p.group;
+  it.q0 = qt * 256;
+  const int delta = p.Tk - p.Tq;
+  const int n_kv_all = (p.Tk + 127) / 128;
+  int nt[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int row0 = it.q0 + t * 128;
+    if (row0 >= p.Tq) {
+      nt[t] = 0;
+    } else {
+      const int last_row = min(row0 + 127, p.Tq - 1);
+      nt[t] = p.causal ? min(n_kv_all, (last_row + delta) / 128 + 1) : n_kv_all;
+    }
+  }
+  it.n0 = nt[0];
+  it.n1 = nt[1];
+  return it;
+}
+
 template <int D>
 __global__ void __launch_bounds__(320, 1)
     prefill_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v,
-                       const __grid_constant__ CUtensorMap tm_o,
                        const PrefillParams p) {
   using C = PrefillCfg<D>;
   constexpr int ST = C::STAGES;
@@ -122,47 +186,32 @@ __global__ void __launch_bounds__(320, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
-  uint64_t *q_full = bars + 0, *drain = bars + 1;
-  uint64_t *s_full = bars + 2, *p_full = bars + 4, *o_done = bars + 6;
-  uint64_t *k_full = bars + 8, *v_full = k_full + ST;
+  uint64_t *drain = bars + 0;
+  uint64_t *q_full = bars + 1, *q_empty = bars + 3, *s_full = bars + 5;
+  uint64_t *p_full = bars + 7, *o_done = bars + 9;
+  uint64_t *item_full = bars + 11, *item_empty = bars + 13;
+  uint64_t *k_full = bars + 15, *v_full = k_full + ST;
   uint64_t *k_empty = v_full + ST, *v_empty = k_empty + ST;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+  volatile int *item_ring = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 8);  // [2]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint64_t wait_ns = p.wait_ns;
 
-  // Work item: the heaviest query-tile pairs of a head first, heads in
-  // order, so the CTAs resident at one time share a few heads' K/V in L2.
-  const int bh = blockIdx.x / p.n_qt;
-  const int qt = p.n_qt - 1 - (int)(blockIdx.x % p.n_qt);
-  const int q0 = qt * (C::NQ * C::BM);
-  const int b = bh / p.Hq;
-  const int h = bh - b * p.Hq;
-  const int bh_kv = b * p.Hkv + h / p.group;
-  const int delta = p.Tk - p.Tq;
-  const int n_kv_all = (p.Tk + C::BN - 1) / C::BN;
-  int n_t[C::NQ];
-#pragma unroll
-  for (int t = 0; t < C::NQ; ++t) {
-    const int row0 = q0 + t * C::BM;
-    if (row0 >= p.Tq) {
-      n_t[t] = 0;
-    } else {
-      const int last_row = min(row0 + C::BM - 1, p.Tq - 1);
-      n_t[t] = p.causal ? min(n_kv_all, (last_row + delta) / C::BN + 1) : n_kv_all;
-    }
-  }
-  const int n_max = max(n_t[0], n_t[1]);
-
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
     mbar_init(drain, 1);
     for (int t = 0; t < C::NQ; ++t) {
+      mbar_init(&q_full[t], 1);
+      mbar_init(&q_empty[t], 1);
       mbar_init(&s_full[t], 1);
       mbar_init(&p_full[t], C::BM);
       mbar_init(&o_done[t], 1);
+    }
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(&item_full[k], 1);
+      mbar_init(&item_empty[k], 9);  // 8 softmax warps + the MMA thread
     }
     for (int s = 0; s < ST; ++s) {
       mbar_init(&k_full[s], 1);
@@ -175,7 +224,6 @@ __global__ void __launch_bounds__(320, 1)
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
-    prefetch_tmap(&tm_o);
   }
   if (warp == 0) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -190,6 +238,15 @@ __global__ void __launch_bounds__(320, 1)
     atomicExch(p.status, kStatusTimeout);
     *abort_flag = 1;
   };
+  // Consumers read the next work item index from the producer's ring
+  // (-1 ends the walk).  Returns false if the wait expired.
+  auto take_item = [&](int &fetch, int &idx) -> bool {
+    const int k = fetch & 1;
+    if (!mbar_wait(&item_full[k], (fetch >> 1) & 1, wait_ns)) return false;
+    idx = item_ring[k];
+    ++fetch;
+    return true;
+  };
 
   if (warp == C::PRODUCER_WARP) {
     // ------------------------------------------------------ TMA producer
@@ -197,33 +254,62 @@ __global__ void __launch_bounds__(320, 1)
       bool ok = true;
       int last_k[ST], last_v[ST];
       for (int s = 0; s < ST; ++s) last_k[s] = last_v[s] = -1;
-      mbar_arrive_expect_tx(q_full, C::NQ * C::Q_BYTES);
-      for (int t = 0; t < C::NQ; ++t)
-        for (int c = 0; c < C::NCHUNK; ++c)
-          tma_load_3d(smem + C::OFF_Q + t * C::Q_BYTES + c * (C::BM * C::SPAN), &tm_q,
-                      q_full, c * C::CHUNK, q0 + t * C::BM, bh);
-      for (int j = 0; j < n_max; ++j) {
-        const int s = j % ST, u = j / ST;
-        if (*abort_flag) { ok = false; break; }
-        if (j >= ST && !mbar_wait(&k_empty[s], (u - 1) & 1, wait_ns)) { ok = false; break; }
-        mbar_arrive_expect_tx(&k_full[s], C::KV_BYTES);
-        for (int c = 0; c < C::NCHUNK; ++c)
-          tma_load_3d(smem + C::OFF_K + s * C::KV_BYTES + c * (C::BN * C::SPAN),
-                      &tm_k, &k_full[s], c * C::CHUNK, j * C::BN, bh_kv);
-        last_k[s] = j;
-        if (j >= ST && !mbar_wait(&v_empty[s], (u - 1) & 1, wait_ns)) { ok = false; break; }
-        if (!(p.inject == 1 && j == 0)) {
-          mbar_arrive_expect_tx(&v_full[s], C::KV_BYTES);
-          for (int c = 0; c < C::NCHUNK; ++c)
-            tma_load_3d(smem + C::OFF_V + s * C::KV_BYTES + c * (C::BN * C::SPAN),
-                        &tm_v, &v_full[s], c * C::CHUNK, j * C::BN, bh_kv);
-          last_v[s] = j;
+      int q_cnt[C::NQ] = {0, 0};
+      int kv = 0;  // K/V tiles issued so far (all items)
+      bool first = true;
+      for (int fetch = 0; ok; ++fetch) {
+        // Take the next work item from the launch-wide counter and publish
+        // it to the other roles through a two-entry ring.
+        const int k = fetch & 1;
+        if (fetch >= 2 && !mbar_wait(&item_empty[k], ((fetch >> 1) - 1) & 1, wait_ns)) {
+          ok = false;
+          break;
         }
+        int idx = (int)atomicAdd(&p.work[0], 1u);
+        if (idx >= p.n_items) idx = -1;
+        item_ring[k] = idx;
+        mbar_arrive(&item_full[k]);
+        if (idx < 0) break;
+        const PrefillItem it = prefill_item(p, idx);
+        for (int t = 0; t < C::NQ && ok; ++t) {
+          if (it.n(t) == 0) continue;
+          // Q_t is free once the previous item's last S_t has completed.
+          if (q_cnt[t] > 0 && !mbar_wait(&q_empty[t], (q_cnt[t] - 1) & 1, wait_ns)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&q_full[t], C::Q_BYTES);
+          for (int c = 0; c < C::NCHUNK; ++c)
+            tma_load_3d(smem + C::OFF_Q + t * C::Q_BYTES + c * (C::BM * C::SPAN), &tm_q,
+                        &q_full[t], c * C::CHUNK, it.q0 + t * C::BM, it.bh);
+          ++q_cnt[t];
+        }
+        const int nmax = it.n_max();
+        for (int j = 0; ok && j < nmax; ++j, ++kv) {
+          const int s = kv % ST, u = kv / ST;
+          if (*abort_flag) { ok = false; break; }
+          if (kv >= ST && !mbar_wait(&k_empty[s], (u - 1) & 1, wait_ns)) { ok = false; break; }
+          mbar_arrive_expect_tx(&k_full[s], C::KV_BYTES);
+          for (int c = 0; c < C::NCHUNK; ++c)
+            tma_load_3d(smem + C::OFF_K + s * C::KV_BYTES + c * (C::BN * C::SPAN),
+                        &tm_k, &k_full[s], c * C::CHUNK, j * C::BN, it.bh_kv);
+          last_k[s] = kv;
+          if (kv >= ST && !mbar_wait(&v_empty[s], (u - 1) & 1, wait_ns)) { ok = false; break; }
+          if (!(p.inject == 1 && first && j == 0)) {
+            mbar_arrive_expect_tx(&v_full[s], C::KV_BYTES);
+            for (int c = 0; c < C::NCHUNK; ++c)
+              tma_load_3d(smem + C::OFF_V + s * C::KV_BYTES + c * (C::BN * C::SPAN),
+                          &tm_v, &v_full[s], c * C::CHUNK, j * C::BN, it.bh_kv);
+            last_v[s] = kv;
+          }
+        }
+        first = false;
       }
       if (!ok) fail();
       // Drain: every copy this thread issued has landed before the CTA's
       // shared memory can be released.
-      mbar_wait(q_full, 0, wait_ns);
+      for (int t = 0; t < C::NQ; ++t)
+        if (q_cnt[t] > 0) mbar_wait(&q_full[t], (q_cnt[t] - 1) & 1, wait_ns);
       for (int s = 0; s < ST; ++s) {
         if (last_k[s] >= 0) mbar_wait(&k_full[s], (last_k[s] / ST) & 1, wait_ns);
         if (last_v[s] >= 0) mbar_wait(&v_full[s], (last_v[s] / ST) & 1, wait_ns);
@@ -232,76 +318,104 @@ __global__ void __launch_bounds__(320, 1)
     __syncwarp();
   } else if (warp == C::MMA_WARP) {
     // ------------------------------------------------------- MMA issuer
+    // The tensor core's instruction queue is short, so every instruction this
+    // thread runs between MMAs can leave it idle: descriptors are built once
+    // and advanced by compile-time byte offsets (the start address sits in
+    // the low bits in 16-byte units), the two tiles are unrolled, and only
+    // waits on barriers that other threads' tensor-memory writes complete are
+    // followed by a tcgen05 fence.
     if (lane == 0) {
       constexpr uint32_t IDESC_QK = make_idesc_bf16(C::BM, C::BN, false);
       constexpr uint32_t IDESC_PV = make_idesc_bf16(C::BM, D, true);
-      auto issue_s = [&](int t, int s) {
+      const uint64_t q_desc = make_smem_desc(sbase + C::OFF_Q, 16, 8 * C::SPAN, C::LAYOUT);
+      const uint64_t k_desc = make_smem_desc(sbase + C::OFF_K, 16, 8 * C::SPAN, C::LAYOUT);
+      // V as B of P V: MN-major, LBO = next CHUNK head-dim columns, SBO = next 8 keys
+      const uint64_t v_desc =
+          make_smem_desc(sbase + C::OFF_V, C::BN * C::SPAN, 8 * C::SPAN, C::LAYOUT);
+      auto adv = [](uint64_t desc, uint32_t bytes) { return desc + (uint64_t)(bytes >> 4); };
+      auto issue_s = [&](const int t, const int s) {
+        const uint64_t kd = adv(k_desc, s * C::KV_BYTES);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const int c = (kk * 16) / C::CHUNK;
-          const int inner = ((kk * 16) % C::CHUNK) * 2;
-          const uint64_t ad = make_smem_desc(
-              sbase + C::OFF_Q + t * C::Q_BYTES + c * (C::BM * C::SPAN) + inner, 16,
-              8 * C::SPAN, C::LAYOUT);
-          const uint64_t bd = make_smem_desc(
-              sbase + C::OFF_K + s * C::KV_BYTES + c * (C::BN * C::SPAN) + inner, 16,
-              8 * C::SPAN, C::LAYOUT);
-          mma_bf16_ss(tmem + C::tm_s(t), ad, bd, IDESC_QK, kk > 0 ? 1u : 0u);
+          const uint32_t off = ((kk * 16) / C::CHUNK) * (C::BM * C::SPAN) + ((kk * 16) % C::CHUNK) * 2;
+          mma_bf16_ss(tmem + C::tm_s(t), adv(q_desc, t * C::Q_BYTES + off), adv(kd, off),
+                      IDESC_QK, kk > 0 ? 1u : 0u);
         }
       };
-      auto issue_pv = [&](int t, int s, bool acc) {
+      auto issue_pv = [&](const int t, const int s, const bool acc) {
+        const uint64_t vd = adv(v_desc, s * C::KV_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < C::BN / 16; ++kk) {
-          // A = P_t in tensor memory: 16 keys = 8 columns of bf16 pairs.
-          // B = V tile, MN-major (d contiguous): 16 keys = 16 rows per step,
-          // LBO = next group of CHUNK head-dim columns, SBO = next 8 keys.
-          const uint64_t bd = make_smem_desc(
-              sbase + C::OFF_V + s * C::KV_BYTES + kk * 16 * C::SPAN, C::BN * C::SPAN,
-              8 * C::SPAN, C::LAYOUT);
-          mma_bf16_ts(tmem + C::tm_o(t), tmem + C::tm_s(t) + kk * 8, bd, IDESC_PV,
-                      (acc || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < C::BN / 16; ++kk)  // 16 keys = 8 TMEM columns of P
+          mma_bf16_ts(tmem + C::tm_o(t), tmem + C::tm_s(t) + kk * 8, adv(vd, kk * 16 * C::SPAN),
+                      IDESC_PV, (acc || kk > 0) ? 1u : 0u);
       };
-      bool ok = mbar_wait(q_full, 0, wait_ns) && mbar_wait(&k_full[0], 0, wait_ns);
-      if (ok && n_max > 0) {
-        tc_fence_after();
-        for (int t = 0; t < C::NQ; ++t) {
-          if (n_t[t] > 0) {
-            issue_s(t, 0);
-            mma_commit(&s_full[t]);
+      bool ok = true;
+      int q_cnt0 = 0, q_cnt1 = 0;  // Q_t tiles consumed
+      int p_cnt0 = 0, p_cnt1 = 0;  // P_t tiles consumed
+      int kv = 0;                  // K/V tiles consumed (all items)
+      for (int fetch = 0; ok;) {
+        int idx = -1;
+        if (!take_item(fetch, idx)) { ok = false; break; }
+        mbar_arrive(&item_empty[(fetch - 1) & 1]);
+        if (idx < 0) break;
+        const PrefillItem it = prefill_item(p, idx);
+        const int nmax = it.n_max();
+        {
+          // First S of both tiles, on K/V tile 0 of this item.
+          const int s0 = kv % ST;
+          if (*abort_flag || !mbar_wait(&k_full[s0], (kv / ST) & 1, wait_ns)) { ok = false; break; }
+          if (it.n0 > 0) {
+            if (!mbar_wait(&q_full[0], q_cnt0 & 1, wait_ns)) { ok = false; break; }
+            ++q_cnt0;
+            issue_s(0, s0);
+            mma_commit(&s_full[0]);
+            if (it.n0 == 1) mma_commit(&q_empty[0]);
           }
+          if (it.n1 > 0) {
+            if (!mbar_wait(&q_full[1], q_cnt1 & 1, wait_ns)) { ok = false; break; }
+            ++q_cnt1;
+            issue_s(1, s0);
+            mma_commit(&s_full[1]);
+            if (it.n1 == 1) mma_commit(&q_empty[1]);
+          }
+          mma_commit(&k_empty[s0]);
         }
-        mma_commit(&k_empty[0]);
-      }
-      for (int j = 0; ok && j < n_max; ++j) {
-        const int s = j % ST, u = j / ST;
-        const int s1 = (j + 1) % ST, u1 = (j + 1) / ST;
-        if (*abort_flag) { ok = false; break; }
-        bool v_ready = false, k_ready = false;
-        for (int t = 0; t < C::NQ && ok; ++t) {
-          if (j >= n_t[t]) continue;
-          if (!mbar_wait(&p_full[t], j & 1, wait_ns)) { ok = false; break; }
-          if (!v_ready) {
-            if (!mbar_wait(&v_full[s], u & 1, wait_ns)) { ok = false; break; }
-            v_ready = true;
-          }
-          tc_fence_after();
-          issue_pv(t, s, j > 0);
-          if (j + 1 < n_t[t]) {
-            if (!k_ready) {
-              if (!mbar_wait(&k_full[s1], u1 & 1, wait_ns)) { ok = false; break; }
-              k_ready = true;
-              tc_fence_after();
+        for (int j = 0; j < nmax; ++j) {
+          const int s = (kv + j) % ST, u = (kv + j) / ST;
+          const int s1 = (kv + j + 1) % ST, u1 = (kv + j + 1) / ST;
+          bool v_ready = false, k_ready = false;
+          // One query tile: P_t V_j, then S_t of the next K/V tile.
+          auto tile_step = [&](const int t, int &p_cnt, const int nt) -> bool {
+            if (j >= nt) return true;
+            if (!mbar_wait(&p_full[t], p_cnt & 1, wait_ns)) return false;
+            ++p_cnt;
+            if (!v_ready) {
+              if (!mbar_wait(&v_full[s], u & 1, wait_ns)) return false;
+              v_ready = true;
             }
-            issue_s(t, s1);
-            mma_commit(&s_full[t]);
-          } else {
-            mma_commit(&o_done[t]);
+            tc_fence_after();  // P_t was written to tensor memory by the softmax threads
+            issue_pv(t, s, j > 0);
+            if (j + 1 < nt) {
+              if (!k_ready) {
+                if (!mbar_wait(&k_full[s1], u1 & 1, wait_ns)) return false;
+                k_ready = true;
+              }
+              issue_s(t, s1);
+              mma_commit(&s_full[t]);
+              if (j + 2 == nt) mma_commit(&q_empty[t]);  // last S_t of the item
+            } else {
+              mma_commit(&o_done[t]);
+            }
+            return true;
+          };
+          if (*abort_flag || !tile_step(0, p_cnt0, it.n0) || !tile_step(1, p_cnt1, it.n1)) {
+            ok = false;
+            break;
           }
+          mma_commit(&v_empty[s]);
+          if (k_ready) mma_commit(&k_empty[s1]);
         }
-        if (!ok) break;
-        mma_commit(&v_empty[s]);
-        if (k_ready) mma_commit(&k_empty[s1]);
+        kv += nmax;
       }
       if (!ok) fail();
       // Drain: all MMAs issued by this thread have completed before tensor
@@ -317,147 +431,147 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t t_s = tmem + lane_base + C::tm_s(t);
     const uint32_t t_o = tmem + lane_base + C::tm_o(t);
-    const int row0 = q0 + t * C::BM;
-    const int row_g = row0 + r;
-    const int lim = p.causal ? row_g + delta : 0x7fffffff;
     const float sl2 = p.scale_log2;
-    const int n = n_t[t];
-    float m_used = -INFINITY;  // reference max, log2 units
-    float l_sum = 0.f;
+    const int delta = p.Tk - p.Tq;
+    int s_cnt = 0;  // S_t tiles consumed (all items)
+    int o_cnt = 0;  // O_t tiles finished (all items)
     bool ok = true;
 
-    for (int j = 0; j < n; ++j) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t], j & 1, wait_ns) && !*abort_flag);
+    for (int fetch = 0; ok;) {
+      int idx = -1;
+      ok = __all_sync(0xffffffffu, take_item(fetch, idx));
       if (!ok) break;
-      tc_fence_after();
-      float s[C::BN];
-      tmem_ld128_wait(t_s, s);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&item_empty[(fetch - 1) & 1]);
+      if (idx < 0) break;
+      const PrefillItem it = prefill_item(p, idx);
+      const int n = it.n(t);
+      if (n == 0) continue;
+      const int row0 = it.q0 + t * C::BM;
+      const int row_g = row0 + r;
+      const int lim = p.causal ? row_g + delta : 0x7fffffff;
+      float m_used = -INFINITY;  // reference max, log2 units
+      float l_sum = 0.f;
 
-      const int kbase = j * C::BN;
-      const bool need_mask =
-          (kbase + C::BN > p.Tk) || (p.causal && kbase + C::BN - 1 > row0 + delta);
-      if (need_mask) {
-#pragma unroll
-        for (int c = 0; c < C::BN; ++c) {
-          const int key = kbase + c;
-          if (key > lim || key >= p.Tk) s[c] = -INFINITY;
-        }
-      }
-      float mx[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = s[i];
-#pragma unroll
-      for (int c = 8; c < C::BN; c += 8)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], s[c + i]);
-      const float mxa = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                              fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      const float m_tile = mxa * sl2;  // scale > 0, so the max commutes
-      const float m_new = fmaxf(m_used, m_tile);
-      const bool resc = m_new > m_used + kRescaleLog2;
-      float alpha = 1.f;
-      if (resc) {
-        alpha = ex2_approx(m_used - m_new);  // 0 while nothing was seen
-        m_used = m_new;
-      }
-      const float m_ref = (m_used == -INFINITY) ? 0.f : m_used;
-      const float2 c2 = make_float2(sl2, sl2);
-      const float2 b2 = make_float2(-m_ref, -m_ref);
-      float2 acc2[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) acc2[i] = make_float2(0.f, 0.f);
-      uint32_t pw[C::BN / 2];
-#pragma unroll
-      for (int c = 0; c < C::BN / 2; ++c) {
-        const float2 x = __ffma2_rn(make_float2(s[2 * c], s[2 * c + 1]), c2, b2);
-        const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-        acc2[c & 3] = __fadd2_rn(acc2[c & 3], e);
-        pw[c] = pack_bf16x2(e.x, e.y);
-      }
-      const float2 a01 = __fadd2_rn(acc2[0], acc2[1]);
-      const float2 a23 = __fadd2_rn(acc2[2], acc2[3]);
-      const float2 a = __fadd2_rn(a01, a23);
-      l_sum = fmaf(l_sum, alpha, a.x + a.y);
-
-      // O_t is stable here (PV_t(j-1) completed before S_t(j) was signalled).
-      if (j > 0 && __any_sync(0xffffffffu, resc)) {
-        const float2 al2 = make_float2(alpha, alpha);
-#pragma unroll
-        for (int cb = 0; cb < D / 32; ++cb) {
-          float o[32];
-          tmem_ld32_wait(t_o + cb * 32, o);
-          uint32_t ow[32];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float2 y = __fmul2_rn(make_float2(o[2 * i], o[2 * i + 1]), al2);
-            ow[2 * i] = __float_as_uint(y.x);
-            ow[2 * i + 1] = __float_as_uint(y.y);
-          }
-          tmem_st32(t_o + cb * 32, ow);
-        }
-      }
-      // P_t (bf16 pairs) into the first 64 columns of S_t.
-      {
-        uint32_t w0[32], w1[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          w0[i] = pw[i];
-          w1[i] = pw[32 + i];
-        }
-        tmem_st32(t_s, w0);
-        tmem_st32(t_s + 32, w1);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&p_full[t]);
-    }
-
-    // ------------------------------------------------------------ epilogue
-    uint8_t *stage = smem + C::OFF_Q + t * C::Q_BYTES;  // Q_t is no longer read
-    if (n > 0) {
-      if (ok)
-        ok = __all_sync(0xffffffffu, mbar_wait(&o_done[t], 0, wait_ns));
-      if (ok) {
+      for (int j = 0; j < n; ++j) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t], s_cnt & 1, wait_ns) && !*abort_flag);
+        if (!ok) break;
+        ++s_cnt;
         tc_fence_after();
-        const float inv_l = (l_sum > 0.f) ? 1.f / l_sum : 0.f;
+        float s[C::BN];
+        tmem_ld128_wait(t_s, s);
+
+        const int kbase = j * C::BN;
+        const bool need_mask =
+            (kbase + C::BN > p.Tk) || (p.causal && kbase + C::BN - 1 > row0 + delta);
+        if (need_mask) {
 #pragma unroll
-        for (int cb = 0; cb < D / 32; ++cb) {
-          float o[32];
-          tmem_ld32_wait(t_o + cb * 32, o);
-#pragma unroll
-          for (int u4 = 0; u4 < 4; ++u4) {
-            uint4 w;
-            w.x = pack_bf16x2(o[u4 * 8 + 0] * inv_l, o[u4 * 8 + 1] * inv_l);
-            w.y = pack_bf16x2(o[u4 * 8 + 2] * inv_l, o[u4 * 8 + 3] * inv_l);
-            w.z = pack_bf16x2(o[u4 * 8 + 4] * inv_l, o[u4 * 8 + 5] * inv_l);
-            w.w = pack_bf16x2(o[u4 * 8 + 6] * inv_l, o[u4 * 8 + 7] * inv_l);
-            const int col = cb * 32 + u4 * 8;
-            const int c = col / C::CHUNK;
-            const uint32_t off = c * (C::BM * C::SPAN) +
-                                 swizzle_off(r * C::SPAN + (col % C::CHUNK) * 2, C::SPAN);
-            *reinterpret_cast<uint4 *>(stage + off) = w;
+          for (int c = 0; c < C::BN; ++c) {
+            const int key = kbase + c;
+            if (key > lim || key >= p.Tk) s[c] = -INFINITY;
           }
         }
-        if (row_g < p.Tq) {
-          float lse;
-          if (l_sum > 0.f)
-            lse = (m_used + log2f(l_sum)) * kLn2;
-          else
-            lse = (m_used == -INFINITY) ? 0.f : m_used * kLn2;
-          p.lse[(size_t)bh * p.Tq + row_g] = lse;
+        float mx[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = s[i];
+#pragma unroll
+        for (int c = 8; c < C::BN; c += 8)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mx[i] = fmaxf(mx[i], s[c + i]);
+        const float mxa = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        const float m_tile = mxa * sl2;  // scale > 0, so the max commutes
+        const float m_new = fmaxf(m_used, m_tile);
+        const bool resc = m_new > m_used + kRescaleLog2;
+        float alpha = 1.f;
+        if (resc) {
+          alpha = ex2_approx(m_used - m_new);  // 0 while nothing was seen
+          m_used = m_new;
         }
-      } else {
-        fail();
+        // O_t is stable here (PV_t(j-1) completed before S_t(j) was signalled):
+        // rescale it before any of P_t(j) is published.
+        if (j > 0 && __any_sync(0xffffffffu, resc)) {
+          const float2 al2 = make_float2(alpha, alpha);
+#pragma unroll
+          for (int cb = 0; cb < D / 32; ++cb) {
+            float o[32];
+            tmem_ld32_wait(t_o + cb * 32, o);
+            uint32_t ow[32];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float2 y = __fmul2_rn(make_float2(o[2 * i], o[2 * i + 1]), al2);
+              ow[2 * i] = __float_as_uint(y.x);
+              ow[2 * i + 1] = __float_as_uint(y.y);
+            }
+            tmem_st32(t_o + cb * 32, ow);
+          }
+          tmem_st_wait();
+        }
+        const float m_ref = (m_used == -INFINITY) ? 0.f : m_used;
+        const float2 c2 = make_float2(sl2, sl2);
+        const float2 b2 = make_float2(-m_ref, -m_ref);
+        float2 acc2[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc2[i] = make_float2(0.f, 0.f);
+        {
+          uint32_t pw[C::BN / 2];
+#pragma unroll
+          for (int c = 0; c < C::BN / 2; ++c) {
+            const float2 x = __ffma2_rn(make_float2(s[2 * c], s[2 * c + 1]), c2, b2);
+            const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            acc2[c & 3] = __fadd2_rn(acc2[c & 3], e);
+            pw[c] = pack_bf16x2(e.x, e.y);
+          }
+          tmem_st32(t_s, *reinterpret_cast<const uint32_t(*)[32]>(&pw[0]));
+          tmem_st32(t_s + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pw[32]));
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(&p_full[t]);
+        }
+        const float2 a01 = __fadd2_rn(acc2[0], acc2[1]);
+        const float2 a23 = __fadd2_rn(acc2[2], acc2[3]);
+        const float2 a = __fadd2_rn(a01, a23);
+        l_sum = fmaf(l_sum, alpha, a.x + a.y);
       }
-      fence_proxy_async_smem();
-      named_barrier_sync(1 + t, C::BM);
-      if (r == 0 && !*abort_flag) {
-        for (int c = 0; c < C::NCHUNK; ++c)
-          tma_store_3d(&tm_o, stage + c * (C::BM * C::SPAN), c * C::CHUNK, row0, bh);
-        bulk_commit_group();
-        bulk_wait_group_read0();
+      if (!ok) break;
+
+      // ---------------------------------------------------------- epilogue
+      ok = __all_sync(0xffffffffu, mbar_wait(&o_done[t], o_cnt & 1, wait_ns));
+      if (!ok) break;
+      ++o_cnt;
+      tc_fence_after();
+      const float inv_l = (l_sum > 0.f) ? 1.f / l_sum : 0.f;
+      uint4 packed[D / 8];
+#pragma unroll
+      for (int cb = 0; cb < D / 32; ++cb) {
+        float o[32];
+        tmem_ld32_wait(t_o + cb * 32, o);
+#pragma unroll
+        for (int u4 = 0; u4 < 4; ++u4) {
+          uint4 w;
+          w.x = pack_bf16x2(o[u4 * 8 + 0] * inv_l, o[u4 * 8 + 1] * inv_l);
+          w.y = pack_bf16x2(o[u4 * 8 + 2] * inv_l, o[u4 * 8 + 3] * inv_l);
+          w.z = pack_bf16x2(o[u4 * 8 + 4] * inv_l, o[u4 * 8 + 5] * inv_l);
+          w.w = pack_bf16x2(o[u4 * 8 + 6] * inv_l, o[u4 * 8 + 7] * inv_l);
+          packed[cb * 4 + u4] = w;
+        }
+      }
+      // O_t has been read: the next item's first PV_t may overwrite it (it
+      // waits for this group's next P_t, published after this fence).
+      tc_fence_before();
+      if (row_g < p.Tq) {
+        uint4 *orow = reinterpret_cast<uint4 *>(p.o + ((size_t)it.bh * p.Tq + row_g) * D);
+#pragma unroll
+        for (int i = 0; i < D / 8; ++i) orow[i] = packed[i];
+        float lse;
+        if (l_sum > 0.f)
+          lse = (m_used + log2f(l_sum)) * kLn2;
+        else
+          lse = (m_used == -INFINITY) ? 0.f : m_used * kLn2;
+        p.lse[(size_t)it.bh * p.Tq + row_g] = lse;
       }
     }
+    if (!ok) fail();
   }
 
   tc_fence_before();
@@ -465,6 +579,16 @@ __global__ void __launch_bounds__(320, 1)
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+  if (threadIdx.x == 0) {
+    // Every producer of this launch has stopped fetching once all CTAs have
+    // arrived here, so the last CTA resets the counters for the next launch.
+    __threadfence();
+    if (atomicAdd(&p.work[1], 1u) == gridDim.x - 1) {
+      atomicExch(&p.work[0], 0u);
+      atomicExch(&p.work[1], 0u);
+      __threadfence();
+    }
   }
 }
 
