@@ -489,21 +489,22 @@ __global__ void __launch_bounds__(320, 1)
           m_used = m_new;
         }
         // O_t is stable here (PV_t(j-1) completed before S_t(j) was signalled):
-        // rescale it before any of P_t(j) is published.
+        // rescale it before any of P_t(j) is published.  Chunks of 16 columns
+        // keep the registers this rare path needs small next to the S row.
         if (j > 0 && __any_sync(0xffffffffu, resc)) {
           const float2 al2 = make_float2(alpha, alpha);
+#pragma unroll 1
+          for (int cb = 0; cb < D / 16; ++cb) {
+            float o[16];
+            tmem_ld16_wait(t_o + cb * 16, o);
+            uint32_t ow[16];
 #pragma unroll
-          for (int cb = 0; cb < D / 32; ++cb) {
-            float o[32];
-            tmem_ld32_wait(t_o + cb * 32, o);
-            uint32_t ow[32];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
+            for (int i = 0; i < 8; ++i) {
               const float2 y = __fmul2_rn(make_float2(o[2 * i], o[2 * i + 1]), al2);
               ow[2 * i] = __float_as_uint(y.x);
               ow[2 * i + 1] = __float_as_uint(y.y);
             }
-            tmem_st32(t_o + cb * 32, ow);
+            tmem_st16(t_o + cb * 16, ow);
           }
           tmem_st_wait();
         }
@@ -513,21 +514,25 @@ __global__ void __launch_bounds__(320, 1)
         float2 acc2[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc2[i] = make_float2(0.f, 0.f);
-        {
-          uint32_t pw[C::BN / 2];
+        // P_t as bf16 pairs into the first 64 columns of S_t (whose scores
+        // are all in registers already), stored 16 columns (32 keys) at a
+        // time as they are produced so the packed row never lives whole.
 #pragma unroll
-          for (int c = 0; c < C::BN / 2; ++c) {
-            const float2 x = __ffma2_rn(make_float2(s[2 * c], s[2 * c + 1]), c2, b2);
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t pw[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const int cc = q4 * 16 + c;
+            const float2 x = __ffma2_rn(make_float2(s[2 * cc], s[2 * cc + 1]), c2, b2);
             const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
             acc2[c & 3] = __fadd2_rn(acc2[c & 3], e);
             pw[c] = pack_bf16x2(e.x, e.y);
           }
-          tmem_st32(t_s, *reinterpret_cast<const uint32_t(*)[32]>(&pw[0]));
-          tmem_st32(t_s + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pw[32]));
-          tmem_st_wait();
-          tc_fence_before();
-          mbar_arrive(&p_full[t]);
+          tmem_st16(t_s + q4 * 16, pw);
         }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&p_full[t]);
         const float2 a01 = __fadd2_rn(acc2[0], acc2[1]);
         const float2 a23 = __fadd2_rn(acc2[2], acc2[3]);
         const float2 a = __fadd2_rn(a01, a23);
