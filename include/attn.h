@@ -85,6 +85,23 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
              float scale, void *stream);
 
 /*
+ * attn_fwd_window -- causal sliding-window forward pass.
+ *
+ * As attn_fwd with the causal mask, and each query additionally sees only the
+ * `window` most recent keys: query row i (at key position p = i + Tk - Tq)
+ * attends to keys j with p - window < j <= p ("4.2 FlashAttention I",
+ * Exercise 4: i - W < j <= i; "Efficient attention & KV cache", exercise 2).
+ * K/V tiles that lie wholly outside every row's window are never loaded.
+ *   window    number of keys each query sees (>= 1; window >= Tk is plain
+ *             causal attention)
+ * Other arguments, layouts and errors are those of attn_fwd; Tq > Tk and
+ * window < 1 return ATTN_ERR_INVALID_ARG.
+ */
+int attn_fwd_window(const void *q, const void *k, const void *v, void *o, float *lse,
+                    int B, int Hq, int Hkv, int Tq, int Tk, int d, int window,
+                    float scale, void *stream);
+
+/*
  * attn_decode_workspace_bytes -- scratch needed by attn_decode.
  *
  * Depends only on the sizes (not on the GPU), so it may be called before any

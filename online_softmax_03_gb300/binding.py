@@ -50,6 +50,8 @@ def load_library():
             vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
             lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
             lib.attn_fwd.restype = i
+            lib.attn_fwd_window.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
+            lib.attn_fwd_window.restype = i
             lib.attn_decode_workspace_bytes.argtypes = [i, i, i, i, i]
             lib.attn_decode_workspace_bytes.restype = ctypes.c_size_t
             lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp,
@@ -70,6 +72,11 @@ def load_library():
 def attn_fwd(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, causal, scale, stream) -> int:
     return load_library().attn_fwd(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, causal,
                                    scale, stream)
+
+
+def attn_fwd_window(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, window, scale, stream) -> int:
+    return load_library().attn_fwd_window(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, window,
+                                          scale, stream)
 
 
 def attn_decode_workspace_bytes(B, Hq, Hkv, Tk, d) -> int:
@@ -121,8 +128,10 @@ def _stream_handle(stream):
 
 
 def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None,
-        lse=None, stream=None):
-    """O, LSE = attention(q [B,Hq,Tq,d], k/v [B,Hkv,Tk,d]) through attn_fwd."""
+        lse=None, stream=None, window: int | None = None):
+    """O, LSE = attention(q [B,Hq,Tq,d], k/v [B,Hkv,Tk,d]) through attn_fwd, or
+    through attn_fwd_window (causal, `window` most recent keys) if window is
+    given."""
     import torch
 
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
@@ -135,11 +144,18 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None,
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, Hq, Tq), dtype=torch.float32, device=q.device)
-    rc = attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                  B, Hq, Hkv, Tq, Tk, d, int(bool(causal)),
-                  0.0 if scale is None else float(scale), _stream_handle(stream))
+    sc = 0.0 if scale is None else float(scale)
+    if window is None:
+        rc = attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                      B, Hq, Hkv, Tq, Tk, d, int(bool(causal)), sc, _stream_handle(stream))
+        where = "attn_fwd"
+    else:
+        rc = attn_fwd_window(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                             lse.data_ptr(), B, Hq, Hkv, Tq, Tk, d, int(window), sc,
+                             _stream_handle(stream))
+        where = "attn_fwd_window"
     if rc != ATTN_OK:
-        raise AttnError(rc, "attn_fwd")
+        raise AttnError(rc, where)
     return out, lse
 
 

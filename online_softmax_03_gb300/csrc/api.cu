@@ -99,9 +99,10 @@ int validate_decode_args(const void *q, const void *k, const void *v, const void
 
 }  // namespace attn_host
 
-ATTN_API int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
-                      int B, int Hq, int Hkv, int Tq, int Tk, int d, int causal,
-                      float scale, void *stream) {
+namespace {
+int fwd_common(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq,
+               int Hkv, int Tq, int Tk, int d, int causal, int window, float scale,
+               void *stream) {
   float sc = 0.f;
   int rc = validate(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, causal, scale, &sc);
   if (rc != ATTN_OK) return rc;
@@ -120,11 +121,26 @@ ATTN_API int attn_fwd(const void *q, const void *k, const void *v, void *o, floa
   a.Tk = Tk;
   a.d = d;
   a.causal = causal;
+  a.window = window;
   a.scale = sc;
   a.stream = static_cast<cudaStream_t>(stream);
   a.wait_ns = g_wait_ns.load();
   a.inject = g_inject.load();
   return attn_host::prefill_launch(a);
+}
+}  // namespace
+
+ATTN_API int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                      int B, int Hq, int Hkv, int Tq, int Tk, int d, int causal,
+                      float scale, void *stream) {
+  return fwd_common(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, causal, 0, scale, stream);
+}
+
+ATTN_API int attn_fwd_window(const void *q, const void *k, const void *v, void *o,
+                             float *lse, int B, int Hq, int Hkv, int Tq, int Tk, int d,
+                             int window, float scale, void *stream) {
+  if (window < 1) return ATTN_ERR_INVALID_ARG;
+  return fwd_common(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, 1, window, scale, stream);
 }
 
 ATTN_API size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Tk, int d) {

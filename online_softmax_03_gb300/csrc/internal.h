@@ -13,6 +13,7 @@ struct PrefillArgs {
   void *o;
   float *lse;
   int B, Hq, Hkv, Tq, Tk, d, causal;
+  int window;  // > 0: causal sliding window of this many keys (0 = none)
   float scale;
   cudaStream_t stream;
   unsigned long long wait_ns;

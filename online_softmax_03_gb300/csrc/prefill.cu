@@ -18,7 +18,7 @@ constexpr int kWorkSlots = 64;
 __device__ unsigned int g_prefill_work[2 * kWorkSlots];
 std::atomic<unsigned int> g_launch_seq{0};
 
-template <int D>
+template <int D, bool kWindow>
 int launch_d(const attn_host::PrefillArgs &a, unsigned int *status, unsigned int *work,
              int sms) {
   using C = attn_dev::PrefillCfg<D>;
@@ -50,6 +50,7 @@ int launch_d(const attn_host::PrefillArgs &a, unsigned int *status, unsigned int
     p.head_group = (int)g;
   }
   p.causal = a.causal;
+  p.window = a.window;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.wait_ns = a.wait_ns;
   p.inject = a.inject;
@@ -60,7 +61,7 @@ int launch_d(const attn_host::PrefillArgs &a, unsigned int *status, unsigned int
   // Persistent: one CTA per SM (each holds all of an SM's tensor memory);
   // CTAs take work items from the slot's counter until the list is done.
   const uint64_t grid = items < (uint64_t)sms ? items : (uint64_t)sms;
-  auto kern = attn_dev::prefill_fwd_kernel<D>;
+  auto kern = attn_dev::prefill_fwd_kernel<D, kWindow>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)C::SMEM_BYTES) != cudaSuccess)
     return ATTN_ERR_CUDA;
@@ -80,10 +81,14 @@ int prefill_launch(const PrefillArgs &a) {
           cudaSuccess ||
       cudaGetSymbolAddress(reinterpret_cast<void **>(&work), g_prefill_work) != cudaSuccess)
     return ATTN_ERR_CUDA;
+  const bool win = a.window > 0;
   switch (a.d) {
-    case 32: return launch_d<32>(a, status, work, sms);
-    case 64: return launch_d<64>(a, status, work, sms);
-    case 128: return launch_d<128>(a, status, work, sms);
+    case 32: return win ? launch_d<32, true>(a, status, work, sms)
+                        : launch_d<32, false>(a, status, work, sms);
+    case 64: return win ? launch_d<64, true>(a, status, work, sms)
+                        : launch_d<64, false>(a, status, work, sms);
+    case 128: return win ? launch_d<128, true>(a, status, work, sms)
+                         : launch_d<128, false>(a, status, work, sms);
     default: return ATTN_ERR_UNSUPPORTED;
   }
 }

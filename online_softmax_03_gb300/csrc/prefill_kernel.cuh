@@ -52,8 +52,11 @@
 // final ratio", section 2.1) while e^(s - m) stays in range (<= 2^8 here).
 //
 // Causal masking is bottom-right aligned (query i sees keys j <= i + Tk - Tq);
-// K/V tiles wholly above the diagonal are never loaded, and only tiles that
-// cross the diagonal or the ragged end of K are masked element by element.
+// with a sliding window of W keys it also sees only j > i + Tk - Tq - W
+// ("4.2 FlashAttention I", Exercise 4; "Efficient attention & KV cache",
+// exercise 2).  K/V tiles wholly outside every row's visible range are never
+// loaded, and only tiles that cross an edge of it or the ragged end of K are
+// masked element by element.
 // Work items are ordered by groups of heads whose K/V fit in L2, heaviest
 // query tiles first within a group.
 //
@@ -84,6 +87,7 @@ struct PrefillParams {
   int n_items;            // n_bh * n_qt
   unsigned int *work;     // {next item, finished CTAs}: zero on entry, zero on exit
   int causal;
+  int window;             // > 0: causal sliding window of this many keys
   float scale_log2;       // scale * log2(e)
   unsigned long long wait_ns;
   int inject;             // test hook: 1 = withhold the first V tile
@@ -124,14 +128,22 @@ struct PrefillCfg {
   static_assert(256 + 2 * D <= 512, "tensor memory budget");
 };
 
-// Geometry of one work item, computed identically by every role.
+// Geometry of one work item, computed identically by every role: query tile
+// t visits the K/V tiles [lo_t, hi_t) (empty if equal); the item walks the
+// union of the two ranges, which is contiguous.
 struct PrefillItem {
   int bh, bh_kv, q0;
-  int n0, n1;  // K/V tiles visited by query tile 0 and 1 (0 = tile empty)
-  __device__ __forceinline__ int n(int t) const { return t == 0 ? n0 : n1; }
-  __device__ __forceinline__ int n_max() const { return n0 > n1 ? n0 : n1; }
+  int lo0, hi0, lo1, hi1;
+  __device__ __forceinline__ int lo(int t) const { return t == 0 ? lo0 : lo1; }
+  __device__ __forceinline__ int hi(int t) const { return t == 0 ? hi0 : hi1; }
+  __device__ __forceinline__ bool has(int t) const { return lo(t) < hi(t); }
+  __device__ __forceinline__ int jbeg() const {
+    return !(lo1 < hi1) ? lo0 : !(lo0 < hi0) ? lo1 : min(lo0, lo1);
+  }
+  __device__ __forceinline__ int jend() const { return max(hi0, hi1); }
 };
 
+template <bool kWindow>
 __device__ __forceinline__ PrefillItem prefill_item(const PrefillParams &p, int idx) {
   // Heads are taken in groups of head_group; inside a group the heaviest
   // query-tile pairs of every head come first, so the items in flight share
@@ -157,23 +169,28 @@ __device__ __forceinline__ PrefillItem prefill_item(const PrefillParams &p, int 
   it.q0 = qt * 256;
   const int delta = p.Tk - p.Tq;
   const int n_kv_all = (p.Tk + 127) / 128;
-  int nt[2];
+  int lo[2], hi[2];
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const int row0 = it.q0 + t * 128;
     if (row0 >= p.Tq) {
-      nt[t] = 0;
+      lo[t] = hi[t] = 0;
     } else {
       const int last_row = min(row0 + 127, p.Tq - 1);
-      nt[t] = p.causal ? min(n_kv_all, (last_row + delta) / 128 + 1) : n_kv_all;
+      hi[t] = p.causal ? min(n_kv_all, (last_row + delta) / 128 + 1) : n_kv_all;
+      // the window's left edge for the tile's first row: keys below it are
+      // outside every row's window
+      lo[t] = kWindow ? max(0, row0 + delta - p.window + 1) / 128 : 0;
     }
   }
-  it.n0 = nt[0];
-  it.n1 = nt[1];
+  it.lo0 = lo[0];
+  it.hi0 = hi[0];
+  it.lo1 = lo[1];
+  it.hi1 = hi[1];
   return it;
 }
 
-template <int D>
+template <int D, bool kWindow>
 __global__ void __launch_bounds__(320, 1)
     prefill_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
@@ -270,9 +287,9 @@ __global__ void __launch_bounds__(320, 1)
         item_ring[k] = idx;
         mbar_arrive(&item_full[k]);
         if (idx < 0) break;
-        const PrefillItem it = prefill_item(p, idx);
+        const PrefillItem it = prefill_item<kWindow>(p, idx);
         for (int t = 0; t < C::NQ && ok; ++t) {
-          if (it.n(t) == 0) continue;
+          if (!it.has(t)) continue;
           // Q_t is free once the previous item's last S_t has completed.
           if (q_cnt[t] > 0 && !mbar_wait(&q_empty[t], (q_cnt[t] - 1) & 1, wait_ns)) {
             ok = false;
@@ -284,8 +301,8 @@ __global__ void __launch_bounds__(320, 1)
                         &q_full[t], c * C::CHUNK, it.q0 + t * C::BM, it.bh);
           ++q_cnt[t];
         }
-        const int nmax = it.n_max();
-        for (int j = 0; ok && j < nmax; ++j, ++kv) {
+        const int jb = kWindow ? it.jbeg() : 0, je = it.jend();
+        for (int j = jb; ok && j < je; ++j, ++kv) {
           const int s = kv % ST, u = kv / ST;
           if (*abort_flag) { ok = false; break; }
           if (kv >= ST && !mbar_wait(&k_empty[s], (u - 1) & 1, wait_ns)) { ok = false; break; }
@@ -295,7 +312,7 @@ __global__ void __launch_bounds__(320, 1)
                         &tm_k, &k_full[s], c * C::CHUNK, j * C::BN, it.bh_kv);
           last_k[s] = kv;
           if (kv >= ST && !mbar_wait(&v_empty[s], (u - 1) & 1, wait_ns)) { ok = false; break; }
-          if (!(p.inject == 1 && first && j == 0)) {
+          if (!(p.inject == 1 && first && j == jb)) {
             mbar_arrive_expect_tx(&v_full[s], C::KV_BYTES);
             for (int c = 0; c < C::NCHUNK; ++c)
               tma_load_3d(smem + C::OFF_V + s * C::KV_BYTES + c * (C::BN * C::SPAN),
@@ -358,64 +375,73 @@ __global__ void __launch_bounds__(320, 1)
         if (!take_item(fetch, idx)) { ok = false; break; }
         mbar_arrive(&item_empty[(fetch - 1) & 1]);
         if (idx < 0) break;
-        const PrefillItem it = prefill_item(p, idx);
-        const int nmax = it.n_max();
+        const PrefillItem it = prefill_item<kWindow>(p, idx);
+        const int jb = kWindow ? it.jbeg() : 0, je = it.jend();
+        // S_t of K/V tile jj in stage sj, the first S of tile t's range.
+        auto start_tile = [&](const int t, int &q_cnt, const int sj, const int jj) -> bool {
+          if (!mbar_wait(&q_full[t], q_cnt & 1, wait_ns)) return false;
+          ++q_cnt;
+          issue_s(t, sj);
+          mma_commit(&s_full[t]);
+          if (jj + 1 == it.hi(t)) mma_commit(&q_empty[t]);  // its only S
+          return true;
+        };
         {
-          // First S of both tiles, on K/V tile 0 of this item.
+          // First S of the tiles whose range starts at the item's first tile.
           const int s0 = kv % ST;
           if (*abort_flag || !mbar_wait(&k_full[s0], (kv / ST) & 1, wait_ns)) { ok = false; break; }
-          if (it.n0 > 0) {
-            if (!mbar_wait(&q_full[0], q_cnt0 & 1, wait_ns)) { ok = false; break; }
-            ++q_cnt0;
-            issue_s(0, s0);
-            mma_commit(&s_full[0]);
-            if (it.n0 == 1) mma_commit(&q_empty[0]);
-          }
-          if (it.n1 > 0) {
-            if (!mbar_wait(&q_full[1], q_cnt1 & 1, wait_ns)) { ok = false; break; }
-            ++q_cnt1;
-            issue_s(1, s0);
-            mma_commit(&s_full[1]);
-            if (it.n1 == 1) mma_commit(&q_empty[1]);
-          }
+          if (it.has(0) && it.lo0 == jb && !start_tile(0, q_cnt0, s0, jb)) { ok = false; break; }
+          if (it.has(1) && it.lo1 == jb && !start_tile(1, q_cnt1, s0, jb)) { ok = false; break; }
           mma_commit(&k_empty[s0]);
         }
-        for (int j = 0; j < nmax; ++j) {
-          const int s = (kv + j) % ST, u = (kv + j) / ST;
-          const int s1 = (kv + j + 1) % ST, u1 = (kv + j + 1) / ST;
+        for (int j = jb; j < je; ++j) {
+          const int c = kv + (j - jb);  // ring position of K/V tile j
+          const int s = c % ST, u = c / ST;
+          const int s1 = (c + 1) % ST, u1 = (c + 1) / ST;
           bool v_ready = false, k_ready = false;
-          // One query tile: P_t V_j, then S_t of the next K/V tile.
-          auto tile_step = [&](const int t, int &p_cnt, const int nt) -> bool {
-            if (j >= nt) return true;
-            if (!mbar_wait(&p_full[t], p_cnt & 1, wait_ns)) return false;
-            ++p_cnt;
-            if (!v_ready) {
-              if (!mbar_wait(&v_full[s], u & 1, wait_ns)) return false;
-              v_ready = true;
-            }
-            tc_fence_after();  // P_t was written to tensor memory by the softmax threads
-            issue_pv(t, s, j > 0);
-            if (j + 1 < nt) {
-              if (!k_ready) {
-                if (!mbar_wait(&k_full[s1], u1 & 1, wait_ns)) return false;
-                k_ready = true;
+          auto need_k = [&]() -> bool {
+            if (k_ready) return true;
+            if (!mbar_wait(&k_full[s1], u1 & 1, wait_ns)) return false;
+            k_ready = true;
+            return true;
+          };
+          // One query tile: P_t V_j and S_t of the next K/V tile, or the first
+          // S_t if the tile's range starts with the next K/V tile.
+          auto tile_step = [&](const int t, int &p_cnt, int &q_cnt) -> bool {
+            // Without a window every range starts at 0 and this reduces to
+            // "j < hi": the issuing thread is the kernel's bottleneck, so the
+            // plain case carries none of the range logic.
+            const int lo = kWindow ? it.lo(t) : 0, hi = it.hi(t);
+            if ((!kWindow || lo <= j) && j < hi) {
+              if (!mbar_wait(&p_full[t], p_cnt & 1, wait_ns)) return false;
+              ++p_cnt;
+              if (!v_ready) {
+                if (!mbar_wait(&v_full[s], u & 1, wait_ns)) return false;
+                v_ready = true;
               }
-              issue_s(t, s1);
-              mma_commit(&s_full[t]);
-              if (j + 2 == nt) mma_commit(&q_empty[t]);  // last S_t of the item
-            } else {
-              mma_commit(&o_done[t]);
+              tc_fence_after();  // P_t was written to tensor memory by the softmax threads
+              issue_pv(t, s, j > lo);
+              if (j + 1 < hi) {
+                if (!need_k()) return false;
+                issue_s(t, s1);
+                mma_commit(&s_full[t]);
+                if (j + 2 == hi) mma_commit(&q_empty[t]);  // last S_t of the item
+              } else {
+                mma_commit(&o_done[t]);
+              }
+            } else if (kWindow && j + 1 == lo && lo < hi) {
+              if (!need_k() || !start_tile(t, q_cnt, s1, j + 1)) return false;
             }
             return true;
           };
-          if (*abort_flag || !tile_step(0, p_cnt0, it.n0) || !tile_step(1, p_cnt1, it.n1)) {
+          if (*abort_flag || !tile_step(0, p_cnt0, q_cnt0) || !tile_step(1, p_cnt1, q_cnt1)) {
             ok = false;
             break;
           }
           mma_commit(&v_empty[s]);
           if (k_ready) mma_commit(&k_empty[s1]);
         }
-        kv += nmax;
+        kv += je - jb;
       }
       if (!ok) fail();
       // Drain: all MMAs issued by this thread have completed before tensor
@@ -444,16 +470,19 @@ __global__ void __launch_bounds__(320, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&item_empty[(fetch - 1) & 1]);
       if (idx < 0) break;
-      const PrefillItem it = prefill_item(p, idx);
-      const int n = it.n(t);
-      if (n == 0) continue;
+      const PrefillItem it = prefill_item<kWindow>(p, idx);
+      if (!it.has(t)) continue;
+      const int jlo = kWindow ? it.lo(t) : 0, jhi = it.hi(t);
       const int row0 = it.q0 + t * C::BM;
       const int row_g = row0 + r;
-      const int lim = p.causal ? row_g + delta : 0x7fffffff;
+      const int lim = p.causal ? row_g + delta : 0x7fffffff;                 // last visible key
+      const int lim_lo = kWindow ? row_g + delta - p.window + 1 : -1;   // first visible key
+      // the largest first-visible key of the tile's rows
+      const int tile_lo = kWindow ? min(row0 + C::BM - 1, p.Tq - 1) + delta - p.window + 1 : -1;
       float m_used = -INFINITY;  // reference max, log2 units
       float l_sum = 0.f;
 
-      for (int j = 0; j < n; ++j) {
+      for (int j = jlo; j < jhi; ++j) {
         ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t], s_cnt & 1, wait_ns) && !*abort_flag);
         if (!ok) break;
         ++s_cnt;
@@ -462,13 +491,14 @@ __global__ void __launch_bounds__(320, 1)
         tmem_ld128_wait(t_s, s);
 
         const int kbase = j * C::BN;
-        const bool need_mask =
-            (kbase + C::BN > p.Tk) || (p.causal && kbase + C::BN - 1 > row0 + delta);
+        const bool need_mask = (kbase + C::BN > p.Tk) ||
+                               (p.causal && kbase + C::BN - 1 > row0 + delta) ||
+                               (kWindow && kbase < tile_lo);
         if (need_mask) {
 #pragma unroll
           for (int c = 0; c < C::BN; ++c) {
             const int key = kbase + c;
-            if (key > lim || key >= p.Tk) s[c] = -INFINITY;
+            if (key > lim || (kWindow && key < lim_lo) || key >= p.Tk) s[c] = -INFINITY;
           }
         }
         float mx[8];
@@ -491,7 +521,7 @@ __global__ void __launch_bounds__(320, 1)
         // O_t is stable here (PV_t(j-1) completed before S_t(j) was signalled):
         // rescale it before any of P_t(j) is published.  Chunks of 16 columns
         // keep the registers this rare path needs small next to the S row.
-        if (j > 0 && __any_sync(0xffffffffu, resc)) {
+        if (j > jlo && __any_sync(0xffffffffu, resc)) {
           const float2 al2 = make_float2(alpha, alpha);
 #pragma unroll 1
           for (int cb = 0; cb < D / 16; ++cb) {

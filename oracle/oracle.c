@@ -11,6 +11,8 @@
  *
  *   s_ij   = scale * sum_c Q[b,h,i,c] * K[b,g,j,c]          g = h / (Hq/Hkv)
  *   J_i    = { j < Tk : !causal  or  j <= i + (Tk - Tq) }   (visible keys)
+ *            and, with a sliding window W > 0 (causal only),
+ *            additionally j > i + (Tk - Tq) - W
  *   m_i    = max_{j in J_i} s_ij
  *   P_ij   = exp(s_ij - m_i) / sum_{j in J_i} exp(s_ij - m_i)
  *   O_i    = sum_j P_ij V[b,g,j,:]
@@ -24,6 +26,9 @@
  *  - "Explain tiled attention and verify its output", lab.py:
  *    standard_attention (materialised N x N scores, max shift optional).
  *  - "Efficient attention & KV cache", section 3, standard_attention.
+ *  - The sliding window (query i sees keys i - W < j <= i): "4.2
+ *    FlashAttention I", Exercise 4 (reference_swa), and "Efficient attention
+ *    & KV cache", exercise 2.
  *  - Causal with Tq != Tk (bottom-right alignment, query i at key position
  *    i + Tk - Tq) and the GQA head map h -> h / (Hq/Hkv) are readings of
  *    the pages, which define causal only for Tq == Tk and name enable_gqa
@@ -69,17 +74,21 @@ static void load_rows(const void *src, int in_type, size_t head_offset, int r0,
 }
 
 static int check_shape(int B, int Hq, int Hkv, int Tq, int Tk, int d,
-                       int causal) {
+                       int causal, int window) {
   if (B < 1 || Hq < 1 || Hkv < 1 || Tq < 1 || Tk < 1 || d < 1)
     return ORACLE_ERR_ARG;
   if (Hq % Hkv != 0) return ORACLE_ERR_ARG;
   if (causal && Tq > Tk) return ORACLE_ERR_ARG;
+  if (window < 0 || (window > 0 && !causal)) return ORACLE_ERR_ARG;
   return ORACLE_OK;
 }
 
 /* Is key j visible to query row i? */
-static int visible(int i, int j, int Tq, int Tk, int causal) {
-  return !causal || j <= i + (Tk - Tq);
+static int visible(int i, int j, int Tq, int Tk, int causal, int window) {
+  const int p = i + (Tk - Tq);  /* the query's position among the keys */
+  if (!causal) return 1;
+  if (j > p) return 0;
+  return window == 0 || j > p - window;
 }
 
 /*
@@ -98,9 +107,9 @@ static int visible(int i, int j, int Tq, int Tk, int causal) {
  */
 int oracle_attn_dense(const void *q, const void *k, const void *v, int in_type,
                       int B, int Hq, int Hkv, int Tq, int Tk, int d, int causal,
-                      double scale, int subtract_max, double *o, double *lse,
-                      double *p_out, long long *visible_pairs) {
-  int rc = check_shape(B, Hq, Hkv, Tq, Tk, d, causal);
+                      int window, double scale, int subtract_max, double *o,
+                      double *lse, double *p_out, long long *visible_pairs) {
+  int rc = check_shape(B, Hq, Hkv, Tq, Tk, d, causal, window);
   if (rc) return rc;
   const int group = Hq / Hkv;
   const int nheads = B * Hq;
@@ -130,7 +139,7 @@ int oracle_attn_dense(const void *q, const void *k, const void *v, int in_type,
     for (int i = 0; i < Tq; ++i) {
       for (int j = 0; j < Tk; ++j) {
         double *sij = &S[(size_t)i * Tk + j];
-        if (!visible(i, j, Tq, Tk, causal)) {
+        if (!visible(i, j, Tq, Tk, causal, window)) {
           *sij = -INFINITY;
           continue;
         }
@@ -191,9 +200,10 @@ int oracle_attn_dense(const void *q, const void *k, const void *v, int in_type,
  */
 int oracle_attn_rows(const void *q, const void *k, const void *v, int in_type,
                      int B, int Hq, int Hkv, int Tq, int Tk, int d, int causal,
-                     double scale, int nrows, const int *rb, const int *rh,
-                     const int *ri, double *o_rows, double *lse_rows) {
-  int rc = check_shape(B, Hq, Hkv, Tq, Tk, d, causal);
+                     int window, double scale, int nrows, const int *rb,
+                     const int *rh, const int *ri, double *o_rows,
+                     double *lse_rows) {
+  int rc = check_shape(B, Hq, Hkv, Tq, Tk, d, causal, window);
   if (rc) return rc;
   for (int r = 0; r < nrows; ++r)
     if (rb[r] < 0 || rb[r] >= B || rh[r] < 0 || rh[r] >= Hq || ri[r] < 0 ||
@@ -219,7 +229,7 @@ int oracle_attn_rows(const void *q, const void *k, const void *v, int in_type,
     load_rows(q, in_type, qoff, i, 1, d, qi);
     double m = -INFINITY;
     for (int j = 0; j < Tk; ++j) {
-      if (!visible(i, j, Tq, Tk, causal)) {
+      if (!visible(i, j, Tq, Tk, causal, window)) {
         s[j] = -INFINITY;
         continue;
       }
@@ -266,7 +276,8 @@ int oracle_attn_rows(const void *q, const void *k, const void *v, int in_type,
  * "Explain tiled attention and verify its output" (rescale_previous_acc).
  *
  * Under causal masking, K/V blocks that lie wholly above the diagonal of
- * the query block are skipped.
+ * the query block are skipped, and with a window also those wholly left of
+ * every row's window ("4.2 FlashAttention I", Exercise 4).
  *
  *   kv_order  optional permutation of the K/V block indices [0, nkb), used
  *             for every query block (NULL: natural order).  The result does
@@ -278,10 +289,10 @@ int oracle_attn_rows(const void *q, const void *k, const void *v, int in_type,
  */
 int oracle_attn_blocked(const void *q, const void *k, const void *v,
                         int in_type, int B, int Hq, int Hkv, int Tq, int Tk,
-                        int d, int causal, double scale, int bq, int bk,
-                        const int *kv_order, int rescale_acc, double *o,
+                        int d, int causal, int window, double scale, int bq,
+                        int bk, const int *kv_order, int rescale_acc, double *o,
                         double *lse, long long *tiles_visited) {
-  int rc = check_shape(B, Hq, Hkv, Tq, Tk, d, causal);
+  int rc = check_shape(B, Hq, Hkv, Tq, Tk, d, causal, window);
   if (rc) return rc;
   if (bq < 1 || bk < 1) return ORACLE_ERR_ARG;
   const int nkb = (Tk + bk - 1) / bk;
@@ -335,6 +346,8 @@ int oracle_attn_blocked(const void *q, const void *k, const void *v,
         const int cols = (Tk - j0 < bk) ? (Tk - j0) : bk;
         /* causal: the block holds no key visible to any row of this block */
         if (causal && j0 > q0 + rows - 1 + delta) continue;
+        /* window: the block lies wholly left of every row's window */
+        if (window > 0 && j0 + cols - 1 < q0 + delta - window + 1) continue;
         visited += 1;
         load_rows(k, in_type, kvoff, j0, cols, d, Kj);
         load_rows(v, in_type, kvoff, j0, cols, d, Vj);
@@ -343,7 +356,7 @@ int oracle_attn_blocked(const void *q, const void *k, const void *v,
           double *srow = &Sij[(size_t)r * bk];
           double mblk = -INFINITY;
           for (int cj = 0; cj < cols; ++cj) {
-            if (!visible(i, j0 + cj, Tq, Tk, causal)) {
+            if (!visible(i, j0 + cj, Tq, Tk, causal, window)) {
               srow[cj] = -INFINITY;
               continue;
             }

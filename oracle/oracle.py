@@ -59,11 +59,11 @@ def _load():
             vp, ip, dp = ctypes.c_void_p, ctypes.c_int, ctypes.c_double
             llp = ctypes.POINTER(ctypes.c_longlong)
             lib.oracle_attn_dense.argtypes = [vp, vp, vp, ip, ip, ip, ip, ip, ip,
-                                              ip, ip, dp, ip, vp, vp, vp, llp]
+                                              ip, ip, ip, dp, ip, vp, vp, vp, llp]
             lib.oracle_attn_rows.argtypes = [vp, vp, vp, ip, ip, ip, ip, ip, ip,
-                                             ip, ip, dp, ip, vp, vp, vp, vp, vp]
+                                             ip, ip, ip, dp, ip, vp, vp, vp, vp, vp]
             lib.oracle_attn_blocked.argtypes = [vp, vp, vp, ip, ip, ip, ip, ip,
-                                                ip, ip, ip, dp, ip, ip, vp, ip,
+                                                ip, ip, ip, ip, dp, ip, ip, vp, ip,
                                                 vp, vp, llp]
             lib.oracle_online_softmax_1d.argtypes = [vp, ip, ip, vp, vp, vp, vp,
                                                      vp]
@@ -115,8 +115,9 @@ def _inputs(q, k, v):
 
 
 def attention_dense(q, k, v, causal=False, scale=None, subtract_max=True,
-                    return_p=False):
-    """Dense fp64 attention with materialised S and P.
+                    return_p=False, window=0):
+    """Dense fp64 attention with materialised S and P (window > 0: causal
+    sliding window of that many keys).
 
     Returns (o [B,Hq,Tq,d], lse [B,Hq,Tq], extras) where extras holds
     'visible_pairs' and, if return_p, 'p' [B,Hq,Tq,Tk].
@@ -129,7 +130,7 @@ def attention_dense(q, k, v, causal=False, scale=None, subtract_max=True,
     p = np.empty((B, Hq, Tq, Tk), np.float64) if return_p else None
     vis = ctypes.c_longlong(0)
     rc = _load().oracle_attn_dense(_ptr(q), _ptr(k), _ptr(v), t, B, Hq, Hkv, Tq,
-                                   Tk, d, int(bool(causal)), scale,
+                                   Tk, d, int(bool(causal)), int(window), scale,
                                    int(bool(subtract_max)), _ptr(o), _ptr(lse),
                                    _ptr(p), ctypes.byref(vis))
     _check(rc)
@@ -139,7 +140,8 @@ def attention_dense(q, k, v, causal=False, scale=None, subtract_max=True,
     return o, lse, extras
 
 
-def attention_rows(q, k, v, rows_b, rows_h, rows_i, causal=False, scale=None):
+def attention_rows(q, k, v, rows_b, rows_h, rows_i, causal=False, scale=None,
+                   window=0):
     """The dense definition evaluated for selected rows (b, h, i) only.
 
     Returns (o_rows [n, d], lse_rows [n]).
@@ -156,14 +158,15 @@ def attention_rows(q, k, v, rows_b, rows_h, rows_i, causal=False, scale=None):
     o = np.empty((n, d), np.float64)
     lse = np.empty((n,), np.float64)
     rc = _load().oracle_attn_rows(_ptr(q), _ptr(k), _ptr(v), t, B, Hq, Hkv, Tq,
-                                  Tk, d, int(bool(causal)), scale, n, _ptr(rb),
+                                  Tk, d, int(bool(causal)), int(window), scale, n,
+                                  _ptr(rb),
                                   _ptr(rh), _ptr(ri), _ptr(o), _ptr(lse))
     _check(rc)
     return o, lse
 
 
 def attention_blocked(q, k, v, block_q, block_kv, causal=False, scale=None,
-                      kv_order=None, rescale_acc=True):
+                      kv_order=None, rescale_acc=True, window=0):
     """Blocked online-softmax forward (fp64).
 
     Returns (o, lse, tiles_visited).
@@ -180,7 +183,7 @@ def attention_blocked(q, k, v, block_q, block_kv, causal=False, scale=None,
     lse = np.empty((B, Hq, Tq), np.float64)
     visited = ctypes.c_longlong(0)
     rc = _load().oracle_attn_blocked(_ptr(q), _ptr(k), _ptr(v), t, B, Hq, Hkv,
-                                     Tq, Tk, d, int(bool(causal)), scale,
+                                     Tq, Tk, d, int(bool(causal)), int(window), scale,
                                      int(block_q), int(block_kv), _ptr(order),
                                      int(bool(rescale_acc)), _ptr(o), _ptr(lse),
                                      ctypes.byref(visited))

@@ -301,3 +301,73 @@ def test_causal_tiles_visited_half_the_grid():
     assert visited == 1 + 2 + 3 + 4
     _, _, visited = ora.attention_blocked(q, k, v, 16, 16, causal=False)
     assert visited == 16
+
+
+# --- sliding window ("4.2 FlashAttention I", Exercise 4) ---------------------
+
+def test_window_one_sees_only_the_diagonal_key():
+    """W = 1: each query sees exactly its own position, so O_i = v_{i+d} and
+    LSE_i = s_{i,i+d} with d = Tk - Tq."""
+    Tq, Tk, d = 9, 13, 8
+    q, k, v = _rand((2, 2, Tq, d), 40), _rand((2, 2, Tk, d), 41), _rand((2, 2, Tk, d), 42)
+    o, lse, ex = ora.attention_dense(q, k, v, causal=True, window=1)
+    idx = np.arange(Tq) + (Tk - Tq)
+    np.testing.assert_allclose(o, v[:, :, idx], rtol=0, atol=1e-15)
+    s_diag = (q * k[:, :, idx]).sum(-1) / math.sqrt(d)
+    np.testing.assert_allclose(lse, s_diag, rtol=0, atol=1e-14)
+    assert ex["visible_pairs"] == 2 * 2 * Tq
+
+
+def test_window_at_least_tk_is_plain_causal():
+    q, k, v = _rand((1, 3, 20, 8), 43), _rand((1, 3, 27, 8), 44), _rand((1, 3, 27, 8), 45)
+    o, lse, _ = ora.attention_dense(q, k, v, causal=True)
+    for w in (27, 40):
+        ow, lw, _ = ora.attention_dense(q, k, v, causal=True, window=w)
+        np.testing.assert_array_equal(o, ow)
+        np.testing.assert_array_equal(lse, lw)
+
+
+def test_window_equal_keys_give_windowed_mean():
+    T, d, W = 30, 4, 7
+    q = _rand((1, 1, T, d), 46)
+    k = np.broadcast_to(_rand((1, 1, 1, d), 47), (1, 1, T, d)).copy()
+    v = _rand((1, 1, T, d), 48)
+    o, _, _ = ora.attention_dense(q, k, v, causal=True, window=W)
+    for i in range(T):
+        lo = max(0, i - W + 1)
+        np.testing.assert_allclose(o[0, 0, i], v[0, 0, lo:i + 1].mean(0), rtol=0, atol=1e-14)
+
+
+def test_window_exercise_setup_blocked_equals_dense():
+    """The exercise's check: N = 100, d = 16, W = 24, 32 x 32 blocks."""
+    q, k, v = _rand((1, 1, 100, 16), 7), _rand((1, 1, 100, 16), 8), _rand((1, 1, 100, 16), 9)
+    o, lse, ex = ora.attention_dense(q, k, v, causal=True, window=24)
+    ob, lseb, visited = ora.attention_blocked(q, k, v, 32, 32, causal=True, window=24)
+    assert np.abs(ob - o).max() < 1e-12
+    assert np.abs(lseb - lse).max() < 1e-12
+    _, _, visited_causal = ora.attention_blocked(q, k, v, 32, 32, causal=True)
+    assert visited < visited_causal
+
+
+@pytest.mark.parametrize("bq,bk", [(8, 8), (13, 19), (32, 8), (1, 1), (16, 64)])
+@pytest.mark.parametrize("W", [1, 5, 24, 64])
+def test_window_blocked_skips_exactly_the_empty_blocks(bq, bk, W):
+    """Blocked with the left-edge skip equals dense, and the blocks it
+    visits are exactly those holding at least one visible (row, key) pair
+    (found by brute force from the dense probability matrix)."""
+    Tq, Tk, d = 45, 61, 8
+    q, k, v = _rand((1, 1, Tq, d), 49), _rand((1, 1, Tk, d), 50), _rand((1, 1, Tk, d), 51)
+    o, lse, ex = ora.attention_dense(q, k, v, causal=True, window=W, return_p=True)
+    ob, lseb, visited = ora.attention_blocked(q, k, v, bq, bk, causal=True, window=W)
+    assert np.abs(ob - o).max() < 1e-12
+    assert np.abs(lseb - lse).max() < 1e-12
+    vis = ex["p"][0, 0] > 0
+    nonempty = sum(vis[i0:i0 + bq, j0:j0 + bk].any()
+                   for i0 in range(0, Tq, bq) for j0 in range(0, Tk, bk))
+    assert visited == nonempty
+
+
+def test_window_requires_causal():
+    q = k = v = _rand((1, 1, 8, 4), 52)
+    with pytest.raises(ValueError):
+        ora.attention_dense(q, k, v, causal=False, window=3)
