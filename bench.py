@@ -288,6 +288,25 @@ def run_ours(args, rank, world, local_rank):
     pre_flops = acct.attention_flops(PREFILL.B, PREFILL.Hq, PREFILL.Tq, PREFILL.Tk, PREFILL.d,
                                      PREFILL.causal)
     dec_bytes = acct.decode_bytes(DECODE.B, DECODE.Hq, DECODE.Hkv, DECODE.Tk, DECODE.d)
+    # ---- sliding-window prefill (a row beyond the specified step), timed alone
+    win_ms = None
+    if not args.no_extra_rows:
+        qw, kw, vw = synth.make_inputs(synth.WINDOW_8K, dev)
+        ow = torch.empty_like(qw)
+        lw = torch.empty(qw.shape[:3], dtype=torch.float32, device=dev)
+        for _ in range(3):
+            binding.fwd(qw, kw, vw, window=synth.WINDOW_KEYS, out=ow, lse=lw)
+        torch.cuda.synchronize()
+        ew0, ew1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_win = 30
+        ew0.record(stream)
+        for _ in range(n_win):
+            binding.fwd(qw, kw, vw, window=synth.WINDOW_KEYS, out=ow, lse=lw)
+        ew1.record(stream)
+        torch.cuda.synchronize()
+        win_ms = ew0.elapsed_time(ew1) / n_win
+        del qw, kw, vw, ow, lw
+
     agg = aggregate_ranks(
         {"pre_s": sum(pre_ms) / 1e3, "dec_s": sum(dec_ms) / 1e3, "total_ms": total_ms,
          "e2e_pre_ms": e2e_pre_ms, "e2e_dec_ms": e2e_dec_ms},
@@ -375,6 +394,21 @@ def run_ours(args, rank, world, local_rank):
             "steps": E,
             "note": "prefill leg; the decode leg's e2e is under decode.e2e",
         },
+        "window": None if win_ms is None else {
+            "workload": synth.WINDOW_8K.name,
+            "window_keys": synth.WINDOW_KEYS,
+            "value": round(acct.window_flops(synth.WINDOW_8K.B, synth.WINDOW_8K.Hq,
+                                             synth.WINDOW_8K.Tq, synth.WINDOW_8K.Tk,
+                                             synth.WINDOW_8K.d, synth.WINDOW_KEYS)
+                           / (win_ms / 1e3) / 1e12, 2),
+            "unit": "TFLOP/s (4*d per visible pair)",
+            "ms": round(win_ms, 4),
+            "traffic": ncu_traffic("prefill_fwd_kernel<128,window>/" + synth.WINDOW_8K.name,
+                                   source_sha(*PREFILL_SOURCES)),
+            "frac_of_sustained_peak": round(acct.window_flops(
+                synth.WINDOW_8K.B, synth.WINDOW_8K.Hq, synth.WINDOW_8K.Tq, synth.WINDOW_8K.Tk,
+                synth.WINDOW_8K.d, synth.WINDOW_KEYS) / (win_ms / 1e3) / 1e12 / peak_tf, 4),
+        },
         "gpu_launches": K * 3,
         "clocks": clk,
     }
@@ -457,6 +491,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra-rows", action="store_true",
+                    help="skip the separately timed rows beyond the specified step")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")

@@ -29,6 +29,24 @@ def attention_flops(B: int, Hq: int, Tq: int, Tk: int, d: int, causal: bool) -> 
     return f / 2.0 if causal else f
 
 
+def visible_pairs(Tq: int, Tk: int, causal: bool, window: int = 0) -> int:
+    """(row, key) pairs inside the mask of one (batch, head): all Tq*Tk, the
+    bottom-right causal triangle, or the causal band of `window` keys."""
+    if not causal:
+        return Tq * Tk
+    total = 0
+    for i in range(Tq):
+        p = i + Tk - Tq  # the query's position among the keys
+        total += (p + 1) if window <= 0 else min(window, p + 1)
+    return total
+
+
+def window_flops(B: int, Hq: int, Tq: int, Tk: int, d: int, window: int) -> float:
+    """Sliding-window forward: 4*d per visible (row, key) pair (QK^T and PV
+    each cost 2*d per pair), counted exactly rather than halved."""
+    return 4.0 * d * B * Hq * visible_pairs(Tq, Tk, True, window)
+
+
 def prefill_compulsory_bytes(B: int, Hq: int, Hkv: int, Tq: int, Tk: int, d: int) -> int:
     """Read Q, K, V once and write O (bf16) and LSE (fp32) once."""
     q = B * Hq * Tq * d * BF16_BYTES

@@ -71,6 +71,12 @@ LONG_8000_FULL = LONG_8K_CAUSAL.with_(name="long_b1_h32_t8000_d64_full_q4",
 DECODE_GQA = Workload("decode_b64_hq32_hkv8_tk8192_d128", 64, 32, 8, 1, 8192, 128,
                       False, "normal", 4, decode=True)
 
+# Sliding-window prefill (causal band of WINDOW_KEYS keys); measured beside
+# the specified workloads.
+WINDOW_KEYS = 1024
+WINDOW_8K = Workload("window_b4_h32_t8192_d128_w1024", 4, 32, 32, 8192, 8192, 128, True,
+                     "normal", 6)
+
 ALL = (TINY, TINY_NONCAUSAL, PREFILL_1K, PREFILL_4K, LONG_8K_CAUSAL, LONG_8K_FULL,
        LONG_8000_CAUSAL, LONG_8000_FULL, DECODE_GQA)
 

@@ -33,3 +33,21 @@ def test_flops_and_intensity():
     # GQA decode: 4 query heads share each K/V head, AI about 4 FLOP/byte
     ai_dec = acc.decode_flops(64, 32, 8192, 128) / acc.decode_bytes(64, 32, 8, 8192, 128)
     assert 3.9 < ai_dec < 4.1
+
+
+def test_visible_pairs_and_window_flops():
+    """Pair counts match brute force over the mask definition, and the
+    window count has the closed form W(W+1)/2 + (T-W)W for Tq = Tk = T >= W."""
+    import numpy as np
+
+    for Tq, Tk, W in ((5, 5, 0), (7, 11, 0), (7, 11, 3), (16, 16, 4), (9, 9, 20)):
+        i = np.arange(Tq)[:, None] + (Tk - Tq)
+        j = np.arange(Tk)[None, :]
+        mask = j <= i
+        if W:
+            mask &= j > i - W
+        assert acc.visible_pairs(Tq, Tk, True, W) == int(mask.sum())
+    T, W = 8192, 1024
+    assert acc.visible_pairs(T, T, True, W) == W * (W + 1) // 2 + (T - W) * W
+    assert acc.window_flops(4, 32, T, T, 128, W) == 4.0 * 128 * 4 * 32 * acc.visible_pairs(T, T, True, W)
+    assert acc.visible_pairs(6, 9, False) == 54

@@ -72,3 +72,17 @@ def test_window_rejects_bad_windows():
     q, k, v = synth.make_inputs(w, "cuda")
     with pytest.raises(binding.AttnError):
         binding.fwd(q, k, v, window=0)
+
+
+def test_window_benchmarked_workload_sampled_rows():
+    """The sliding-window workload the benchmark times (B=4, H=32, T=8192,
+    d=128, 1024-key window), checked on sampled rows in the same launch."""
+    w = synth.WINDOW_8K
+    q, k, v = synth.make_inputs(w, "cuda")
+    o, lse = binding.fwd(q, k, v, window=synth.WINDOW_KEYS)
+    torch.cuda.synchronize()
+    rb, rh, ri = synth.sample_rows(w, 128)
+    o_ref, lse_ref = ora.attention_rows(synth.bf16_bits(q), synth.bf16_bits(k),
+                                        synth.bf16_bits(v), rb, rh, ri, causal=True,
+                                        scale=w.scale, window=synth.WINDOW_KEYS)
+    assert_close(o[rb, rh, ri], lse[rb, rh, ri], o_ref, lse_ref, w.name)
