@@ -436,3 +436,91 @@ int oracle_online_softmax_1d(const double *x, int n, int block, double *p,
   if (lse_out) *lse_out = m + log(l);
   return ORACLE_OK;
 }
+
+/*
+ * Decode against a paged KV cache: one query token per sequence, its keys
+ * and values gathered through a per-sequence block table ("Efficient
+ * attention & KV cache", section 2.5 "Paged and shared caches": the cache
+ * lives in fixed-size blocks and the kernel fetches each block from its
+ * physical location by looking it up in the sequence's table; the same
+ * page's interview answer on what PagedAttention changes in the kernel).
+ *
+ * Layout (a reading: the page fixes blocks and a table, not the order of
+ * the axes inside a block):
+ *   q            [B, Hq, d]                    one query row per (b, h)
+ *   k_pages      [num_pages, Hkv, page_size, d]
+ *   v_pages      [num_pages, Hkv, page_size, d]
+ *   block_table  [B, max_pages]  int32, physical page of logical page p
+ *   seq_lens     [B]             int32, keys of sequence b (1..max_pages*page_size)
+ *
+ * Key j of sequence b (j < seq_lens[b]) is row j % page_size of head g in
+ * physical page block_table[b][j / page_size].  The result is the plain
+ * definition over those keys (no mask: a decode query sees its whole
+ * cache):  s_j = scale * q . K_j,  O = sum_j softmax(s)_j V_j,
+ * LSE = m + ln sum_j exp(s_j - m).  o is [B, Hq, d], lse is [B, Hq].
+ */
+int oracle_attn_paged_decode(const void *q, const void *k_pages,
+                             const void *v_pages, int in_type,
+                             const int *block_table, const int *seq_lens,
+                             int B, int Hq, int Hkv, int d, int page_size,
+                             int num_pages, int max_pages, double scale,
+                             double *o, double *lse) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || d < 1 || page_size < 1 || num_pages < 1 ||
+      max_pages < 1 || Hq % Hkv != 0)
+    return ORACLE_ERR_ARG;
+  for (int b = 0; b < B; ++b) {
+    const int len = seq_lens[b];
+    if (len < 1 || len > max_pages * page_size) return ORACLE_ERR_ARG;
+    const int used = (len + page_size - 1) / page_size;
+    for (int pg = 0; pg < used; ++pg) {
+      const int phys = block_table[(size_t)b * max_pages + pg];
+      if (phys < 0 || phys >= num_pages) return ORACLE_ERR_ARG;
+    }
+  }
+  const int group = Hq / Hkv;
+  int status = ORACLE_OK;
+
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+  for (int b = 0; b < B; ++b) {
+    for (int h = 0; h < Hq; ++h) {
+      const int g = h / group, len = seq_lens[b];
+      double *qi = malloc(sizeof(double) * d);
+      double *row = malloc(sizeof(double) * d);
+      double *s = malloc(sizeof(double) * (size_t)len);
+      if (!qi || !row || !s) {
+#pragma omp atomic write
+        status = ORACLE_ERR_NOMEM;
+        free(qi); free(row); free(s);
+        continue;
+      }
+      load_rows(q, in_type, ((size_t)b * Hq + h) * (size_t)d, 0, 1, d, qi);
+      double m = -INFINITY;
+      for (int j = 0; j < len; ++j) {
+        const int phys = block_table[(size_t)b * max_pages + j / page_size];
+        const size_t slab = ((size_t)phys * Hkv + g) * (size_t)page_size * d;
+        load_rows(k_pages, in_type, slab, j % page_size, 1, d, row);
+        double acc = 0.0;
+        for (int c = 0; c < d; ++c) acc += qi[c] * row[c];
+        s[j] = scale * acc;
+        if (s[j] > m) m = s[j];
+      }
+      double denom = 0.0;
+      for (int j = 0; j < len; ++j) {
+        s[j] = exp(s[j] - m);
+        denom += s[j];
+      }
+      double *orow = &o[((size_t)b * Hq + h) * d];
+      for (int c = 0; c < d; ++c) orow[c] = 0.0;
+      for (int j = 0; j < len; ++j) {
+        const int phys = block_table[(size_t)b * max_pages + j / page_size];
+        const size_t slab = ((size_t)phys * Hkv + g) * (size_t)page_size * d;
+        load_rows(v_pages, in_type, slab, j % page_size, 1, d, row);
+        const double pj = s[j] / denom;
+        for (int c = 0; c < d; ++c) orow[c] += pj * row[c];
+      }
+      lse[(size_t)b * Hq + h] = m + log(denom);
+      free(qi); free(row); free(s);
+    }
+  }
+  return status;
+}

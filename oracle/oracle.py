@@ -67,8 +67,11 @@ def _load():
                                                 vp, vp, llp]
             lib.oracle_online_softmax_1d.argtypes = [vp, ip, ip, vp, vp, vp, vp,
                                                      vp]
+            lib.oracle_attn_paged_decode.argtypes = [vp, vp, vp, ip, vp, vp, ip, ip,
+                                                     ip, ip, ip, ip, ip, dp, vp, vp]
             for f in (lib.oracle_attn_dense, lib.oracle_attn_rows,
-                      lib.oracle_attn_blocked, lib.oracle_online_softmax_1d):
+                      lib.oracle_attn_blocked, lib.oracle_online_softmax_1d,
+                      lib.oracle_attn_paged_decode):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -189,6 +192,36 @@ def attention_blocked(q, k, v, block_q, block_kv, causal=False, scale=None,
                                      ctypes.byref(visited))
     _check(rc)
     return o, lse, visited.value
+
+
+def attention_paged_decode(q, k_pages, v_pages, block_table, seq_lens, scale=None):
+    """Decode of one query token per sequence against a paged KV cache.
+
+    q [B, Hq, d]; k_pages, v_pages [num_pages, Hkv, page_size, d];
+    block_table int [B, max_pages]; seq_lens int [B].
+    Returns (o [B, Hq, d], lse [B, Hq]) in float64.
+    """
+    if q.ndim != 3 or k_pages.ndim != 4 or v_pages.shape != k_pages.shape:
+        raise ValueError("q must be [B, Hq, d] and the pages [num_pages, Hkv, page_size, d]")
+    B, Hq, d = q.shape
+    num_pages, Hkv, page_size, dk = k_pages.shape
+    if dk != d:
+        raise ValueError("head dims differ")
+    (qa, tq), (ka, tk), (va, tv) = _as_input(q), _as_input(k_pages), _as_input(v_pages)
+    if not tq == tk == tv:
+        raise TypeError("q, k, v must share one input type")
+    table = np.ascontiguousarray(block_table, dtype=np.int32)
+    lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    if table.ndim != 2 or table.shape[0] != B or lens.shape != (B,):
+        raise ValueError("block_table must be [B, max_pages] and seq_lens [B]")
+    scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+    o = np.empty((B, Hq, d), np.float64)
+    lse = np.empty((B, Hq), np.float64)
+    rc = _load().oracle_attn_paged_decode(_ptr(qa), _ptr(ka), _ptr(va), tq, _ptr(table),
+                                          _ptr(lens), B, Hq, Hkv, d, page_size, num_pages,
+                                          table.shape[1], scale, _ptr(o), _ptr(lse))
+    _check(rc)
+    return o, lse
 
 
 def online_softmax_1d(x, block):

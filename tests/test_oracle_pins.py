@@ -371,3 +371,115 @@ def test_window_requires_causal():
     q = k = v = _rand((1, 1, 8, 4), 52)
     with pytest.raises(ValueError):
         ora.attention_dense(q, k, v, causal=False, window=3)
+
+
+# --- paged-KV decode ("Efficient attention & KV cache", section 2.5) -------
+
+def _paginate(k, v, page_size, seed=None):
+    """Cut a contiguous cache [B, Hkv, Tk, d] into pages [num_pages, Hkv,
+    page_size, d] (sequence b owns pages b*npp .. b*npp + npp - 1, the tail
+    of its last page zero) and return (k_pages, v_pages, table).  With a
+    seed the physical pages are shuffled and the table follows them."""
+    B, Hkv, Tk, d = k.shape
+    npp = -(-Tk // page_size)
+    pad = npp * page_size - Tk
+    kp = np.pad(k, ((0, 0), (0, 0), (0, pad), (0, 0)))
+    vp = np.pad(v, ((0, 0), (0, 0), (0, pad), (0, 0)))
+    # [B, Hkv, npp, ps, d] -> [B, npp, Hkv, ps, d] -> [B*npp, Hkv, ps, d]
+    kp = kp.reshape(B, Hkv, npp, page_size, d).transpose(0, 2, 1, 3, 4).reshape(-1, Hkv, page_size, d)
+    vp = vp.reshape(B, Hkv, npp, page_size, d).transpose(0, 2, 1, 3, 4).reshape(-1, Hkv, page_size, d)
+    table = np.arange(B * npp, dtype=np.int32).reshape(B, npp)
+    if seed is not None:
+        perm = np.random.default_rng(seed).permutation(B * npp)
+        kp2, vp2 = np.empty_like(kp), np.empty_like(vp)
+        kp2[perm], vp2[perm] = kp, vp
+        kp, vp, table = kp2, vp2, perm[table].astype(np.int32)
+    return np.ascontiguousarray(kp), np.ascontiguousarray(vp), table
+
+
+@pytest.mark.parametrize("page_size", [1, 4, 16, 7])
+def test_paged_decode_identity_table_equals_dense(page_size):
+    """Pages laid out in order with full lengths: the result is the dense
+    definition on the contiguous cache (GQA group 3, Tk not a multiple of the
+    page size)."""
+    B, Hq, Hkv, Tk, d = 2, 6, 2, 37, 8
+    q, k, v = _rand((B, Hq, 1, d), 60), _rand((B, Hkv, Tk, d), 61), _rand((B, Hkv, Tk, d), 62)
+    o, lse, _ = ora.attention_dense(q, k, v, causal=False)
+    kp, vp, table = _paginate(k, v, page_size)
+    op, lp = ora.attention_paged_decode(q[:, :, 0], kp, vp, table, np.full(B, Tk))
+    np.testing.assert_allclose(op, o[:, :, 0], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lp, lse[:, :, 0], rtol=0, atol=1e-14)
+
+
+def test_paged_decode_shuffled_pages_change_nothing():
+    """Moving physical pages and updating the table is invisible."""
+    B, Hq, Hkv, Tk, d = 3, 4, 4, 50, 16
+    q, k, v = _rand((B, Hq, 1, d), 63), _rand((B, Hkv, Tk, d), 64), _rand((B, Hkv, Tk, d), 65)
+    lens = np.array([50, 17, 1])
+    a = ora.attention_paged_decode(q[:, :, 0], *_paginate(k, v, 8), lens)
+    b = ora.attention_paged_decode(q[:, :, 0], *_paginate(k, v, 8, seed=5), lens)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+
+
+def test_paged_decode_ragged_lengths_read_only_their_keys():
+    """Sequence b sees exactly its first seq_lens[b] keys: every slot past
+    them (the rest of the last page, whole unused pages) holds NaN and the
+    result equals the dense definition on the truncated cache."""
+    B, Hq, Hkv, Tk, d, ps = 4, 4, 2, 40, 8, 16
+    q, k, v = _rand((B, Hq, 1, d), 66), _rand((B, Hkv, Tk, d), 67), _rand((B, Hkv, Tk, d), 68)
+    lens = np.array([40, 33, 16, 5])
+    kn, vn = k.copy(), v.copy()
+    for b, n in enumerate(lens):
+        kn[b, :, n:] = np.nan
+        vn[b, :, n:] = np.nan
+    kp, vp, table = _paginate(kn, vn, ps, seed=9)
+    op, lp = ora.attention_paged_decode(q[:, :, 0], kp, vp, table, lens)
+    assert np.isfinite(op).all() and np.isfinite(lp).all()
+    for b, n in enumerate(lens):
+        o, lse, _ = ora.attention_dense(q[b:b + 1], k[b:b + 1, :, :n], v[b:b + 1, :, :n])
+        np.testing.assert_allclose(op[b], o[0, :, 0], rtol=0, atol=1e-14)
+        np.testing.assert_allclose(lp[b], lse[0, :, 0], rtol=0, atol=1e-14)
+
+
+def test_paged_decode_single_key_and_shared_prefix():
+    """seq_len 1: O is that key's value row and LSE its scaled score.  Two
+    sequences whose tables point at the same pages (a shared prefix) with
+    the same query give identical rows."""
+    Hq = Hkv = 2
+    d, ps = 8, 4
+    kp, vp = _rand((3, Hkv, ps, d), 69), _rand((3, Hkv, ps, d), 70)
+    q = _rand((2, Hq, d), 71)
+    q[1] = q[0]
+    table = np.array([[2, 0], [2, 0]], dtype=np.int32)
+    o, lse = ora.attention_paged_decode(q, kp, vp, table, np.array([1, 1]))
+    for h in range(Hq):
+        np.testing.assert_array_equal(o[0, h], vp[2, h, 0])
+        np.testing.assert_allclose(lse[0, h], q[0, h] @ kp[2, h, 0] / math.sqrt(d), rtol=0, atol=1e-15)
+    o, lse = ora.attention_paged_decode(q, kp, vp, table, np.array([6, 6]))
+    np.testing.assert_array_equal(o[0], o[1])
+    np.testing.assert_array_equal(lse[0], lse[1])
+
+
+def test_paged_decode_bf16_inputs_match_the_upcast_f64_inputs():
+    rng = np.random.default_rng(72)
+    bits = lambda shape: rng.integers(0x3c00, 0x4000, size=shape, dtype=np.uint16) ^ (
+        rng.integers(0, 2, size=shape, dtype=np.uint16) << 15)
+    qb, kb, vb = bits((2, 4, 32)), bits((5, 2, 16, 32)), bits((5, 2, 16, 32))
+    up = lambda x: (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    table = np.array([[4, 1, 0], [3, 2, 0]], dtype=np.int32)
+    lens = np.array([40, 20])
+    a = ora.attention_paged_decode(qb, kb, vb, table, lens)
+    b = ora.attention_paged_decode(up(qb), up(kb), up(vb), table, lens)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("lens,table_fix", [([0], None), ([9], None), ([3], -1), ([3], 2)])
+def test_paged_decode_rejects_bad_lengths_and_pages(lens, table_fix):
+    q, kp, vp = _rand((1, 1, 4), 73), _rand((2, 1, 4, 4), 74), _rand((2, 1, 4, 4), 75)
+    table = np.array([[0, 1]], dtype=np.int32)
+    if table_fix is not None:
+        table[0, 0] = table_fix
+    with pytest.raises(ValueError):
+        ora.attention_paged_decode(q, kp, vp, table, np.array(lens))
