@@ -288,24 +288,41 @@ def run_ours(args, rank, world, local_rank):
     pre_flops = acct.attention_flops(PREFILL.B, PREFILL.Hq, PREFILL.Tq, PREFILL.Tk, PREFILL.d,
                                      PREFILL.causal)
     dec_bytes = acct.decode_bytes(DECODE.B, DECODE.Hq, DECODE.Hkv, DECODE.Tk, DECODE.d)
-    # ---- sliding-window prefill (a row beyond the specified step), timed alone
-    win_ms = None
+    def time_alone(fn, n):
+        """Average device time of n back-to-back launches of fn (ms)."""
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    # ---- rows beyond the specified step, each timed alone after it
+    win_ms = paged_ms = None
     if not args.no_extra_rows:
+        # sliding-window prefill
         qw, kw, vw = synth.make_inputs(synth.WINDOW_8K, dev)
         ow = torch.empty_like(qw)
         lw = torch.empty(qw.shape[:3], dtype=torch.float32, device=dev)
-        for _ in range(3):
-            binding.fwd(qw, kw, vw, window=synth.WINDOW_KEYS, out=ow, lse=lw)
-        torch.cuda.synchronize()
-        ew0, ew1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        n_win = 30
-        ew0.record(stream)
-        for _ in range(n_win):
-            binding.fwd(qw, kw, vw, window=synth.WINDOW_KEYS, out=ow, lse=lw)
-        ew1.record(stream)
-        torch.cuda.synchronize()
-        win_ms = ew0.elapsed_time(ew1) / n_win
+        win_ms = time_alone(
+            lambda: binding.fwd(qw, kw, vw, window=synth.WINDOW_KEYS, out=ow, lse=lw), 30)
         del qw, kw, vw, ow, lw
+        # decode against a paged cache (16-token pages, shuffled pool)
+        pw = synth.PAGED_DECODE
+        pq, pk, pv, ptab, plen = synth.make_paged_inputs(
+            pw.B, pw.Hq, pw.Hkv, pw.d, synth.PAGED_PAGE_SIZE, [pw.Tk] * pw.B, pw.seed, dev)
+        pws = torch.empty(binding.attn_decode_workspace_bytes(pw.B, pw.Hq, pw.Hkv, pw.Tk, pw.d),
+                          dtype=torch.uint8, device=dev)
+        po, pl = torch.empty_like(pq), torch.empty((pw.B, pw.Hq, 1), dtype=torch.float32,
+                                                   device=dev)
+        paged_ms = time_alone(
+            lambda: binding.decode_paged(pq, pk, pv, ptab, plen, max_seq_len=pw.Tk,
+                                         scale=pw.scale, workspace=pws, out=po, lse=pl), 100)
+        del pq, pk, pv, ptab, plen, pws, po, pl
 
     agg = aggregate_ranks(
         {"pre_s": sum(pre_ms) / 1e3, "dec_s": sum(dec_ms) / 1e3, "total_ms": total_ms,
@@ -324,6 +341,11 @@ def run_ours(args, rank, world, local_rank):
     d2h_pre = op.numel() * 2 + lp.numel() * 4
     h2d_dec = sum(t.numel() * t.element_size() for t in (qd, kd, vd))
     d2h_dec = od.numel() * 2 + ld.numel() * 4
+
+    paged_bytes = acct.paged_decode_bytes(
+        synth.PAGED_DECODE.B, synth.PAGED_DECODE.Hq, synth.PAGED_DECODE.Hkv,
+        [synth.PAGED_DECODE.Tk] * synth.PAGED_DECODE.B, synth.PAGED_DECODE.d,
+        synth.PAGED_PAGE_SIZE)
 
     if rank != 0:
         return
@@ -408,6 +430,17 @@ def run_ours(args, rank, world, local_rank):
             "frac_of_sustained_peak": round(acct.window_flops(
                 synth.WINDOW_8K.B, synth.WINDOW_8K.Hq, synth.WINDOW_8K.Tq, synth.WINDOW_8K.Tk,
                 synth.WINDOW_8K.d, synth.WINDOW_KEYS) / (win_ms / 1e3) / 1e12 / peak_tf, 4),
+        },
+        "paged_decode": None if paged_ms is None else {
+            "workload": synth.PAGED_DECODE.name,
+            "page_size": synth.PAGED_PAGE_SIZE,
+            "value": round(paged_bytes / (paged_ms / 1e3) / 1e9, 1),
+            "unit": "GB/s",
+            "ms": round(paged_ms, 4),
+            "frac_of_measured_hbm": round(paged_bytes / (paged_ms / 1e3) / 1e9 / peak_bw, 4),
+            "algorithmic_bytes_per_launch": paged_bytes,
+            "traffic": ncu_traffic("decode_split_kernel<128,4,paged>/" + synth.PAGED_DECODE.name,
+                                   source_sha(*DECODE_SOURCES)),
         },
         "gpu_launches": K * 3,
         "clocks": clk,

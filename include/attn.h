@@ -167,6 +167,51 @@ int attn_decode_noalloc(const void *q, const void *k_cache, const void *v_cache,
                         void *o, float *lse, int B, int Hq, int Hkv, int Tk, int d,
                         float scale, void *stream);
 
+/*
+ * attn_decode_paged -- decode (Tq = 1) against a paged KV cache.
+ *
+ * The cache lives in fixed-size pages of `page_size` tokens held in two
+ * pools, and each sequence lists its pages in a block table; the kernel
+ * fetches each page from wherever it sits instead of reading one
+ * contiguous cache ("Efficient attention & KV cache", section 2.5 "Paged
+ * and shared caches", and the same page's answer on what PagedAttention
+ * changes in the attention kernel).  Sequences may have different lengths
+ * and may share pages (a common prefix).
+ *
+ *   q            [B, Hq, 1, d] bf16 (device)
+ *   k_pages      [num_pages, Hkv, page_size, d] bf16 (device): page p holds,
+ *   v_pages      for every K/V head, page_size consecutive token rows
+ *   block_table  [B, max_pages_per_seq] int32 (device): entry [b][i] is the
+ *                physical page holding tokens i*page_size .. (i+1)*page_size-1
+ *                of sequence b; entries past a sequence's last page are
+ *                never read
+ *   seq_lens     [B] int32 (device): tokens in sequence b's cache,
+ *                1 <= seq_lens[b] <= max_seq_len
+ *   o, lse       [B, Hq, 1, d] bf16 and [B, Hq, 1] fp32 (device, written)
+ *   page_size    a power of two, 1 .. 4096
+ *   num_pages    pages in each pool (bounds the table entries)
+ *   max_seq_len  host-side upper bound of seq_lens, used to plan the split
+ *                along the keys; max_seq_len <= max_pages_per_seq*page_size
+ *   scale        as for attn_fwd
+ *   workspace    device scratch of at least
+ *                attn_decode_workspace_bytes(B, Hq, Hkv, max_seq_len, d)
+ *                bytes, 16-byte aligned, caller-owned (contents ignored)
+ *
+ * Query head h reads K/V head h / (Hq/Hkv), and every query token sees its
+ * whole cache, as in attn_decode.  Host-visible errors (sizes, alignment,
+ * page_size, workspace) return before anything is launched.  The lengths
+ * and table entries live on the device and are checked there: a length
+ * outside 1..max_seq_len or a page outside 0..num_pages-1 is never used to
+ * address memory (the sequence is skipped, or page 0 is read in its place),
+ * the affected rows are unspecified, and attn_device_status then reports
+ * ATTN_ERR_INVALID_ARG.
+ */
+int attn_decode_paged(const void *q, const void *k_pages, const void *v_pages,
+                      const int *block_table, const int *seq_lens, void *o, float *lse,
+                      int B, int Hq, int Hkv, int d, int page_size, int num_pages,
+                      int max_pages_per_seq, int max_seq_len, float scale,
+                      void *workspace, size_t workspace_bytes, void *stream);
+
 /* Human-readable name of a status code (never NULL). */
 const char *attn_status_string(int status);
 
@@ -177,7 +222,9 @@ const char *attn_status_string(int status);
  * Every wait inside the kernels is bounded in time.  A kernel that gives up
  * stops its work, drains its own copies and tensor-core operations, frees
  * its tensor memory, records ATTN_ERR_DEVICE_TIMEOUT here and returns, so
- * the CUDA context stays usable.  This call synchronises `stream`, copies
+ * the CUDA context stays usable.  attn_decode_paged also records
+ * ATTN_ERR_INVALID_ARG here for a device-side length or page index it could
+ * not use.  This call synchronises `stream`, copies
  * the word to *status (ATTN_OK when nothing was recorded) and resets it.
  * Returns ATTN_OK, or ATTN_ERR_CUDA if the copy fails.
  */

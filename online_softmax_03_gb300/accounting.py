@@ -63,6 +63,17 @@ def decode_bytes(B: int, Hq: int, Hkv: int, Tk: int, d: int) -> int:
     return prefill_compulsory_bytes(B, Hq, Hkv, 1, Tk, d)
 
 
+def paged_decode_bytes(B: int, Hq: int, Hkv: int, seq_lens, d: int, page_size: int) -> int:
+    """Algorithmic bytes of one paged decode call: every sequence's keys and
+    values once (per K/V head), the block-table entries of its pages, its
+    length, q read and o, lse written."""
+    lens = [int(n) for n in seq_lens]
+    kv = sum(2 * Hkv * n * d * BF16_BYTES for n in lens)
+    table = sum(-(-n // page_size) for n in lens) * 4
+    q_o = 2 * B * Hq * d * BF16_BYTES
+    return kv + table + 4 * B + q_o + B * Hq * LSE_BYTES
+
+
 def decode_flops(B: int, Hq: int, Tk: int, d: int) -> float:
     return attention_flops(B, Hq, 1, Tk, d, causal=False)
 

@@ -1,8 +1,8 @@
 """Thin ctypes binding over libattn.so (the C ABI in include/attn.h).
 
 The functions named like the C entry points (attn_fwd, attn_decode, ...)
-take raw integers and pointers exactly as the C ABI does.  `fwd` and
-`decode` marshal torch CUDA tensors into those calls: they check dtype,
+take raw integers and pointers exactly as the C ABI does.  `fwd`, `decode`
+and `decode_paged` marshal torch CUDA tensors into those calls: they check dtype,
 device, layout and shapes, allocate the outputs with torch, and pass the
 current CUDA stream.  All attention arithmetic runs in the library's
 kernels; if the library is missing these functions raise instead of
@@ -57,6 +57,9 @@ def load_library():
             lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp,
                                         ctypes.c_size_t, vp]
             lib.attn_decode.restype = i
+            lib.attn_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i,
+                                              i, i, f, vp, ctypes.c_size_t, vp]
+            lib.attn_decode_paged.restype = i
             lib.attn_status_string.argtypes = [i]
             lib.attn_status_string.restype = ctypes.c_char_p
             lib.attn_device_status.argtypes = [vp, ctypes.POINTER(i)]
@@ -87,6 +90,15 @@ def attn_decode(q, k_cache, v_cache, o, lse, B, Hq, Hkv, Tk, d, scale, workspace
                 workspace_bytes, stream) -> int:
     return load_library().attn_decode(q, k_cache, v_cache, o, lse, B, Hq, Hkv, Tk, d,
                                       scale, workspace, workspace_bytes, stream)
+
+
+def attn_decode_paged(q, k_pages, v_pages, block_table, seq_lens, o, lse, B, Hq, Hkv, d,
+                      page_size, num_pages, max_pages_per_seq, max_seq_len, scale, workspace,
+                      workspace_bytes, stream) -> int:
+    return load_library().attn_decode_paged(q, k_pages, v_pages, block_table, seq_lens, o, lse,
+                                            B, Hq, Hkv, d, page_size, num_pages,
+                                            max_pages_per_seq, max_seq_len, scale, workspace,
+                                            workspace_bytes, stream)
 
 
 def attn_status_string(status: int) -> str:
@@ -193,4 +205,50 @@ def decode(q, k_cache, v_cache, scale: float | None = None, workspace=None, out=
                      workspace.numel() * workspace.element_size(), _stream_handle(stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_decode")
+    return out, lse
+
+
+def decode_paged(q, k_pages, v_pages, block_table, seq_lens, max_seq_len: int | None = None,
+                 scale: float | None = None, workspace=None, out=None, lse=None, stream=None):
+    """O, LSE for one query token per sequence against a paged cache.
+
+    q [B,Hq,1,d] bf16; k_pages, v_pages [num_pages,Hkv,page_size,d] bf16;
+    block_table [B,max_pages] int32 and seq_lens [B] int32, all on the GPU.
+    max_seq_len bounds seq_lens (it plans the split along the keys); when
+    omitted it is taken to be the table's capacity, max_pages*page_size.
+    """
+    import torch
+
+    for t, n in ((q, "q"), (k_pages, "k_pages"), (v_pages, "v_pages")):
+        _check_tensor(t, n, 4)
+    B, Hq, Tq, d = q.shape
+    num_pages, Hkv, page_size, dk = k_pages.shape
+    if Tq != 1 or dk != d or tuple(v_pages.shape) != tuple(k_pages.shape):
+        raise ValueError("decode_paged expects q [B,Hq,1,d] and pages [num_pages,Hkv,page_size,d]")
+    for t, n, shape in ((block_table, "block_table", None), (seq_lens, "seq_lens", (B,))):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.int32 or t.device != q.device \
+                or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous int32 tensor on {q.device}")
+    if block_table.dim() != 2 or block_table.shape[0] != B or tuple(seq_lens.shape) != (B,):
+        raise ValueError("block_table must be [B, max_pages] and seq_lens [B]")
+    max_pages = block_table.shape[1]
+    if max_seq_len is None:
+        max_seq_len = max_pages * page_size
+    if workspace is None:
+        n = attn_decode_workspace_bytes(B, Hq, Hkv, int(max_seq_len), d)
+        if n == 0:
+            raise ValueError("invalid decode sizes")
+        workspace = torch.empty((n + 15) // 16 * 16, dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, 1), dtype=torch.float32, device=q.device)
+    rc = attn_decode_paged(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(),
+                           block_table.data_ptr(), seq_lens.data_ptr(), out.data_ptr(),
+                           lse.data_ptr(), B, Hq, Hkv, d, page_size, num_pages, max_pages,
+                           int(max_seq_len), 0.0 if scale is None else float(scale),
+                           workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                           _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_decode_paged")
     return out, lse

@@ -177,6 +177,50 @@ ATTN_API int attn_decode(const void *q, const void *k_cache, const void *v_cache
   return attn_host::decode_launch(a);
 }
 
+ATTN_API int attn_decode_paged(const void *q, const void *k_pages, const void *v_pages,
+                               const int *block_table, const int *seq_lens, void *o,
+                               float *lse, int B, int Hq, int Hkv, int d, int page_size,
+                               int num_pages, int max_pages_per_seq, int max_seq_len,
+                               float scale, void *workspace, size_t workspace_bytes,
+                               void *stream) {
+  float sc = 0.f;
+  int rc = validate(q, k_pages, v_pages, o, lse, B, Hq, Hkv, 1, max_seq_len, d, 0, scale, &sc);
+  if (rc != ATTN_OK) return rc;
+  if (!block_table || !seq_lens) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(block_table, 4) || !aligned(seq_lens, 4)) return ATTN_ERR_MISALIGNED;
+  if (page_size < 1 || page_size > 4096 || (page_size & (page_size - 1)) != 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (num_pages < 1 || max_pages_per_seq < 1 ||
+      (long long)max_seq_len > (long long)max_pages_per_seq * page_size)
+    return ATTN_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 16) ||
+      workspace_bytes < attn_decode_workspace_bytes(B, Hq, Hkv, max_seq_len, d))
+    return ATTN_ERR_WORKSPACE;
+  attn_host::DecodeArgs a;
+  a.q = q;
+  a.k = k_pages;
+  a.v = v_pages;
+  a.o = o;
+  a.lse = lse;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.Tk = max_seq_len;
+  a.d = d;
+  a.scale = sc;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  a.stream = static_cast<cudaStream_t>(stream);
+  a.wait_ns = g_wait_ns.load();
+  a.paged = true;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.page_size = page_size;
+  a.num_pages = num_pages;
+  a.max_pages = max_pages_per_seq;
+  return attn_host::decode_launch(a);
+}
+
 ATTN_API const char *attn_status_string(int status) {
   switch (status) {
     case ATTN_OK: return "ATTN_OK";

@@ -9,10 +9,10 @@
 namespace {
 __device__ unsigned int g_decode_status;
 
-template <int D, int GP>
+template <int D, int GP, bool kPaged>
 int launch_split(const attn_dev::DecodeParams &p, dim3 grid, cudaStream_t st) {
   using C = attn_dev::DecodeCfg<D, GP>;
-  auto kern = attn_dev::decode_split_kernel<D, GP>;
+  auto kern = attn_dev::decode_split_kernel<D, GP, kPaged>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)C::SMEM_BYTES) != cudaSuccess)
     return ATTN_ERR_CUDA;
@@ -23,7 +23,7 @@ int launch_split(const attn_dev::DecodeParams &p, dim3 grid, cudaStream_t st) {
 template <int D, int GP>
 int resident_ctas(int *out) {
   using C = attn_dev::DecodeCfg<D, GP>;
-  auto kern = attn_dev::decode_split_kernel<D, GP>;
+  auto kern = attn_dev::decode_split_kernel<D, GP, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)C::SMEM_BYTES) != cudaSuccess ||
       cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, kern, C::THREADS,
@@ -33,8 +33,11 @@ int resident_ctas(int *out) {
 }
 
 template <int D>
-int dispatch_split(int gp, const attn_dev::DecodeParams &p, dim3 grid, cudaStream_t st) {
-  return gp == 4 ? launch_split<D, 4>(p, grid, st) : launch_split<D, 8>(p, grid, st);
+int dispatch_split(int gp, bool paged, const attn_dev::DecodeParams &p, dim3 grid,
+                   cudaStream_t st) {
+  if (paged)
+    return gp == 4 ? launch_split<D, 4, true>(p, grid, st) : launch_split<D, 8, true>(p, grid, st);
+  return gp == 4 ? launch_split<D, 4, false>(p, grid, st) : launch_split<D, 8, false>(p, grid, st);
 }
 
 template <int D>
@@ -116,11 +119,17 @@ int decode_launch(const DecodeArgs &a) {
   p.n_hc = n_hc;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.wait_ns = a.wait_ns;
+  p.block_table = a.block_table;
+  p.seq_lens = a.seq_lens;
+  p.page_shift = 0;
+  while (a.paged && (1 << p.page_shift) < a.page_size) ++p.page_shift;
+  p.max_pages = a.max_pages;
+  p.num_pages = a.num_pages;
   const dim3 grid(nsplit, a.Hkv * n_hc, a.B);
   switch (a.d) {
-    case 32: rc = dispatch_split<32>(gp, p, grid, a.stream); break;
-    case 64: rc = dispatch_split<64>(gp, p, grid, a.stream); break;
-    default: rc = dispatch_split<128>(gp, p, grid, a.stream); break;
+    case 32: rc = dispatch_split<32>(gp, a.paged, p, grid, a.stream); break;
+    case 64: rc = dispatch_split<64>(gp, a.paged, p, grid, a.stream); break;
+    default: rc = dispatch_split<128>(gp, a.paged, p, grid, a.stream); break;
   }
   if (rc != ATTN_OK) return rc;
   const unsigned cblocks = (unsigned)((rows + 3) / 4);

@@ -23,6 +23,13 @@
 //    lanes over head-dim columns.  Products use packed fp32x2 FMAs.  The
 //    warps' partial (m, l, acc) are merged in shared memory and written to
 //    the workspace.
+//    With kPaged the cache is a pool of pages and each sequence a list of
+//    page numbers ("Efficient attention & KV cache", section 2.5): the
+//    producer looks each tile's page(s) up in the block table and copies
+//    the rows from there, one bulk copy per page piece; everything the
+//    consumers do is unchanged.  Per-sequence lengths come from the device,
+//    so a split may find no keys at all; it then writes an empty partial
+//    (m = -inf, l = 0, acc = 0), which the merge weighs with 0.
 //  * decode_combine_kernel: one warp per (batch, query head) merges the
 //    splits with the same rescaling (m* = max m_s, weights e^(m_s - m*)),
 //    writes O as bf16 and LSE in natural log.
@@ -37,11 +44,12 @@
 namespace attn_dev {
 
 constexpr unsigned int kDecodeStatusTimeout = 6;  // ATTN_ERR_DEVICE_TIMEOUT
+constexpr unsigned int kDecodeStatusBadArg = 1;   // ATTN_ERR_INVALID_ARG
 
 struct DecodeParams {
   const __nv_bfloat16 *q;   // [B, Hq, 1, D]
-  const __nv_bfloat16 *k;   // [B, Hkv, Tk, D]
-  const __nv_bfloat16 *v;   // [B, Hkv, Tk, D]
+  const __nv_bfloat16 *k;   // [B, Hkv, Tk, D], paged: [num_pages, Hkv, page, D]
+  const __nv_bfloat16 *v;   // same layout as k
   float *part_acc;          // [B*Hq, nsplit, D]
   float *part_ml;           // [B*Hq, nsplit, 2]  (m in log2 units, l)
   unsigned int *status;
@@ -50,6 +58,11 @@ struct DecodeParams {
   int n_hc;                 // head chunks of GP per K/V head
   float scale_log2;
   unsigned long long wait_ns;
+  // paged cache only (Tk is then the longest allowed sequence)
+  const int *block_table;   // [B, max_pages]
+  const int *seq_lens;      // [B]
+  int page_shift;           // log2(page size)
+  int max_pages, num_pages;
 };
 
 template <int D, int GP>
@@ -109,7 +122,7 @@ __device__ __forceinline__ void load_bf16_row(const uint8_t *src, float (&f)[VEC
   }
 }
 
-template <int D, int GP>
+template <int D, int GP, bool kPaged>
 __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS)
     decode_split_kernel(const DecodeParams p) {
   using C = DecodeCfg<D, GP>;
@@ -130,10 +143,19 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS)
   const int b = blockIdx.z;
   const int h0 = hk * p.group + hc * GP;          // first query head served
   const int nh = min(GP, p.group - hc * GP);      // query heads served
+  int seq_len = p.Tk;
+  if constexpr (kPaged) {
+    seq_len = p.seq_lens[b];
+    if (seq_len < 1 || seq_len > p.Tk) {  // never used to address memory
+      if (threadIdx.x == 0) atomicMax(p.status, kDecodeStatusBadArg);
+      seq_len = 0;
+    }
+  }
   const int k0 = sidx * p.chunk;
-  const int len = min(p.Tk, k0 + p.chunk) - k0;   // >= 1 (host guarantees)
+  // contiguous: >= 1 (host guarantees); paged: 0 for splits past the end
+  const int len = max(0, min(seq_len, k0 + p.chunk) - k0);
   const int ntiles = (len + C::TILE - 1) / C::TILE;
-  const size_t kv_off = ((size_t)(b * p.Hkv + hk) * p.Tk + k0) * D;
+  const size_t kv_off = kPaged ? 0 : ((size_t)(b * p.Hkv + hk) * p.Tk + k0) * D;
   const uint8_t *kg = reinterpret_cast<const uint8_t *>(p.k + kv_off);
   const uint8_t *vg = reinterpret_cast<const uint8_t *>(p.v + kv_off);
 
@@ -154,16 +176,38 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS)
       for (int t = 0; t < ntiles; ++t) {
         const int s = t % ST, u = t / ST;
         if (t >= ST && !mbar_wait(&empty[s], (u - 1) & 1, p.wait_ns)) {
-          atomicExch(p.status, kDecodeStatusTimeout);
+          atomicMax(p.status, kDecodeStatusTimeout);
           break;
         }
         const int rows = min(C::TILE, len - t * C::TILE);
         const uint32_t bytes = rows * C::ROW_BYTES;
         mbar_arrive_expect_tx(&full[s], 2 * bytes);
-        bulk_load(smem + C::OFF_K + s * C::TILE_BYTES, kg + (size_t)t * C::TILE_BYTES,
-                  bytes, &full[s]);
-        bulk_load(smem + C::OFF_V + s * C::TILE_BYTES, vg + (size_t)t * C::TILE_BYTES,
-                  bytes, &full[s]);
+        uint8_t *dk = smem + C::OFF_K + s * C::TILE_BYTES;
+        uint8_t *dv = smem + C::OFF_V + s * C::TILE_BYTES;
+        if constexpr (kPaged) {
+          // The tile's keys k0 + t*TILE + [0, rows) may span several pages:
+          // one copy per piece that lies within one page.
+          const int page = 1 << p.page_shift;
+          const int *table = p.block_table + (size_t)b * p.max_pages;
+          for (int r = 0; r < rows;) {
+            const int key = k0 + t * C::TILE + r;
+            const int off = key & (page - 1);
+            const int n = min(rows - r, page - off);
+            int phys = __ldg(table + (key >> p.page_shift));
+            if ((unsigned)phys >= (unsigned)p.num_pages) {  // read page 0 instead
+              atomicMax(p.status, kDecodeStatusBadArg);
+              phys = 0;
+            }
+            const size_t src =
+                ((((size_t)phys * p.Hkv + hk) << p.page_shift) + off) * C::ROW_BYTES;
+            bulk_load(dk + r * C::ROW_BYTES, kg + src, n * C::ROW_BYTES, &full[s]);
+            bulk_load(dv + r * C::ROW_BYTES, vg + src, n * C::ROW_BYTES, &full[s]);
+            r += n;
+          }
+        } else {
+          bulk_load(dk, kg + (size_t)t * C::TILE_BYTES, bytes, &full[s]);
+          bulk_load(dv, vg + (size_t)t * C::TILE_BYTES, bytes, &full[s]);
+        }
         last[s] = t;
       }
       for (int s = 0; s < ST; ++s)
@@ -308,7 +352,7 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS)
     }
     if (lane == 0) mbar_arrive(&empty[s]);
   }
-  if (!ok) atomicExch(p.status, kDecodeStatusTimeout);
+  if (!ok) atomicMax(p.status, kDecodeStatusTimeout);
   float acc[GP][VEC];
 #pragma unroll
   for (int hh = 0; hh < GP; ++hh) {

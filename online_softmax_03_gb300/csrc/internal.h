@@ -24,12 +24,17 @@ struct DecodeArgs {
   const void *q, *k, *v;
   void *o;
   float *lse;
-  int B, Hq, Hkv, Tk, d;
+  int B, Hq, Hkv, Tk, d;  // paged: Tk = the longest allowed sequence
   float scale;
   void *workspace;
   size_t workspace_bytes;
   cudaStream_t stream;
   unsigned long long wait_ns;
+  // paged cache (k, v are page pools [num_pages, Hkv, page_size, d])
+  bool paged = false;
+  const int *block_table = nullptr;
+  const int *seq_lens = nullptr;
+  int page_size = 0, num_pages = 0, max_pages = 0;
 };
 
 // Return an attn_status code.

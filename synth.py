@@ -77,6 +77,13 @@ WINDOW_KEYS = 1024
 WINDOW_8K = Workload("window_b4_h32_t8192_d128_w1024", 4, 32, 32, 8192, 8192, 128, True,
                      "normal", 6)
 
+# Paged-cache decode measured beside the specified workloads: the decode
+# workload's shapes with the cache cut into 16-token pages placed in a
+# shuffled pool.
+PAGED_DECODE = Workload("paged_decode_b64_hq32_hkv8_tk8192_d128_p16", 64, 32, 8, 1, 8192,
+                        128, False, "normal", 5, decode=True)
+PAGED_PAGE_SIZE = 16
+
 ALL = (TINY, TINY_NONCAUSAL, PREFILL_1K, PREFILL_4K, LONG_8K_CAUSAL, LONG_8K_FULL,
        LONG_8000_CAUSAL, LONG_8000_FULL, DECODE_GQA)
 
@@ -125,3 +132,38 @@ def sample_rows(w: Workload, n: int, seed: int = 1234):
     fixed_i = torch.tensor([0, w.Tq - 1, 0, w.Tq - 1])
     return (torch.cat([fixed_b, b]).numpy(), torch.cat([fixed_h, h]).numpy(),
             torch.cat([fixed_i, i]).numpy())
+
+
+def make_paged_inputs(B: int, Hq: int, Hkv: int, d: int, page_size: int, seq_lens,
+                      seed: int, device="cpu", spare_pages: int = 0, max_pages=None):
+    """Draw a paged decode problem: q [B,Hq,1,d], k_pages and v_pages
+    [num_pages,Hkv,page_size,d] (bf16), block_table [B,max_pages] and
+    seq_lens [B] (int32).
+
+    Sequence b needs ceil(seq_lens[b]/page_size) pages; the pool holds
+    those plus `spare_pages` unused ones.  Which physical page serves which
+    (sequence, logical page) is a seeded random permutation (CPU generator,
+    seed + 1), so neighbouring logical pages are scattered over the pool.
+    Table entries past a sequence's last page are -1 (never read).  q, then
+    the K pool, then the V pool are drawn N(0,1) in fp32 on `device` from a
+    generator seeded with `seed` and rounded to bf16.
+    """
+    device = torch.device(device)
+    lens = [int(x) for x in seq_lens]
+    need = [-(-n // page_size) for n in lens]
+    num_pages = sum(need) + spare_pages
+    width = max(need) if max_pages is None else max_pages
+    perm = torch.randperm(num_pages, generator=torch.Generator().manual_seed(seed + 1))
+    table = torch.full((B, width), -1, dtype=torch.int32)
+    at = 0
+    for b, n in enumerate(need):
+        table[b, :n] = perm[at:at + n].to(torch.int32)
+        at += n
+    g = torch.Generator(device=device).manual_seed(seed)
+    q = torch.randn((B, Hq, 1, d), generator=g, dtype=torch.float32, device=device)
+    kp = torch.randn((num_pages, Hkv, page_size, d), generator=g, dtype=torch.float32,
+                     device=device)
+    vp = torch.randn((num_pages, Hkv, page_size, d), generator=g, dtype=torch.float32,
+                     device=device)
+    return (q.to(torch.bfloat16), kp.to(torch.bfloat16), vp.to(torch.bfloat16),
+            table.to(device), torch.tensor(lens, dtype=torch.int32, device=device))

@@ -26,7 +26,8 @@ def _declared_functions():
 
 def test_header_declares_the_entry_points():
     names = _declared_functions()
-    for n in ("attn_fwd", "attn_decode", "attn_decode_workspace_bytes",
+    for n in ("attn_fwd", "attn_fwd_window", "attn_decode", "attn_decode_paged",
+              "attn_decode_noalloc", "attn_decode_workspace_bytes",
               "attn_status_string", "attn_device_status", "attn_debug_set"):
         assert n in names
 
@@ -129,6 +130,43 @@ def _decode(**kw):
 ])
 def test_decode_rejects_bad_arguments_on_the_host(lib, kw, code):
     assert _decode(**kw) == code
+
+
+T_, S_ = 0x70000, 0x80000  # fake table and length addresses (4-byte aligned)
+
+
+def _decode_paged(**kw):
+    a = dict(q=Q, k=K, v=V, table=T_, lens=S_, o=O, lse=L, B=2, Hq=8, Hkv=2, d=128,
+             page_size=16, num_pages=64, max_pages=8, max_len=100, scale=0.0, ws=W,
+             ws_bytes=1 << 20)
+    a.update(kw)
+    return binding.attn_decode_paged(a["q"], a["k"], a["v"], a["table"], a["lens"], a["o"],
+                                     a["lse"], a["B"], a["Hq"], a["Hkv"], a["d"],
+                                     a["page_size"], a["num_pages"], a["max_pages"],
+                                     a["max_len"], a["scale"], a["ws"], a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), binding.ATTN_ERR_INVALID_ARG),
+    (dict(table=None), binding.ATTN_ERR_INVALID_ARG),
+    (dict(lens=None), binding.ATTN_ERR_INVALID_ARG),
+    (dict(Hq=8, Hkv=3), binding.ATTN_ERR_INVALID_ARG),
+    (dict(max_len=0), binding.ATTN_ERR_INVALID_ARG),
+    (dict(max_len=129), binding.ATTN_ERR_INVALID_ARG),   # > max_pages * page_size
+    (dict(page_size=0), binding.ATTN_ERR_INVALID_ARG),
+    (dict(page_size=24), binding.ATTN_ERR_INVALID_ARG),  # not a power of two
+    (dict(page_size=8192), binding.ATTN_ERR_INVALID_ARG),
+    (dict(num_pages=0), binding.ATTN_ERR_INVALID_ARG),
+    (dict(max_pages=0), binding.ATTN_ERR_INVALID_ARG),
+    (dict(d=96), binding.ATTN_ERR_UNSUPPORTED),
+    (dict(v=V + 8), binding.ATTN_ERR_MISALIGNED),
+    (dict(table=T_ + 2), binding.ATTN_ERR_MISALIGNED),
+    (dict(lens=S_ + 1), binding.ATTN_ERR_MISALIGNED),
+    (dict(ws=None), binding.ATTN_ERR_WORKSPACE),
+    (dict(ws_bytes=64), binding.ATTN_ERR_WORKSPACE),
+])
+def test_decode_paged_rejects_bad_arguments_on_the_host(lib, kw, code):
+    assert _decode_paged(**kw) == code
 
 
 def test_library_has_no_oracle_dependency():

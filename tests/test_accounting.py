@@ -51,3 +51,13 @@ def test_visible_pairs_and_window_flops():
     assert acc.visible_pairs(T, T, True, W) == W * (W + 1) // 2 + (T - W) * W
     assert acc.window_flops(4, 32, T, T, 128, W) == 4.0 * 128 * 4 * 32 * acc.visible_pairs(T, T, True, W)
     assert acc.visible_pairs(6, 9, False) == 54
+
+
+def test_paged_decode_bytes():
+    """Full-length sequences cost the contiguous decode bytes plus one 4-byte
+    table entry per page and one length per sequence."""
+    base = acc.decode_bytes(64, 32, 8, 8192, 128)
+    assert acc.paged_decode_bytes(64, 32, 8, [8192] * 64, 128, 16) == base + 64 * 512 * 4 + 64 * 4
+    # ragged: K/V bytes follow the lengths, pages round up
+    assert acc.paged_decode_bytes(2, 4, 2, [1, 17], 64, 16) == (
+        2 * 2 * 18 * 64 * 2 + (1 + 2) * 4 + 2 * 4 + 2 * 2 * 4 * 64 * 2 + 2 * 4 * 4)
