@@ -524,3 +524,89 @@ int oracle_attn_paged_decode(const void *q, const void *k_pages,
   }
   return status;
 }
+
+/*
+ * Packed variable-length batches: B sequences concatenated without padding,
+ * sequence b owning query rows cu_q[b] .. cu_q[b+1]-1 and key rows
+ * cu_k[b] .. cu_k[b+1]-1 ("SDPA and FlashAttention's tiling", the packed
+ * flash_attn_varlen_func call: cumulative int32 offsets of length B+1, and
+ * no score between two documents is ever formed).  Each sequence is an
+ * independent attention problem with the definition at the top of this
+ * file (causal: bottom-right aligned inside the sequence).
+ *
+ * Layout (token-major, as packed activations come):
+ *   q, o  [total_q, Hq, d]      k, v  [total_k, Hkv, d]     lse  [Hq, total_q]
+ * Offsets must start at 0, never decrease and end within total_q /
+ * total_k; a sequence with queries needs at least one key, and causal
+ * needs at most as many queries as keys.  Rows not covered by any sequence
+ * are left untouched.
+ */
+int oracle_attn_varlen(const void *q, const void *k, const void *v, int in_type,
+                       const int *cu_q, const int *cu_k, int B, int Hq, int Hkv,
+                       int total_q, int total_k, int d, int causal, double scale,
+                       double *o, double *lse) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || d < 1 || total_q < 0 || total_k < 0 ||
+      Hq % Hkv != 0 || cu_q[0] != 0 || cu_k[0] != 0)
+    return ORACLE_ERR_ARG;
+  for (int b = 0; b < B; ++b) {
+    const int nq = cu_q[b + 1] - cu_q[b], nk = cu_k[b + 1] - cu_k[b];
+    if (nq < 0 || nk < 0 || cu_q[b + 1] > total_q || cu_k[b + 1] > total_k)
+      return ORACLE_ERR_ARG;
+    if (nq > 0 && nk < 1) return ORACLE_ERR_ARG;
+    if (causal && nq > nk) return ORACLE_ERR_ARG;
+  }
+  const int group = Hq / Hkv;
+  int status = ORACLE_OK;
+
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+  for (int b = 0; b < B; ++b) {
+    for (int h = 0; h < Hq; ++h) {
+      const int nq = cu_q[b + 1] - cu_q[b], nk = cu_k[b + 1] - cu_k[b];
+      if (nq == 0) continue;
+      const int g = h / group;
+      double *qi = malloc(sizeof(double) * d);
+      double *row = malloc(sizeof(double) * d);
+      double *s = malloc(sizeof(double) * (size_t)nk);
+      if (!qi || !row || !s) {
+#pragma omp atomic write
+        status = ORACLE_ERR_NOMEM;
+        free(qi); free(row); free(s);
+        continue;
+      }
+      for (int i = 0; i < nq; ++i) {
+        const size_t qrow = (size_t)cu_q[b] + i;
+        load_rows(q, in_type, (qrow * Hq + h) * (size_t)d, 0, 1, d, qi);
+        double m = -INFINITY;
+        for (int j = 0; j < nk; ++j) {
+          if (!visible(i, j, nq, nk, causal, 0)) {
+            s[j] = -INFINITY;
+            continue;
+          }
+          const size_t krow = (size_t)cu_k[b] + j;
+          load_rows(k, in_type, (krow * Hkv + g) * (size_t)d, 0, 1, d, row);
+          double acc = 0.0;
+          for (int c = 0; c < d; ++c) acc += qi[c] * row[c];
+          s[j] = scale * acc;
+          if (s[j] > m) m = s[j];
+        }
+        double denom = 0.0;
+        for (int j = 0; j < nk; ++j) {
+          s[j] = (s[j] == -INFINITY) ? 0.0 : exp(s[j] - m);
+          denom += s[j];
+        }
+        double *orow = &o[(qrow * Hq + h) * (size_t)d];
+        for (int c = 0; c < d; ++c) orow[c] = 0.0;
+        for (int j = 0; j < nk; ++j) {
+          if (s[j] == 0.0) continue;
+          const size_t krow = (size_t)cu_k[b] + j;
+          load_rows(v, in_type, (krow * Hkv + g) * (size_t)d, 0, 1, d, row);
+          const double pj = s[j] / denom;
+          for (int c = 0; c < d; ++c) orow[c] += pj * row[c];
+        }
+        lse[(size_t)h * total_q + qrow] = m + log(denom);
+      }
+      free(qi); free(row); free(s);
+    }
+  }
+  return status;
+}

@@ -69,9 +69,11 @@ def _load():
                                                      vp]
             lib.oracle_attn_paged_decode.argtypes = [vp, vp, vp, ip, vp, vp, ip, ip,
                                                      ip, ip, ip, ip, ip, dp, vp, vp]
+            lib.oracle_attn_varlen.argtypes = [vp, vp, vp, ip, vp, vp, ip, ip, ip, ip,
+                                               ip, ip, ip, dp, vp, vp]
             for f in (lib.oracle_attn_dense, lib.oracle_attn_rows,
                       lib.oracle_attn_blocked, lib.oracle_online_softmax_1d,
-                      lib.oracle_attn_paged_decode):
+                      lib.oracle_attn_paged_decode, lib.oracle_attn_varlen):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -220,6 +222,34 @@ def attention_paged_decode(q, k_pages, v_pages, block_table, seq_lens, scale=Non
     rc = _load().oracle_attn_paged_decode(_ptr(qa), _ptr(ka), _ptr(va), tq, _ptr(table),
                                           _ptr(lens), B, Hq, Hkv, d, page_size, num_pages,
                                           table.shape[1], scale, _ptr(o), _ptr(lse))
+    _check(rc)
+    return o, lse
+
+
+def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, causal=False, scale=None):
+    """Packed variable-length attention.
+
+    q [total_q, Hq, d]; k, v [total_k, Hkv, d]; cu_seqlens_q / _k int [B+1].
+    Returns (o [total_q, Hq, d], lse [Hq, total_q]) in float64; rows outside
+    every sequence are NaN.
+    """
+    if q.ndim != 3 or k.ndim != 3 or v.shape != k.shape or q.shape[2] != k.shape[2]:
+        raise ValueError("q must be [total_q, Hq, d] and k, v [total_k, Hkv, d]")
+    total_q, Hq, d = q.shape
+    total_k, Hkv, _ = k.shape
+    (qa, tq), (ka, tk), (va, tv) = _as_input(q), _as_input(k), _as_input(v)
+    if not tq == tk == tv:
+        raise TypeError("q, k, v must share one input type")
+    cq = np.ascontiguousarray(cu_seqlens_q, dtype=np.int32)
+    ck = np.ascontiguousarray(cu_seqlens_k, dtype=np.int32)
+    if cq.ndim != 1 or cq.shape != ck.shape or cq.size < 2:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must both be [B+1]")
+    scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+    o = np.full((total_q, Hq, d), np.nan)
+    lse = np.full((Hq, total_q), np.nan)
+    rc = _load().oracle_attn_varlen(_ptr(qa), _ptr(ka), _ptr(va), tq, _ptr(cq), _ptr(ck),
+                                    cq.size - 1, Hq, Hkv, total_q, total_k, d,
+                                    int(bool(causal)), scale, _ptr(o), _ptr(lse))
     _check(rc)
     return o, lse
 

@@ -483,3 +483,76 @@ def test_paged_decode_rejects_bad_lengths_and_pages(lens, table_fix):
         table[0, 0] = table_fix
     with pytest.raises(ValueError):
         ora.attention_paged_decode(q, kp, vp, table, np.array(lens))
+
+
+# --- packed variable-length batches ("SDPA and FlashAttention's tiling",
+# flash_attn_varlen_func with cu_seqlens) ---------------------------------
+
+def _pack(xs):
+    """List of [H, T_b, d] arrays -> packed [sum T_b, H, d] and offsets."""
+    cu = np.concatenate([[0], np.cumsum([x.shape[1] for x in xs])]).astype(np.int32)
+    return np.concatenate([x.transpose(1, 0, 2) for x in xs], axis=0), cu
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_each_sequence_is_its_own_dense_problem(causal):
+    """Every sequence of the pack equals the dense definition run on that
+    sequence alone (GQA 3, Tq < Tk per sequence, ragged lengths, an empty
+    query sequence)."""
+    Hq, Hkv, d = 6, 2, 8
+    lq, lk = [5, 0, 17, 1], [9, 4, 17, 3]
+    qs = [_rand((Hq, n, d), 80 + i) for i, n in enumerate(lq)]
+    ks = [_rand((Hkv, n, d), 90 + i) for i, n in enumerate(lk)]
+    vs = [_rand((Hkv, n, d), 100 + i) for i, n in enumerate(lk)]
+    (q, cq), (k, ck), (v, _) = _pack(qs), _pack(ks), _pack(vs)
+    o, lse = ora.attention_varlen(q, k, v, cq, ck, causal=causal)
+    for b in range(len(lq)):
+        if lq[b] == 0:
+            continue
+        od, ld, _ = ora.attention_dense(qs[b][None], ks[b][None], vs[b][None], causal=causal)
+        np.testing.assert_allclose(o[cq[b]:cq[b + 1]], od[0].transpose(1, 0, 2), rtol=0, atol=1e-14)
+        np.testing.assert_allclose(lse[:, cq[b]:cq[b + 1]], ld[0], rtol=0, atol=1e-14)
+
+
+def test_varlen_no_score_crosses_documents():
+    """Changing one document's keys and values leaves every other document's
+    rows bit-identical (nothing attends across the pack)."""
+    lens = [7, 12, 3]
+    H, d = 2, 4
+    q, cu = _pack([_rand((H, n, d), 110 + i) for i, n in enumerate(lens)])
+    k, _ = _pack([_rand((H, n, d), 120 + i) for i, n in enumerate(lens)])
+    v, _ = _pack([_rand((H, n, d), 130 + i) for i, n in enumerate(lens)])
+    o, lse = ora.attention_varlen(q, k, v, cu, cu, causal=True)
+    k2, v2 = k.copy(), v.copy()
+    k2[cu[1]:cu[2]] *= -3.0
+    v2[cu[1]:cu[2]] += 5.0
+    o2, lse2 = ora.attention_varlen(q, k2, v2, cu, cu, causal=True)
+    for b in (0, 2):
+        sl = slice(cu[b], cu[b + 1])
+        np.testing.assert_array_equal(o[sl], o2[sl])
+        np.testing.assert_array_equal(lse[:, sl], lse2[:, sl])
+    assert np.abs(o[cu[1]:cu[2]] - o2[cu[1]:cu[2]]).max() > 0.1
+
+
+def test_varlen_equal_lengths_is_the_batched_dense_problem():
+    B, H, T, d = 3, 4, 11, 8
+    q4, k4, v4 = _rand((B, H, T, d), 140), _rand((B, H, T, d), 141), _rand((B, H, T, d), 142)
+    od, ld, _ = ora.attention_dense(q4, k4, v4, causal=True)
+    pk = lambda x: x.transpose(0, 2, 1, 3).reshape(B * T, H, d)
+    cu = np.arange(0, B * T + 1, T, dtype=np.int32)
+    o, lse = ora.attention_varlen(pk(q4), pk(k4), pk(v4), cu, cu, causal=True)
+    np.testing.assert_allclose(o, pk(od), rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lse, ld.transpose(1, 0, 2).reshape(H, B * T), rtol=0, atol=1e-14)
+
+
+@pytest.mark.parametrize("cq,ck,causal", [
+    ([1, 3], [0, 3], False),      # must start at 0
+    ([0, 3, 2], [0, 3, 5], False),  # decreasing
+    ([0, 3], [0, 0], False),      # queries without keys
+    ([0, 4], [0, 3], True),       # causal with more queries than keys
+    ([0, 9], [0, 3], False),      # past total_q
+])
+def test_varlen_rejects_bad_offsets(cq, ck, causal):
+    q, k = _rand((8, 1, 4), 150), _rand((5, 1, 4), 151)
+    with pytest.raises(ValueError):
+        ora.attention_varlen(q, k, k, cq, ck, causal=causal)
