@@ -302,7 +302,8 @@ def run_ours(args, rank, world, local_rank):
         return e0.elapsed_time(e1) / n
 
     # ---- rows beyond the specified step, each timed alone after it
-    win_ms = paged_ms = None
+    win_ms = paged_ms = varlen_ms = None
+    varlen_flops = varlen_docs = 0
     if not args.no_extra_rows:
         # sliding-window prefill
         qw, kw, vw = synth.make_inputs(synth.WINDOW_8K, dev)
@@ -323,6 +324,23 @@ def run_ours(args, rank, world, local_rank):
             lambda: binding.decode_paged(pq, pk, pv, ptab, plen, max_seq_len=pw.Tk,
                                          scale=pw.scale, workspace=pws, out=po, lse=pl), 100)
         del pq, pk, pv, ptab, plen, pws, po, pl
+        # packed variable-length prefill (documents of mixed length)
+        vw = synth.VARLEN
+        vlens = synth.packed_lengths(synth.VARLEN_TOKENS, vw.seed)
+        vq, vk, vv, vcq, vck = synth.make_varlen_inputs(vlens, vlens, vw.Hq, vw.Hkv, vw.d,
+                                                        vw.seed, dev)
+        vo = torch.empty_like(vq)
+        vl = torch.empty((vw.Hq, vq.shape[0]), dtype=torch.float32, device=dev)
+        vws = torch.empty(binding.attn_fwd_varlen_workspace_bytes(len(vlens), vq.shape[0],
+                                                                  max(vlens)),
+                          dtype=torch.uint8, device=dev)
+        varlen_ms = time_alone(
+            lambda: binding.fwd_varlen(vq, vk, vv, vcq, vck, max(vlens), max(vlens),
+                                       causal=True, scale=vw.scale, workspace=vws, out=vo,
+                                       lse=vl), 30)
+        varlen_flops = acct.varlen_flops(vlens, vlens, vw.Hq, vw.d, True)
+        varlen_docs = len(vlens)
+        del vq, vk, vv, vcq, vck, vo, vl, vws
 
     agg = aggregate_ranks(
         {"pre_s": sum(pre_ms) / 1e3, "dec_s": sum(dec_ms) / 1e3, "total_ms": total_ms,
@@ -441,6 +459,17 @@ def run_ours(args, rank, world, local_rank):
             "algorithmic_bytes_per_launch": paged_bytes,
             "traffic": ncu_traffic("decode_split_kernel<128,4,paged>/" + synth.PAGED_DECODE.name,
                                    source_sha(*DECODE_SOURCES)),
+        },
+        "varlen": None if varlen_ms is None else {
+            "workload": synth.VARLEN.name,
+            "documents": varlen_docs,
+            "value": round(varlen_flops / (varlen_ms / 1e3) / 1e12, 2),
+            "unit": "TFLOP/s (4*d per visible pair)",
+            "ms": round(varlen_ms, 4),
+            "frac_of_sustained_peak": round(varlen_flops / (varlen_ms / 1e3) / 1e12 / peak_tf, 4),
+            "launches": "planning kernel + prefill kernel",
+            "traffic": ncu_traffic("prefill_fwd_kernel<128,varlen>/" + synth.VARLEN.name,
+                                   source_sha(*PREFILL_SOURCES)),
         },
         "gpu_launches": K * 3,
         "clocks": clk,

@@ -102,6 +102,53 @@ int attn_fwd_window(const void *q, const void *k, const void *v, void *o, float 
                     float scale, void *stream);
 
 /*
+ * attn_fwd_varlen_workspace_bytes -- scratch needed by attn_fwd_varlen.
+ *
+ * Depends only on the sizes; returns 0 for invalid sizes.
+ */
+size_t attn_fwd_varlen_workspace_bytes(int B, int total_q, int max_seqlen_q);
+
+/*
+ * attn_fwd_varlen -- forward pass over a packed batch of variable-length
+ * sequences.
+ *
+ * The B sequences are concatenated without padding and located by
+ * cumulative offsets, and no score between two sequences is ever formed
+ * ("SDPA and FlashAttention's tiling": the packed flash_attn_varlen_func
+ * call with int32 cu_seqlens of length B+1).  Each sequence is attention as
+ * in attn_fwd on its own (causal: bottom-right aligned inside the sequence).
+ *
+ *   q, o          [total_q, Hq, d] bf16, token-major (device)
+ *   k, v          [total_k, Hkv, d] bf16, token-major (device)
+ *   lse           [Hq, total_q] fp32 (device, written)
+ *   cu_seqlens_q  [B+1] int32 (device): sequence b owns query rows
+ *                 cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1
+ *   cu_seqlens_k  [B+1] int32 (device): likewise for key/value rows
+ *   max_seqlen_q, max_seqlen_k   host-side upper bounds of the lengths
+ *   d, causal, scale             as for attn_fwd
+ *   workspace     device scratch of attn_fwd_varlen_workspace_bytes(B,
+ *                 total_q, max_seqlen_q) bytes, 16-byte aligned, caller-
+ *                 owned (contents ignored; it holds the launch's work list)
+ *
+ * Offsets must start at 0, never decrease and end at most at total_q /
+ * total_k; every length must be within its max_seqlen; a sequence with
+ * queries needs at least one key, and causal needs no more queries than
+ * keys.  Empty sequences are allowed.  The offsets live on the device and
+ * are checked there: if they break these rules nothing is computed, rows
+ * of o and lse stay as they were, and attn_device_status reports
+ * ATTN_ERR_INVALID_ARG.  Rows of o and lse outside every sequence are never
+ * written.  Host-visible errors return before any launch, as for attn_fwd.
+ * Inputs must be finite: a key tile that runs past its sequence holds the
+ * next sequence's rows, which are masked out of the softmax (their value
+ * rows are multiplied by zero).
+ */
+int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                    const int *cu_seqlens_q, const int *cu_seqlens_k, int B, int Hq,
+                    int Hkv, int total_q, int total_k, int max_seqlen_q, int max_seqlen_k,
+                    int d, int causal, float scale, void *workspace, size_t workspace_bytes,
+                    void *stream);
+
+/*
  * attn_decode_workspace_bytes -- scratch needed by attn_decode.
  *
  * Depends only on the sizes (not on the GPU), so it may be called before any
@@ -222,9 +269,9 @@ const char *attn_status_string(int status);
  * Every wait inside the kernels is bounded in time.  A kernel that gives up
  * stops its work, drains its own copies and tensor-core operations, frees
  * its tensor memory, records ATTN_ERR_DEVICE_TIMEOUT here and returns, so
- * the CUDA context stays usable.  attn_decode_paged also records
- * ATTN_ERR_INVALID_ARG here for a device-side length or page index it could
- * not use.  This call synchronises `stream`, copies
+ * the CUDA context stays usable.  attn_decode_paged and attn_fwd_varlen
+ * also record ATTN_ERR_INVALID_ARG here for device-side lengths, offsets or
+ * page indices they could not use.  This call synchronises `stream`, copies
  * the word to *status (ATTN_OK when nothing was recorded) and resets it.
  * Returns ATTN_OK, or ATTN_ERR_CUDA if the copy fails.
  */

@@ -47,6 +47,19 @@ def window_flops(B: int, Hq: int, Tq: int, Tk: int, d: int, window: int) -> floa
     return 4.0 * d * B * Hq * visible_pairs(Tq, Tk, True, window)
 
 
+def varlen_flops(lens_q, lens_k, Hq: int, d: int, causal: bool) -> float:
+    """Packed batch: 4*d per visible (row, key) pair of every sequence and
+    head (causal pairs counted exactly, bottom-right aligned)."""
+    pairs = 0
+    for nq, nk in zip(lens_q, lens_k):
+        nq, nk = int(nq), int(nk)
+        if not causal:
+            pairs += nq * nk
+        else:  # row i sees i + (nk - nq) + 1 keys
+            pairs += nq * (nk - nq) + nq * (nq + 1) // 2
+    return 4.0 * d * Hq * pairs
+
+
 def prefill_compulsory_bytes(B: int, Hq: int, Hkv: int, Tq: int, Tk: int, d: int) -> int:
     """Read Q, K, V once and write O (bf16) and LSE (fp32) once."""
     q = B * Hq * Tq * d * BF16_BYTES

@@ -1,8 +1,8 @@
 """Thin ctypes binding over libattn.so (the C ABI in include/attn.h).
 
 The functions named like the C entry points (attn_fwd, attn_decode, ...)
-take raw integers and pointers exactly as the C ABI does.  `fwd`, `decode`
-and `decode_paged` marshal torch CUDA tensors into those calls: they check dtype,
+take raw integers and pointers exactly as the C ABI does.  `fwd`,
+`fwd_varlen`, `decode` and `decode_paged` marshal torch CUDA tensors into those calls: they check dtype,
 device, layout and shapes, allocate the outputs with torch, and pass the
 current CUDA stream.  All attention arithmetic runs in the library's
 kernels; if the library is missing these functions raise instead of
@@ -52,6 +52,11 @@ def load_library():
             lib.attn_fwd.restype = i
             lib.attn_fwd_window.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp]
             lib.attn_fwd_window.restype = i
+            lib.attn_fwd_varlen_workspace_bytes.argtypes = [i, i, i]
+            lib.attn_fwd_varlen_workspace_bytes.restype = ctypes.c_size_t
+            lib.attn_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i,
+                                            i, i, f, vp, ctypes.c_size_t, vp]
+            lib.attn_fwd_varlen.restype = i
             lib.attn_decode_workspace_bytes.argtypes = [i, i, i, i, i]
             lib.attn_decode_workspace_bytes.restype = ctypes.c_size_t
             lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp,
@@ -80,6 +85,18 @@ def attn_fwd(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, causal, scale, stream) -> i
 def attn_fwd_window(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, window, scale, stream) -> int:
     return load_library().attn_fwd_window(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, window,
                                           scale, stream)
+
+
+def attn_fwd_varlen_workspace_bytes(B, total_q, max_seqlen_q) -> int:
+    return load_library().attn_fwd_varlen_workspace_bytes(B, total_q, max_seqlen_q)
+
+
+def attn_fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, B, Hq, Hkv, total_q, total_k,
+                    max_seqlen_q, max_seqlen_k, d, causal, scale, workspace, workspace_bytes,
+                    stream) -> int:
+    return load_library().attn_fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, B, Hq,
+                                          Hkv, total_q, total_k, max_seqlen_q, max_seqlen_k, d,
+                                          causal, scale, workspace, workspace_bytes, stream)
 
 
 def attn_decode_workspace_bytes(B, Hq, Hkv, Tk, d) -> int:
@@ -251,4 +268,45 @@ def decode_paged(q, k_pages, v_pages, block_table, seq_lens, max_seq_len: int | 
                            _stream_handle(stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_decode_paged")
+    return out, lse
+
+
+def fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,
+               causal: bool = False, scale: float | None = None, workspace=None, out=None,
+               lse=None, stream=None):
+    """O [total_q,Hq,d], LSE [Hq,total_q] for a packed batch: q [total_q,Hq,d],
+    k/v [total_k,Hkv,d] (bf16, token-major), cu_seqlens_q/_k int32 [B+1] on
+    the GPU, max_seqlen_q/_k host-side bounds of the lengths."""
+    import torch
+
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check_tensor(t, n, 3)
+    total_q, Hq, d = q.shape
+    total_k, Hkv, dk = k.shape
+    if dk != d or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("inconsistent q/k/v shapes")
+    for t, n in ((cu_seqlens_q, "cu_seqlens_q"), (cu_seqlens_k, "cu_seqlens_k")):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.int32 or t.device != q.device \
+                or t.dim() != 1 or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous 1-d int32 tensor on {q.device}")
+    if cu_seqlens_q.numel() != cu_seqlens_k.numel() or cu_seqlens_q.numel() < 2:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must both hold B+1 offsets")
+    B = cu_seqlens_q.numel() - 1
+    if workspace is None:
+        n = attn_fwd_varlen_workspace_bytes(B, total_q, int(max_seqlen_q))
+        if n == 0:
+            raise ValueError("invalid packed-batch sizes")
+        workspace = torch.empty(n, dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((Hq, total_q), dtype=torch.float32, device=q.device)
+    rc = attn_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                         lse.data_ptr(), cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), B,
+                         Hq, Hkv, total_q, total_k, int(max_seqlen_q), int(max_seqlen_k), d,
+                         int(bool(causal)), 0.0 if scale is None else float(scale),
+                         workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                         _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_varlen")
     return out, lse

@@ -74,12 +74,12 @@ int check_device_sm103(int *num_sms) {
 
 bool encode_tmap_3d_bf16(CUtensorMap *map, const void *base, uint64_t inner,
                          uint64_t rows, uint64_t planes, uint32_t box_inner,
-                         uint32_t box_rows, int swizzle_bytes) {
+                         uint32_t box_rows, uint32_t box_planes, int swizzle_bytes) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[3] = {inner, rows, planes};
   const cuuint64_t strides[2] = {inner * 2, inner * rows * 2};
-  const cuuint32_t box[3] = {box_inner, box_rows, 1};
+  const cuuint32_t box[3] = {box_inner, box_rows, box_planes};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUtensorMapSwizzle sw =
       swizzle_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
@@ -141,6 +141,58 @@ ATTN_API int attn_fwd_window(const void *q, const void *k, const void *v, void *
                              int window, float scale, void *stream) {
   if (window < 1) return ATTN_ERR_INVALID_ARG;
   return fwd_common(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, 1, window, scale, stream);
+}
+
+ATTN_API size_t attn_fwd_varlen_workspace_bytes(int B, int total_q, int max_seqlen_q) {
+  return attn_host::varlen_workspace_bytes_for(B, total_q, max_seqlen_q);
+}
+
+ATTN_API int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                             const int *cu_seqlens_q, const int *cu_seqlens_k, int B, int Hq,
+                             int Hkv, int total_q, int total_k, int max_seqlen_q,
+                             int max_seqlen_k, int d, int causal, float scale, void *workspace,
+                             size_t workspace_bytes, void *stream) {
+  float sc = 0.f;
+  // the shared checks, with the longest sequences standing in for Tq and Tk
+  int rc = validate(q, k, v, o, lse, B, Hq, Hkv, max_seqlen_q, max_seqlen_k, d, 0, scale, &sc);
+  if (rc != ATTN_OK) return rc;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (!cu_seqlens_q || !cu_seqlens_k || total_q < 1 || total_k < 1)
+    return ATTN_ERR_INVALID_ARG;
+  if (!aligned(cu_seqlens_q, 4) || !aligned(cu_seqlens_k, 4)) return ATTN_ERR_MISALIGNED;
+  const long long cap = attn_host::varlen_list_capacity(B, total_q, max_seqlen_q);
+  if (cap < 1 || cap * Hq > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+  if (!workspace || !aligned(workspace, 16) ||
+      workspace_bytes < attn_host::varlen_workspace_bytes_for(B, total_q, max_seqlen_q))
+    return ATTN_ERR_WORKSPACE;
+  rc = attn_host::check_device_sm103(nullptr);
+  if (rc != ATTN_OK) return rc;
+  attn_host::PrefillArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.Tq = max_seqlen_q;
+  a.Tk = max_seqlen_k;
+  a.d = d;
+  a.causal = causal;
+  a.window = 0;
+  a.scale = sc;
+  a.stream = static_cast<cudaStream_t>(stream);
+  a.wait_ns = g_wait_ns.load();
+  a.inject = g_inject.load();
+  a.varlen = true;
+  a.cu_q = cu_seqlens_q;
+  a.cu_k = cu_seqlens_k;
+  a.total_q = total_q;
+  a.total_k = total_k;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  return attn_host::prefill_launch(a);
 }
 
 ATTN_API size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Tk, int d) {

@@ -18,6 +18,14 @@ struct PrefillArgs {
   cudaStream_t stream;
   unsigned long long wait_ns;
   int inject;
+  // packed variable-length batches: q [total_q, Hq, d], k/v [total_k, Hkv, d],
+  // sequence b at cu_q[b]..cu_q[b+1] / cu_k[b]..cu_k[b+1]; B = sequences,
+  // Tq / Tk = the longest query / key sequence allowed
+  bool varlen = false;
+  const int *cu_q = nullptr, *cu_k = nullptr;
+  int total_q = 0, total_k = 0;
+  void *workspace = nullptr;
+  size_t workspace_bytes = 0;
 };
 
 struct DecodeArgs {
@@ -48,9 +56,15 @@ int validate_decode_args(const void *q, const void *k, const void *v, const void
                          const float *lse, int B, int Hq, int Hkv, int Tk, int d,
                          float scale, float *scale_out);
 int check_device_sm103(int *num_sms);
+// 3-D bf16 tensor map over a dense (inner, rows, planes) array; the box is
+// box_inner x box_rows x box_planes elements.
 bool encode_tmap_3d_bf16(CUtensorMap *map, const void *base, uint64_t inner,
                          uint64_t rows, uint64_t planes, uint32_t box_inner,
-                         uint32_t box_rows, int swizzle_bytes);
+                         uint32_t box_rows, uint32_t box_planes, int swizzle_bytes);
+
+// Packed-batch planning list capacity and its scratch bytes.
+long long varlen_list_capacity(int B, int total_q, int max_seqlen_q);
+size_t varlen_workspace_bytes_for(int B, int total_q, int max_seqlen_q);
 
 // Decode split plan: depends only on sizes (and the SM count for the chosen
 // split, bounded above by the size-only maximum).

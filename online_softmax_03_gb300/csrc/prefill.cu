@@ -24,11 +24,11 @@ int launch_d(const attn_host::PrefillArgs &a, unsigned int *status, unsigned int
   using C = attn_dev::PrefillCfg<D>;
   CUtensorMap tq, tk, tv;
   const uint64_t bhq = (uint64_t)a.B * a.Hq, bhk = (uint64_t)a.B * a.Hkv;
-  if (!attn_host::encode_tmap_3d_bf16(&tq, a.q, D, a.Tq, bhq, C::CHUNK, C::BM, C::SPAN) ||
-      !attn_host::encode_tmap_3d_bf16(&tk, a.k, D, a.Tk, bhk, C::CHUNK, C::BN, C::SPAN) ||
-      !attn_host::encode_tmap_3d_bf16(&tv, a.v, D, a.Tk, bhk, C::CHUNK, C::BN, C::SPAN))
+  if (!attn_host::encode_tmap_3d_bf16(&tq, a.q, D, a.Tq, bhq, C::CHUNK, C::BM, 1, C::SPAN) ||
+      !attn_host::encode_tmap_3d_bf16(&tk, a.k, D, a.Tk, bhk, C::CHUNK, C::BN, 1, C::SPAN) ||
+      !attn_host::encode_tmap_3d_bf16(&tv, a.v, D, a.Tk, bhk, C::CHUNK, C::BN, 1, C::SPAN))
     return ATTN_ERR_CUDA;
-  attn_dev::PrefillParams p;
+  attn_dev::PrefillParams p{};
   p.o = static_cast<__nv_bfloat16 *>(a.o);
   p.lse = a.lse;
   p.status = status;
@@ -61,7 +61,165 @@ int launch_d(const attn_host::PrefillArgs &a, unsigned int *status, unsigned int
   // Persistent: one CTA per SM (each holds all of an SM's tensor memory);
   // CTAs take work items from the slot's counter until the list is done.
   const uint64_t grid = items < (uint64_t)sms ? items : (uint64_t)sms;
-  auto kern = attn_dev::prefill_fwd_kernel<D, kWindow>;
+  auto kern = attn_dev::prefill_fwd_kernel<D, kWindow, false>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)C::SMEM_BYTES) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  kern<<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(tq, tk, tv, p);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+// Packed batches: list every (sequence, query-tile pair) heaviest first, as
+// {entries, 0, (b, pair) x entries}.  The weight of a pair is the number of
+// K/V tiles its two query tiles visit; a counting sort over weight classes
+// (pairs of more than kPlanBins - 1 tiles share the top class) orders the
+// list.  The order of equal weights varies from run to run, which changes
+// nothing in the results: every entry owns its output rows.  Offsets that
+// break the documented rules leave the list empty and record
+// ATTN_ERR_INVALID_ARG.
+constexpr int kPlanThreads = 1024;
+constexpr int kPlanBins = 8192;
+constexpr int kBinsPerThread = kPlanBins / kPlanThreads;
+
+__device__ __forceinline__ int pair_weight(int nq, int nk, int pair, int causal) {
+  const int n_kt = (nk + 127) / 128;
+  if (!causal) return n_kt;
+  const int last = min(pair * 256 + 255, nq - 1);
+  return min(n_kt, (last + nk - nq) / 128 + 1);
+}
+
+__global__ void __launch_bounds__(kPlanThreads)
+    varlen_plan_kernel(const int *__restrict__ cu_q, const int *__restrict__ cu_k, int B,
+                       int total_q, int total_k, int max_q, int max_k, int causal,
+                       int *__restrict__ list, long long capacity,
+                       unsigned int *__restrict__ status) {
+  __shared__ int hist[kPlanBins];
+  __shared__ int part[kPlanThreads];
+  __shared__ int bad;
+  const int tid = threadIdx.x;
+  if (tid == 0) bad = (cu_q[0] != 0 || cu_k[0] != 0);
+  for (int i = tid; i < kPlanBins; i += kPlanThreads) hist[i] = 0;
+  __syncthreads();
+  for (int b = tid; b < B; b += kPlanThreads) {
+    const long long q1 = cu_q[b + 1], k1 = cu_k[b + 1];
+    const long long nq = q1 - cu_q[b], nk = k1 - cu_k[b];
+    if (nq < 0 || nk < 0 || q1 > total_q || k1 > total_k || nq > max_q || nk > max_k ||
+        (nq > 0 && nk < 1) || (causal && nq > nk))
+      bad = 1;
+  }
+  __syncthreads();
+  if (bad) {
+    if (tid == 0) {
+      list[0] = 0;
+      list[1] = 0;
+      atomicMax(status, 1u);  // ATTN_ERR_INVALID_ARG
+    }
+    return;
+  }
+  // Offsets are valid from here on: 0 <= cu[b] <= cu[b+1] <= total.
+  for (int b = tid; b < B; b += kPlanThreads) {
+    const int nq = cu_q[b + 1] - cu_q[b], nk = cu_k[b + 1] - cu_k[b];
+    for (int pr = 0; (long long)pr * 256 < nq; ++pr) {
+      const int w = min(pair_weight(nq, nk, pr, causal), kPlanBins - 1);
+      atomicAdd(&hist[kPlanBins - 1 - w], 1);  // heaviest class first
+    }
+  }
+  __syncthreads();
+  // Exclusive prefix sum over the classes: per-thread runs, then a scan of
+  // the run totals.
+  int run = 0;
+#pragma unroll
+  for (int i = 0; i < kBinsPerThread; ++i) run += hist[tid * kBinsPerThread + i];
+  part[tid] = run;
+  __syncthreads();
+  for (int off = 1; off < kPlanThreads; off <<= 1) {
+    const int add = tid >= off ? part[tid - off] : 0;
+    __syncthreads();
+    part[tid] += add;
+    __syncthreads();
+  }
+  const int total = part[kPlanThreads - 1];
+  int start = part[tid] - run;
+#pragma unroll
+  for (int i = 0; i < kBinsPerThread; ++i) {
+    const int c = hist[tid * kBinsPerThread + i];
+    hist[tid * kBinsPerThread + i] = start;
+    start += c;
+  }
+  __syncthreads();
+  for (int b = tid; b < B; b += kPlanThreads) {
+    const int nq = cu_q[b + 1] - cu_q[b], nk = cu_k[b + 1] - cu_k[b];
+    for (int pr = 0; (long long)pr * 256 < nq; ++pr) {
+      const int w = min(pair_weight(nq, nk, pr, causal), kPlanBins - 1);
+      const int pos = atomicAdd(&hist[kPlanBins - 1 - w], 1);
+      if (pos < capacity) {
+        list[2 + 2 * pos] = b;
+        list[3 + 2 * pos] = pr;
+      }
+    }
+  }
+  if (tid == 0) {
+    if (total > capacity) {  // cannot happen for offsets within the documented rules
+      list[0] = 0;
+      atomicMax(status, 1u);
+    } else {
+      list[0] = total;
+    }
+    list[1] = 0;
+  }
+}
+
+template <int D>
+int launch_varlen(const attn_host::PrefillArgs &a, unsigned int *status, unsigned int *work,
+                  int sms) {
+  using C = attn_dev::PrefillCfg<D>;
+  const long long capacity = attn_host::varlen_list_capacity(a.B, a.total_q, a.Tq);
+  if (capacity < 1 || capacity * a.Hq > (long long)INT_MAX) return ATTN_ERR_INVALID_ARG;
+  // (D, heads, tokens) views of the token-major tensors: a box is 128
+  // consecutive tokens of one head.
+  CUtensorMap tq, tk, tv;
+  if (!attn_host::encode_tmap_3d_bf16(&tq, a.q, D, a.Hq, a.total_q, C::CHUNK, 1, C::BM,
+                                      C::SPAN) ||
+      !attn_host::encode_tmap_3d_bf16(&tk, a.k, D, a.Hkv, a.total_k, C::CHUNK, 1, C::BN,
+                                      C::SPAN) ||
+      !attn_host::encode_tmap_3d_bf16(&tv, a.v, D, a.Hkv, a.total_k, C::CHUNK, 1, C::BN,
+                                      C::SPAN))
+    return ATTN_ERR_CUDA;
+  attn_dev::PrefillParams p{};
+  p.o = static_cast<__nv_bfloat16 *>(a.o);
+  p.lse = a.lse;
+  p.status = status;
+  p.Hq = a.Hq;
+  p.Hkv = a.Hkv;
+  p.group = a.Hq / a.Hkv;
+  p.Tq = a.Tq;
+  p.Tk = a.Tk;
+  p.n_bh = a.Hq;
+  {
+    // Heads per scheduling group: as many as keep the group's K and V
+    // (about 48 MiB over all sequences) resident in L2.
+    const uint64_t kv_bytes = 2ull * (uint64_t)a.total_k * D * 2;
+    uint64_t g = ((48ull << 20) / kv_bytes) * (uint64_t)(a.Hq / a.Hkv);
+    if (g < 1) g = 1;
+    if (g > (uint64_t)a.Hq) g = a.Hq;
+    p.head_group = (int)g;
+  }
+  p.causal = a.causal;
+  p.window = 0;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.wait_ns = a.wait_ns;
+  p.inject = a.inject;
+  p.cu_q = a.cu_q;
+  p.cu_k = a.cu_k;
+  p.vl_list = static_cast<const int *>(a.workspace);
+  p.total_q = a.total_q;
+  p.work = work + 2 * (g_launch_seq.fetch_add(1) % kWorkSlots);
+  varlen_plan_kernel<<<1, kPlanThreads, 0, a.stream>>>(
+      a.cu_q, a.cu_k, a.B, a.total_q, a.total_k, a.Tq, a.Tk, a.causal,
+      static_cast<int *>(a.workspace), capacity, status);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+  const long long items = capacity * a.Hq;  // upper bound; the list holds the count
+  const long long grid = items < sms ? items : sms;
+  auto kern = attn_dev::prefill_fwd_kernel<D, false, true>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)C::SMEM_BYTES) != cudaSuccess)
     return ATTN_ERR_CUDA;
@@ -72,6 +230,19 @@ int launch_d(const attn_host::PrefillArgs &a, unsigned int *status, unsigned int
 
 namespace attn_host {
 
+long long varlen_list_capacity(int B, int total_q, int max_seqlen_q) {
+  if (B < 1 || total_q < 1 || max_seqlen_q < 1) return 0;
+  const long long by_max = (long long)B * ((max_seqlen_q + 255) / 256);
+  const long long by_total = (long long)(total_q + 255) / 256 + B;
+  return by_max < by_total ? by_max : by_total;
+}
+
+size_t varlen_workspace_bytes_for(int B, int total_q, int max_seqlen_q) {
+  const long long cap = varlen_list_capacity(B, total_q, max_seqlen_q);
+  if (cap < 1) return 0;
+  return ((size_t)(2 + 2 * cap) * sizeof(int) + 15) / 16 * 16;
+}
+
 int prefill_launch(const PrefillArgs &a) {
   int sms = 0;
   const int rc = check_device_sm103(&sms);
@@ -81,6 +252,14 @@ int prefill_launch(const PrefillArgs &a) {
           cudaSuccess ||
       cudaGetSymbolAddress(reinterpret_cast<void **>(&work), g_prefill_work) != cudaSuccess)
     return ATTN_ERR_CUDA;
+  if (a.varlen) {
+    switch (a.d) {
+      case 32: return launch_varlen<32>(a, status, work, sms);
+      case 64: return launch_varlen<64>(a, status, work, sms);
+      case 128: return launch_varlen<128>(a, status, work, sms);
+      default: return ATTN_ERR_UNSUPPORTED;
+    }
+  }
   const bool win = a.window > 0;
   switch (a.d) {
     case 32: return win ? launch_d<32, true>(a, status, work, sms)

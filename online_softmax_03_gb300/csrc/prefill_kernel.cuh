@@ -60,6 +60,18 @@
 // Work items are ordered by groups of heads whose K/V fit in L2, heaviest
 // query tiles first within a group.
 //
+// Packed variable-length batches (kVarlen; "SDPA and FlashAttention's
+// tiling", flash_attn_varlen_func): sequences are concatenated without
+// padding in token-major tensors q [total_q, Hq, D], k/v [total_k, Hkv, D]
+// and located by offsets cu_q / cu_k.  A small planning kernel lists every
+// (sequence, query-tile pair) heaviest first; an item is one list entry for
+// one head, and the producer publishes its geometry (offsets and lengths)
+// with the item.  The tensor maps view each tensor as (D, heads, tokens), so
+// a box is 128 consecutive tokens of one head, laid out in shared memory
+// exactly like a box of the [B, H, T, D] layout.  A tile that runs past its
+// sequence reads the next sequence's rows (or zero fill at the end): their
+// keys are masked like a ragged K tail and their query rows are not stored.
+//
 // Every barrier wait is bounded in time; on expiry the kernel records
 // ATTN_ERR_DEVICE_TIMEOUT, stops issuing work, drains its own copies and
 // MMAs, frees tensor memory and returns.
@@ -91,6 +103,10 @@ struct PrefillParams {
   float scale_log2;       // scale * log2(e)
   unsigned long long wait_ns;
   int inject;             // test hook: 1 = withhold the first V tile
+  // packed variable-length batches only
+  const int *cu_q, *cu_k;  // [B+1] token offsets of each sequence
+  const int *vl_list;      // {entries, 0, (b, pair) x entries}, heaviest first
+  int total_q;             // tokens in q (row stride of lse [Hq, total_q])
 };
 
 template <int D>
@@ -113,7 +129,8 @@ struct PrefillCfg {
   // item_full[2], item_empty[2], then per stage k_full, v_full, k_empty, v_empty
   static constexpr int NBAR = 15 + 4 * STAGES;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr uint32_t SMEM_USED = OFF_MISC + 32 + 1024;  // + align slack
+  // tmem slot, abort flag, then the two-entry item ring of kRingInts ints each
+  static constexpr uint32_t SMEM_USED = OFF_MISC + 128 + 1024;  // + align slack
   // At least ~116 KB so that only one CTA (which holds all 512 TMEM
   // columns) is resident per SM.
   static constexpr uint32_t SMEM_BYTES = SMEM_USED > 118784u ? SMEM_USED : 118784u;
@@ -143,6 +160,81 @@ struct PrefillItem {
   __device__ __forceinline__ int jend() const { return max(hi0, hi1); }
 };
 
+// Ints per item-ring entry: the item index, then (packed batches) the
+// item's head, pair, query offset and length, key offset and length.
+constexpr int kRingInts = 8;
+
+// Tile ranges of the two query tiles of the pair starting at row q0 of a
+// sequence with Tq queries and Tk keys.
+template <bool kWindow>
+__device__ __forceinline__ void prefill_ranges(PrefillItem &it, int Tq, int Tk, int causal,
+                                               int window) {
+  const int delta = Tk - Tq;
+  const int n_kv_all = (Tk + 127) / 128;
+  int lo[2], hi[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int row0 = it.q0 + t * 128;
+    if (row0 >= Tq) {
+      lo[t] = hi[t] = 0;
+    } else {
+      const int last_row = min(row0 + 127, Tq - 1);
+      hi[t] = causal ? min(n_kv_all, (last_row + delta) / 128 + 1) : n_kv_all;
+      // the window's left edge for the tile's first row: keys below it are
+      // outside every row's window
+      lo[t] = kWindow ? max(0, row0 + delta - window + 1) / 128 : 0;
+    }
+  }
+  it.lo0 = lo[0];
+  it.hi0 = hi[0];
+  it.lo1 = lo[1];
+  it.hi1 = hi[1];
+}
+
+// Packed batches: entry e of the planned list for head h.
+struct VarlenItem {
+  int h, pair, q_base, Tq, k_base, Tk;
+};
+
+__device__ __forceinline__ VarlenItem varlen_item(const PrefillParams &p, int idx,
+                                                  int entries) {
+  // Heads in groups of head_group (K/V of a group stay in L2); inside a
+  // group the list's order (heaviest first), each entry for every head of
+  // the group in turn.
+  const int per_full = p.head_group * entries;
+  const int n_full = p.Hq / p.head_group;
+  int g0, gsize, r;
+  if (idx < n_full * per_full) {
+    g0 = (idx / per_full) * p.head_group;
+    gsize = p.head_group;
+    r = idx % per_full;
+  } else {
+    g0 = n_full * p.head_group;
+    gsize = p.Hq - g0;
+    r = idx - n_full * per_full;
+  }
+  const int e = r / gsize;
+  VarlenItem v;
+  v.h = g0 + r % gsize;
+  const int b = p.vl_list[2 + 2 * e];
+  v.pair = p.vl_list[3 + 2 * e];
+  v.q_base = p.cu_q[b];
+  v.Tq = p.cu_q[b + 1] - v.q_base;
+  v.k_base = p.cu_k[b];
+  v.Tk = p.cu_k[b + 1] - v.k_base;
+  return v;
+}
+
+__device__ __forceinline__ PrefillItem varlen_prefill_item(const PrefillParams &p,
+                                                           const VarlenItem &v) {
+  PrefillItem it;
+  it.bh = v.h;
+  it.bh_kv = v.h / p.group;
+  it.q0 = v.pair * 256;
+  prefill_ranges<false>(it, v.Tq, v.Tk, p.causal, 0);
+  return it;
+}
+
 template <bool kWindow>
 __device__ __forceinline__ PrefillItem prefill_item(const PrefillParams &p, int idx) {
   // Heads are taken in groups of head_group; inside a group the heaviest
@@ -167,30 +259,11 @@ __device__ __forceinline__ PrefillItem prefill_item(const PrefillParams &p, int 
   const int h = it.bh - b * p.Hq;
   it.bh_kv = b * p.Hkv + h / p.group;
   it.q0 = qt * 256;
-  const int delta = p.Tk - p.Tq;
-  const int n_kv_all = (p.Tk + 127) / 128;
-  int lo[2], hi[2];
-#pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    const int row0 = it.q0 + t * 128;
-    if (row0 >= p.Tq) {
-      lo[t] = hi[t] = 0;
-    } else {
-      const int last_row = min(row0 + 127, p.Tq - 1);
-      hi[t] = p.causal ? min(n_kv_all, (last_row + delta) / 128 + 1) : n_kv_all;
-      // the window's left edge for the tile's first row: keys below it are
-      // outside every row's window
-      lo[t] = kWindow ? max(0, row0 + delta - p.window + 1) / 128 : 0;
-    }
-  }
-  it.lo0 = lo[0];
-  it.hi0 = hi[0];
-  it.lo1 = lo[1];
-  it.hi1 = hi[1];
+  prefill_ranges<kWindow>(it, p.Tq, p.Tk, p.causal, p.window);
   return it;
 }
 
-template <int D, bool kWindow>
+template <int D, bool kWindow, bool kVarlen>
 __global__ void __launch_bounds__(320, 1)
     prefill_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
@@ -211,7 +284,8 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t *k_empty = v_full + ST, *v_empty = k_empty + ST;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
-  volatile int *item_ring = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 8);  // [2]
+  volatile int *item_ring =
+      reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 16);  // [2][kRingInts]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -257,10 +331,20 @@ __global__ void __launch_bounds__(320, 1)
   };
   // Consumers read the next work item index from the producer's ring
   // (-1 ends the walk).  Returns false if the wait expired.
-  auto take_item = [&](int &fetch, int &idx) -> bool {
+  // Packed batches: the geometry published with the item.
+  auto take_item = [&](int &fetch, int &idx, VarlenItem &vi) -> bool {
     const int k = fetch & 1;
     if (!mbar_wait(&item_full[k], (fetch >> 1) & 1, wait_ns)) return false;
-    idx = item_ring[k];
+    const volatile int *e = item_ring + k * kRingInts;
+    idx = e[0];
+    if constexpr (kVarlen) {
+      vi.h = e[1];
+      vi.pair = e[2];
+      vi.q_base = e[3];
+      vi.Tq = e[4];
+      vi.k_base = e[5];
+      vi.Tk = e[6];
+    }
     ++fetch;
     return true;
   };
@@ -274,6 +358,8 @@ __global__ void __launch_bounds__(320, 1)
       int q_cnt[C::NQ] = {0, 0};
       int kv = 0;  // K/V tiles issued so far (all items)
       bool first = true;
+      int n_items = p.n_items;
+      if constexpr (kVarlen) n_items = p.vl_list[0] * p.Hq;  // written by the planner
       for (int fetch = 0; ok; ++fetch) {
         // Take the next work item from the launch-wide counter and publish
         // it to the other roles through a two-entry ring.
@@ -283,11 +369,24 @@ __global__ void __launch_bounds__(320, 1)
           break;
         }
         int idx = (int)atomicAdd(&p.work[0], 1u);
-        if (idx >= p.n_items) idx = -1;
-        item_ring[k] = idx;
+        if (idx >= n_items) idx = -1;
+        volatile int *ring = item_ring + k * kRingInts;
+        ring[0] = idx;
+        VarlenItem vi{};
+        if constexpr (kVarlen) {
+          if (idx >= 0) {
+            vi = varlen_item(p, idx, n_items / p.Hq);
+            ring[1] = vi.h;
+            ring[2] = vi.pair;
+            ring[3] = vi.q_base;
+            ring[4] = vi.Tq;
+            ring[5] = vi.k_base;
+            ring[6] = vi.Tk;
+          }
+        }
         mbar_arrive(&item_full[k]);
         if (idx < 0) break;
-        const PrefillItem it = prefill_item<kWindow>(p, idx);
+        const PrefillItem it = kVarlen ? varlen_prefill_item(p, vi) : prefill_item<kWindow>(p, idx);
         for (int t = 0; t < C::NQ && ok; ++t) {
           if (!it.has(t)) continue;
           // Q_t is free once the previous item's last S_t has completed.
@@ -296,9 +395,14 @@ __global__ void __launch_bounds__(320, 1)
             break;
           }
           mbar_arrive_expect_tx(&q_full[t], C::Q_BYTES);
-          for (int c = 0; c < C::NCHUNK; ++c)
-            tma_load_3d(smem + C::OFF_Q + t * C::Q_BYTES + c * (C::BM * C::SPAN), &tm_q,
-                        &q_full[t], c * C::CHUNK, it.q0 + t * C::BM, it.bh);
+          for (int c = 0; c < C::NCHUNK; ++c) {
+            uint8_t *dst = smem + C::OFF_Q + t * C::Q_BYTES + c * (C::BM * C::SPAN);
+            if constexpr (kVarlen)
+              tma_load_3d(dst, &tm_q, &q_full[t], c * C::CHUNK, it.bh,
+                          vi.q_base + it.q0 + t * C::BM);
+            else
+              tma_load_3d(dst, &tm_q, &q_full[t], c * C::CHUNK, it.q0 + t * C::BM, it.bh);
+          }
           ++q_cnt[t];
         }
         const int jb = kWindow ? it.jbeg() : 0, je = it.jend();
@@ -306,17 +410,21 @@ __global__ void __launch_bounds__(320, 1)
           const int s = kv % ST, u = kv / ST;
           if (*abort_flag) { ok = false; break; }
           if (kv >= ST && !mbar_wait(&k_empty[s], (u - 1) & 1, wait_ns)) { ok = false; break; }
+          // K/V row j*BN of the item's K/V head: (column, row, plane) in the
+          // [B*Hkv, Tk, D] view, (column, head, token) in the packed view
+          const int ky = kVarlen ? it.bh_kv : j * C::BN;
+          const int kz = kVarlen ? vi.k_base + j * C::BN : it.bh_kv;
           mbar_arrive_expect_tx(&k_full[s], C::KV_BYTES);
           for (int c = 0; c < C::NCHUNK; ++c)
             tma_load_3d(smem + C::OFF_K + s * C::KV_BYTES + c * (C::BN * C::SPAN),
-                        &tm_k, &k_full[s], c * C::CHUNK, j * C::BN, it.bh_kv);
+                        &tm_k, &k_full[s], c * C::CHUNK, ky, kz);
           last_k[s] = kv;
           if (kv >= ST && !mbar_wait(&v_empty[s], (u - 1) & 1, wait_ns)) { ok = false; break; }
           if (!(p.inject == 1 && first && j == jb)) {
             mbar_arrive_expect_tx(&v_full[s], C::KV_BYTES);
             for (int c = 0; c < C::NCHUNK; ++c)
               tma_load_3d(smem + C::OFF_V + s * C::KV_BYTES + c * (C::BN * C::SPAN),
-                          &tm_v, &v_full[s], c * C::CHUNK, j * C::BN, it.bh_kv);
+                          &tm_v, &v_full[s], c * C::CHUNK, ky, kz);
             last_v[s] = kv;
           }
         }
@@ -372,10 +480,11 @@ __global__ void __launch_bounds__(320, 1)
       int kv = 0;                  // K/V tiles consumed (all items)
       for (int fetch = 0; ok;) {
         int idx = -1;
-        if (!take_item(fetch, idx)) { ok = false; break; }
+        VarlenItem vi;
+        if (!take_item(fetch, idx, vi)) { ok = false; break; }
         mbar_arrive(&item_empty[(fetch - 1) & 1]);
         if (idx < 0) break;
-        const PrefillItem it = prefill_item<kWindow>(p, idx);
+        const PrefillItem it = kVarlen ? varlen_prefill_item(p, vi) : prefill_item<kWindow>(p, idx);
         const int jb = kWindow ? it.jbeg() : 0, je = it.jend();
         // S_t of K/V tile jj in stage sj, the first S of tile t's range.
         auto start_tile = [&](const int t, int &q_cnt, const int sj, const int jj) -> bool {
@@ -458,27 +567,30 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t t_s = tmem + lane_base + C::tm_s(t);
     const uint32_t t_o = tmem + lane_base + C::tm_o(t);
     const float sl2 = p.scale_log2;
-    const int delta = p.Tk - p.Tq;
     int s_cnt = 0;  // S_t tiles consumed (all items)
     int o_cnt = 0;  // O_t tiles finished (all items)
     bool ok = true;
 
     for (int fetch = 0; ok;) {
       int idx = -1;
-      ok = __all_sync(0xffffffffu, take_item(fetch, idx));
+      VarlenItem vi;
+      ok = __all_sync(0xffffffffu, take_item(fetch, idx, vi));
       if (!ok) break;
       __syncwarp();
       if (lane == 0) mbar_arrive(&item_empty[(fetch - 1) & 1]);
       if (idx < 0) break;
-      const PrefillItem it = prefill_item<kWindow>(p, idx);
+      const PrefillItem it = kVarlen ? varlen_prefill_item(p, vi) : prefill_item<kWindow>(p, idx);
       if (!it.has(t)) continue;
+      const int Tq = kVarlen ? vi.Tq : p.Tq;
+      const int Tk = kVarlen ? vi.Tk : p.Tk;
+      const int delta = Tk - Tq;
       const int jlo = kWindow ? it.lo(t) : 0, jhi = it.hi(t);
       const int row0 = it.q0 + t * C::BM;
       const int row_g = row0 + r;
       const int lim = p.causal ? row_g + delta : 0x7fffffff;                 // last visible key
       const int lim_lo = kWindow ? row_g + delta - p.window + 1 : -1;   // first visible key
       // the largest first-visible key of the tile's rows
-      const int tile_lo = kWindow ? min(row0 + C::BM - 1, p.Tq - 1) + delta - p.window + 1 : -1;
+      const int tile_lo = kWindow ? min(row0 + C::BM - 1, Tq - 1) + delta - p.window + 1 : -1;
       float m_used = -INFINITY;  // reference max, log2 units
       float l_sum = 0.f;
 
@@ -491,14 +603,14 @@ __global__ void __launch_bounds__(320, 1)
         tmem_ld128_wait(t_s, s);
 
         const int kbase = j * C::BN;
-        const bool need_mask = (kbase + C::BN > p.Tk) ||
+        const bool need_mask = (kbase + C::BN > Tk) ||
                                (p.causal && kbase + C::BN - 1 > row0 + delta) ||
                                (kWindow && kbase < tile_lo);
         if (need_mask) {
 #pragma unroll
           for (int c = 0; c < C::BN; ++c) {
             const int key = kbase + c;
-            if (key > lim || (kWindow && key < lim_lo) || key >= p.Tk) s[c] = -INFINITY;
+            if (key > lim || (kWindow && key < lim_lo) || key >= Tk) s[c] = -INFINITY;
           }
         }
         float mx[8];
@@ -594,8 +706,13 @@ __global__ void __launch_bounds__(320, 1)
       // O_t has been read: the next item's first PV_t may overwrite it (it
       // waits for this group's next P_t, published after this fence).
       tc_fence_before();
-      if (row_g < p.Tq) {
-        uint4 *orow = reinterpret_cast<uint4 *>(p.o + ((size_t)it.bh * p.Tq + row_g) * D);
+      if (row_g < Tq) {
+        // [B, Hq, Tq, D] rows, or token-major [total_q, Hq, D] rows when packed
+        const size_t orow_idx = kVarlen ? (size_t)(vi.q_base + row_g) * p.Hq + it.bh
+                                        : (size_t)it.bh * Tq + row_g;
+        const size_t lse_idx = kVarlen ? (size_t)it.bh * p.total_q + vi.q_base + row_g
+                                       : (size_t)it.bh * Tq + row_g;
+        uint4 *orow = reinterpret_cast<uint4 *>(p.o + orow_idx * D);
 #pragma unroll
         for (int i = 0; i < D / 8; ++i) orow[i] = packed[i];
         float lse;
@@ -603,7 +720,7 @@ __global__ void __launch_bounds__(320, 1)
           lse = (m_used + log2f(l_sum)) * kLn2;
         else
           lse = (m_used == -INFINITY) ? 0.f : m_used * kLn2;
-        p.lse[(size_t)it.bh * p.Tq + row_g] = lse;
+        p.lse[lse_idx] = lse;
       }
     }
     if (!ok) fail();

@@ -84,6 +84,12 @@ PAGED_DECODE = Workload("paged_decode_b64_hq32_hkv8_tk8192_d128_p16", 64, 32, 8,
                         128, False, "normal", 5, decode=True)
 PAGED_PAGE_SIZE = 16
 
+# Packed variable-length prefill measured beside the specified workloads:
+# documents of mixed length packed into one batch of VARLEN_TOKENS tokens.
+VARLEN_TOKENS = 65536
+VARLEN = Workload("varlen_pack65536_h32_d128_causal", 1, 32, 32, 8192, 8192, 128, True,
+                  "normal", 7)
+
 ALL = (TINY, TINY_NONCAUSAL, PREFILL_1K, PREFILL_4K, LONG_8K_CAUSAL, LONG_8K_FULL,
        LONG_8000_CAUSAL, LONG_8000_FULL, DECODE_GQA)
 
@@ -167,3 +173,42 @@ def make_paged_inputs(B: int, Hq: int, Hkv: int, d: int, page_size: int, seq_len
                      device=device)
     return (q.to(torch.bfloat16), kp.to(torch.bfloat16), vp.to(torch.bfloat16),
             table.to(device), torch.tensor(lens, dtype=torch.int32, device=device))
+
+
+def packed_lengths(total: int, seed: int, mean: float = 2048.0, lo: int = 64,
+                   hi: int = 8192):
+    """Document lengths for a packed batch: drawn from an exponential
+    distribution of the given mean (CPU generator, seeded), clipped to
+    [lo, hi], until they fill `total` tokens (the last one is cut to fit)."""
+    g = torch.Generator().manual_seed(seed)
+    lens, used = [], 0
+    while used < total:
+        n = int(torch.empty(1).exponential_(1.0 / mean, generator=g).item())
+        n = max(lo, min(hi, n), 1)
+        n = min(n, total - used)
+        lens.append(n)
+        used += n
+    return lens
+
+
+def make_varlen_inputs(lens_q, lens_k, Hq: int, Hkv: int, d: int, seed: int, device="cpu",
+                       dist: str = "normal", pad_q: int = 0, pad_k: int = 0):
+    """Draw a packed batch: q [total_q, Hq, d], k and v [total_k, Hkv, d]
+    (bf16, token-major) and int32 offsets cu_q, cu_k of length B+1.  q, then
+    k, then v are drawn in fp32 on `device` from a generator seeded with
+    `seed`, then rounded to bf16.  pad_q / pad_k add rows after the last
+    sequence that belong to no sequence."""
+    device = torch.device(device)
+    cu_q = [0]
+    for n in lens_q:
+        cu_q.append(cu_q[-1] + int(n))
+    cu_k = [0]
+    for n in lens_k:
+        cu_k.append(cu_k[-1] + int(n))
+    g = torch.Generator(device=device).manual_seed(seed)
+    q = _draw(g, (cu_q[-1] + pad_q, Hq, d), dist, device)
+    k = _draw(g, (cu_k[-1] + pad_k, Hkv, d), dist, device)
+    v = _draw(g, (cu_k[-1] + pad_k, Hkv, d), dist, device)
+    return (q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16),
+            torch.tensor(cu_q, dtype=torch.int32, device=device),
+            torch.tensor(cu_k, dtype=torch.int32, device=device))

@@ -26,7 +26,8 @@ def _declared_functions():
 
 def test_header_declares_the_entry_points():
     names = _declared_functions()
-    for n in ("attn_fwd", "attn_fwd_window", "attn_decode", "attn_decode_paged",
+    for n in ("attn_fwd", "attn_fwd_window", "attn_fwd_varlen", "attn_decode",
+              "attn_decode_paged", "attn_fwd_varlen_workspace_bytes",
               "attn_decode_noalloc", "attn_decode_workspace_bytes",
               "attn_status_string", "attn_device_status", "attn_debug_set"):
         assert n in names
@@ -167,6 +168,49 @@ def _decode_paged(**kw):
 ])
 def test_decode_paged_rejects_bad_arguments_on_the_host(lib, kw, code):
     assert _decode_paged(**kw) == code
+
+
+def test_varlen_workspace_bytes(lib):
+    # list capacity min(B * ceil(max_q / 256), ceil(total_q / 256) + B) entries of two ints
+    assert binding.attn_fwd_varlen_workspace_bytes(4, 1000, 600) == (2 + 2 * 8) * 4 + 8
+    assert binding.attn_fwd_varlen_workspace_bytes(4, 5000, 300) == (2 + 2 * 8) * 4 + 8
+    assert binding.attn_fwd_varlen_workspace_bytes(64, 4096, 4096) == (2 + 2 * 80) * 4 + 8
+    assert binding.attn_fwd_varlen_workspace_bytes(0, 10, 10) == 0
+    assert binding.attn_fwd_varlen_workspace_bytes(1, 0, 10) == 0
+
+
+CQ, CK = 0x90000, 0xA0000  # fake offset arrays
+
+
+def _fwd_varlen(**kw):
+    a = dict(q=Q, k=K, v=V, o=O, lse=L, cq=CQ, ck=CK, B=3, Hq=8, Hkv=2, total_q=300,
+             total_k=400, max_q=200, max_k=200, d=64, causal=1, scale=0.0, ws=W,
+             ws_bytes=1 << 16)
+    a.update(kw)
+    return binding.attn_fwd_varlen(a["q"], a["k"], a["v"], a["o"], a["lse"], a["cq"], a["ck"],
+                                   a["B"], a["Hq"], a["Hkv"], a["total_q"], a["total_k"],
+                                   a["max_q"], a["max_k"], a["d"], a["causal"], a["scale"],
+                                   a["ws"], a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), binding.ATTN_ERR_INVALID_ARG),
+    (dict(cq=None), binding.ATTN_ERR_INVALID_ARG),
+    (dict(ck=None), binding.ATTN_ERR_INVALID_ARG),
+    (dict(B=0), binding.ATTN_ERR_INVALID_ARG),
+    (dict(total_q=0), binding.ATTN_ERR_INVALID_ARG),
+    (dict(total_k=0), binding.ATTN_ERR_INVALID_ARG),
+    (dict(max_q=0), binding.ATTN_ERR_INVALID_ARG),
+    (dict(causal=3), binding.ATTN_ERR_INVALID_ARG),
+    (dict(Hq=8, Hkv=3), binding.ATTN_ERR_INVALID_ARG),
+    (dict(d=80), binding.ATTN_ERR_UNSUPPORTED),
+    (dict(o=O + 8), binding.ATTN_ERR_MISALIGNED),
+    (dict(cq=CQ + 2), binding.ATTN_ERR_MISALIGNED),
+    (dict(ws=None), binding.ATTN_ERR_WORKSPACE),
+    (dict(ws_bytes=16), binding.ATTN_ERR_WORKSPACE),
+])
+def test_fwd_varlen_rejects_bad_arguments_on_the_host(lib, kw, code):
+    assert _fwd_varlen(**kw) == code
 
 
 def test_library_has_no_oracle_dependency():

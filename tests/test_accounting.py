@@ -61,3 +61,12 @@ def test_paged_decode_bytes():
     # ragged: K/V bytes follow the lengths, pages round up
     assert acc.paged_decode_bytes(2, 4, 2, [1, 17], 64, 16) == (
         2 * 2 * 18 * 64 * 2 + (1 + 2) * 4 + 2 * 4 + 2 * 2 * 4 * 64 * 2 + 2 * 4 * 4)
+
+
+def test_varlen_flops_counts_each_document_alone():
+    lq, lk = [5, 0, 17, 1], [9, 4, 17, 3]
+    for causal in (False, True):
+        want = sum(acc.visible_pairs(a, b, causal) for a, b in zip(lq, lk) if a) * 4.0 * 8 * 6
+        assert acc.varlen_flops(lq, lk, 6, 8, causal) == want
+    # one document of T tokens is the dense causal count, T(T+1)/2 pairs
+    assert acc.varlen_flops([4096], [4096], 32, 128, True) == 4.0 * 128 * 32 * 4096 * 4097 // 2
