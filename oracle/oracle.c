@@ -610,3 +610,234 @@ int oracle_attn_varlen(const void *q, const void *k, const void *v, int in_type,
   }
   return status;
 }
+
+/*
+ * Backward pass, the plain definition ("4.2 FlashAttention I", section
+ * "The backward pass: recomputation instead of storage": the chain rule
+ * through O = P V and the row softmax; "Efficient attention & KV cache",
+ * section 2.2, backward with recomputation):
+ *
+ *   P     = softmax_row(S),  S = scale Q K^T (masked entries -inf, P = 0)
+ *   O     = P V,   D_i = sum_c dO_ic O_ic
+ *   dV    = P^T dO
+ *   dP    = dO V^T
+ *   dS    = P o (dP - D)        (o: elementwise; D broadcast along rows)
+ *   dQ    = scale dS K,   dK = scale dS^T Q
+ *
+ * For every (b, h) the full Tq x Tk matrices S, P, dP, dS are materialised.
+ * Under grouped-query attention K/V head g serves query heads
+ * g*group .. g*group+group-1, so dK_g and dV_g sum their contributions.
+ * q, k, v and dO are fp64 or bf16 bits (in_type); dq [B,Hq,Tq,d],
+ * dk and dv [B,Hkv,Tk,d], and optionally o [B,Hq,Tq,d] and lse [B,Hq,Tq]
+ * (natural log) are written in fp64.
+ */
+int oracle_attn_bwd_dense(const void *q, const void *k, const void *v, const void *dout,
+                          int in_type, int B, int Hq, int Hkv, int Tq, int Tk, int d,
+                          int causal, double scale, double *dq, double *dk, double *dv,
+                          double *o_out, double *lse_out) {
+  int rc = check_shape(B, Hq, Hkv, Tq, Tk, d, causal, 0);
+  if (rc) return rc;
+  const int group = Hq / Hkv;
+  int status = ORACLE_OK;
+
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+  for (int b = 0; b < B; ++b) {
+    for (int g = 0; g < Hkv; ++g) {
+      const size_t kvoff = ((size_t)b * Hkv + g) * (size_t)Tk * d;
+      double *Kh = malloc(sizeof(double) * (size_t)Tk * d);
+      double *Vh = malloc(sizeof(double) * (size_t)Tk * d);
+      double *Qh = malloc(sizeof(double) * (size_t)Tq * d);
+      double *dOh = malloc(sizeof(double) * (size_t)Tq * d);
+      double *P = malloc(sizeof(double) * (size_t)Tq * Tk);
+      double *dS = malloc(sizeof(double) * (size_t)Tq * Tk);
+      double *Oh = malloc(sizeof(double) * (size_t)Tq * d);
+      double *Dv = malloc(sizeof(double) * (size_t)Tq);
+      if (!Kh || !Vh || !Qh || !dOh || !P || !dS || !Oh || !Dv) {
+#pragma omp atomic write
+        status = ORACLE_ERR_NOMEM;
+        free(Kh); free(Vh); free(Qh); free(dOh); free(P); free(dS); free(Oh); free(Dv);
+        continue;
+      }
+      load_rows(k, in_type, kvoff, 0, Tk, d, Kh);
+      load_rows(v, in_type, kvoff, 0, Tk, d, Vh);
+      double *dKg = &dk[kvoff], *dVg = &dv[kvoff];
+      for (size_t x = 0; x < (size_t)Tk * d; ++x) dKg[x] = dVg[x] = 0.0;
+      for (int h = g * group; h < (g + 1) * group; ++h) {
+        const size_t qoff = ((size_t)b * Hq + h) * (size_t)Tq * d;
+        load_rows(q, in_type, qoff, 0, Tq, d, Qh);
+        load_rows(dout, in_type, qoff, 0, Tq, d, dOh);
+        /* P = softmax(S) row by row, with the row-max shift */
+        for (int i = 0; i < Tq; ++i) {
+          double *Pi = &P[(size_t)i * Tk];
+          double m = -INFINITY;
+          for (int j = 0; j < Tk; ++j) {
+            if (!visible(i, j, Tq, Tk, causal, 0)) {
+              Pi[j] = -INFINITY;
+              continue;
+            }
+            double acc = 0.0;
+            for (int c = 0; c < d; ++c) acc += Qh[(size_t)i * d + c] * Kh[(size_t)j * d + c];
+            Pi[j] = scale * acc;
+            if (Pi[j] > m) m = Pi[j];
+          }
+          double denom = 0.0;
+          for (int j = 0; j < Tk; ++j) {
+            Pi[j] = (Pi[j] == -INFINITY) ? 0.0 : exp(Pi[j] - m);
+            denom += Pi[j];
+          }
+          for (int j = 0; j < Tk; ++j) Pi[j] /= denom;
+          if (lse_out) lse_out[((size_t)b * Hq + h) * Tq + i] = m + log(denom);
+        }
+        /* O = P V and D = rowsum(dO o O) */
+        for (int i = 0; i < Tq; ++i) {
+          double Di = 0.0;
+          for (int c = 0; c < d; ++c) {
+            double acc = 0.0;
+            for (int j = 0; j < Tk; ++j) acc += P[(size_t)i * Tk + j] * Vh[(size_t)j * d + c];
+            Oh[(size_t)i * d + c] = acc;
+            Di += dOh[(size_t)i * d + c] * acc;
+          }
+          Dv[i] = Di;
+        }
+        if (o_out) memcpy(&o_out[qoff], Oh, sizeof(double) * (size_t)Tq * d);
+        /* dP = dO V^T, then dS = P o (dP - D) */
+        for (int i = 0; i < Tq; ++i)
+          for (int j = 0; j < Tk; ++j) {
+            double dp = 0.0;
+            for (int c = 0; c < d; ++c) dp += dOh[(size_t)i * d + c] * Vh[(size_t)j * d + c];
+            dS[(size_t)i * Tk + j] = P[(size_t)i * Tk + j] * (dp - Dv[i]);
+          }
+        /* dQ = scale dS K */
+        double *dQh = &dq[qoff];
+        for (int i = 0; i < Tq; ++i)
+          for (int c = 0; c < d; ++c) {
+            double acc = 0.0;
+            for (int j = 0; j < Tk; ++j) acc += dS[(size_t)i * Tk + j] * Kh[(size_t)j * d + c];
+            dQh[(size_t)i * d + c] = scale * acc;
+          }
+        /* dK += scale dS^T Q,  dV += P^T dO */
+        for (int j = 0; j < Tk; ++j)
+          for (int c = 0; c < d; ++c) {
+            double ak = 0.0, av = 0.0;
+            for (int i = 0; i < Tq; ++i) {
+              ak += dS[(size_t)i * Tk + j] * Qh[(size_t)i * d + c];
+              av += P[(size_t)i * Tk + j] * dOh[(size_t)i * d + c];
+            }
+            dKg[(size_t)j * d + c] += scale * ak;
+            dVg[(size_t)j * d + c] += av;
+          }
+      }
+      free(Kh); free(Vh); free(Qh); free(dOh); free(P); free(dS); free(Oh); free(Dv);
+    }
+  }
+  return status;
+}
+
+/*
+ * Backward with recomputation, in the steps of "4.2 FlashAttention I",
+ * section "The backward pass: recomputation instead of storage": D from
+ * dO and the forward output O; then for each query block of bq rows and
+ * each key block of bk keys, the score tile is recomputed and turned into
+ * probabilities with the saved log-sum-exp, P = exp(S - L), never stored
+ * beyond the tile; dV and dK accumulate over query blocks, dQ over key
+ * blocks.  o [B,Hq,Tq,d] and lse [B,Hq,Tq] are fp64 (what the forward
+ * returned); q, k, v, dO follow in_type.  Masking is bottom-right causal.
+ */
+int oracle_attn_bwd_blocked(const void *q, const void *k, const void *v, const void *dout,
+                            int in_type, const double *o, const double *lse, int B, int Hq,
+                            int Hkv, int Tq, int Tk, int d, int causal, double scale,
+                            int bq, int bk, double *dq, double *dk, double *dv) {
+  int rc = check_shape(B, Hq, Hkv, Tq, Tk, d, causal, 0);
+  if (rc) return rc;
+  if (bq < 1 || bk < 1) return ORACLE_ERR_ARG;
+  const int group = Hq / Hkv;
+  int status = ORACLE_OK;
+
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+  for (int b = 0; b < B; ++b) {
+    for (int g = 0; g < Hkv; ++g) {
+      const size_t kvoff = ((size_t)b * Hkv + g) * (size_t)Tk * d;
+      double *Kh = malloc(sizeof(double) * (size_t)Tk * d);
+      double *Vh = malloc(sizeof(double) * (size_t)Tk * d);
+      double *Qh = malloc(sizeof(double) * (size_t)Tq * d);
+      double *dOh = malloc(sizeof(double) * (size_t)Tq * d);
+      double *Dv = malloc(sizeof(double) * (size_t)Tq);
+      double *Pt = malloc(sizeof(double) * (size_t)bq * bk);
+      double *dSt = malloc(sizeof(double) * (size_t)bq * bk);
+      if (!Kh || !Vh || !Qh || !dOh || !Dv || !Pt || !dSt) {
+#pragma omp atomic write
+        status = ORACLE_ERR_NOMEM;
+        free(Kh); free(Vh); free(Qh); free(dOh); free(Dv); free(Pt); free(dSt);
+        continue;
+      }
+      load_rows(k, in_type, kvoff, 0, Tk, d, Kh);
+      load_rows(v, in_type, kvoff, 0, Tk, d, Vh);
+      double *dKg = &dk[kvoff], *dVg = &dv[kvoff];
+      for (size_t x = 0; x < (size_t)Tk * d; ++x) dKg[x] = dVg[x] = 0.0;
+      for (int h = g * group; h < (g + 1) * group; ++h) {
+        const size_t qoff = ((size_t)b * Hq + h) * (size_t)Tq * d;
+        load_rows(q, in_type, qoff, 0, Tq, d, Qh);
+        load_rows(dout, in_type, qoff, 0, Tq, d, dOh);
+        const double *Oh = &o[qoff];
+        const double *Lh = &lse[((size_t)b * Hq + h) * Tq];
+        double *dQh = &dq[qoff];
+        for (int i = 0; i < Tq; ++i) {
+          double Di = 0.0;
+          for (int c = 0; c < d; ++c) Di += dOh[(size_t)i * d + c] * Oh[(size_t)i * d + c];
+          Dv[i] = Di;
+        }
+        for (size_t x = 0; x < (size_t)Tq * d; ++x) dQh[x] = 0.0;
+        for (int i0 = 0; i0 < Tq; i0 += bq) {
+          const int rows = (Tq - i0 < bq) ? Tq - i0 : bq;
+          for (int j0 = 0; j0 < Tk; j0 += bk) {
+            const int cols = (Tk - j0 < bk) ? Tk - j0 : bk;
+            /* recompute the probability tile from the saved L */
+            for (int r = 0; r < rows; ++r)
+              for (int cj = 0; cj < cols; ++cj) {
+                const int i = i0 + r, j = j0 + cj;
+                double p = 0.0;
+                if (visible(i, j, Tq, Tk, causal, 0)) {
+                  double acc = 0.0;
+                  for (int c = 0; c < d; ++c) acc += Qh[(size_t)i * d + c] * Kh[(size_t)j * d + c];
+                  p = exp(scale * acc - Lh[i]);
+                }
+                Pt[r * bk + cj] = p;
+              }
+            /* dV_j += P^T dO_i;  dP = dO_i V_j^T;  dS = P o (dP - D) */
+            for (int cj = 0; cj < cols; ++cj)
+              for (int c = 0; c < d; ++c) {
+                double acc = 0.0;
+                for (int r = 0; r < rows; ++r)
+                  acc += Pt[r * bk + cj] * dOh[(size_t)(i0 + r) * d + c];
+                dVg[(size_t)(j0 + cj) * d + c] += acc;
+              }
+            for (int r = 0; r < rows; ++r)
+              for (int cj = 0; cj < cols; ++cj) {
+                double dp = 0.0;
+                for (int c = 0; c < d; ++c)
+                  dp += dOh[(size_t)(i0 + r) * d + c] * Vh[(size_t)(j0 + cj) * d + c];
+                dSt[r * bk + cj] = Pt[r * bk + cj] * (dp - Dv[i0 + r]);
+              }
+            /* dQ_i += scale dS K_j;  dK_j += scale dS^T Q_i */
+            for (int r = 0; r < rows; ++r)
+              for (int c = 0; c < d; ++c) {
+                double acc = 0.0;
+                for (int cj = 0; cj < cols; ++cj)
+                  acc += dSt[r * bk + cj] * Kh[(size_t)(j0 + cj) * d + c];
+                dQh[(size_t)(i0 + r) * d + c] += scale * acc;
+              }
+            for (int cj = 0; cj < cols; ++cj)
+              for (int c = 0; c < d; ++c) {
+                double acc = 0.0;
+                for (int r = 0; r < rows; ++r)
+                  acc += dSt[r * bk + cj] * Qh[(size_t)(i0 + r) * d + c];
+                dKg[(size_t)(j0 + cj) * d + c] += scale * acc;
+              }
+          }
+        }
+      }
+      free(Kh); free(Vh); free(Qh); free(dOh); free(Dv); free(Pt); free(dSt);
+    }
+  }
+  return status;
+}

@@ -71,9 +71,14 @@ def _load():
                                                      ip, ip, ip, ip, ip, dp, vp, vp]
             lib.oracle_attn_varlen.argtypes = [vp, vp, vp, ip, vp, vp, ip, ip, ip, ip,
                                                ip, ip, ip, dp, vp, vp]
+            lib.oracle_attn_bwd_dense.argtypes = [vp, vp, vp, vp, ip, ip, ip, ip, ip, ip, ip,
+                                                  ip, dp, vp, vp, vp, vp, vp]
+            lib.oracle_attn_bwd_blocked.argtypes = [vp, vp, vp, vp, ip, vp, vp, ip, ip, ip,
+                                                    ip, ip, ip, ip, dp, ip, ip, vp, vp, vp]
             for f in (lib.oracle_attn_dense, lib.oracle_attn_rows,
                       lib.oracle_attn_blocked, lib.oracle_online_softmax_1d,
-                      lib.oracle_attn_paged_decode, lib.oracle_attn_varlen):
+                      lib.oracle_attn_paged_decode, lib.oracle_attn_varlen,
+                      lib.oracle_attn_bwd_dense, lib.oracle_attn_bwd_blocked):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -252,6 +257,54 @@ def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, causal=False, scale=No
                                     int(bool(causal)), scale, _ptr(o), _ptr(lse))
     _check(rc)
     return o, lse
+
+
+def attention_backward(q, k, v, dout, causal=False, scale=None):
+    """Gradients of attention from the plain definition (S, P, dP, dS
+    materialised).  q, dout [B,Hq,Tq,d]; k, v [B,Hkv,Tk,d]; float64 or bf16
+    bits, all of one type.  Returns (dq, dk, dv, o, lse) in float64."""
+    B, Hq, Hkv, Tq, Tk, d = _shapes(q, k, v)
+    q, k, v, t = _inputs(q, k, v)
+    do, td = _as_input(dout)
+    if td != t or do.shape != q.shape:
+        raise ValueError("dout must match q in shape and type")
+    scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+    dq = np.empty((B, Hq, Tq, d), np.float64)
+    dk = np.empty((B, Hkv, Tk, d), np.float64)
+    dv = np.empty((B, Hkv, Tk, d), np.float64)
+    o = np.empty((B, Hq, Tq, d), np.float64)
+    lse = np.empty((B, Hq, Tq), np.float64)
+    rc = _load().oracle_attn_bwd_dense(_ptr(q), _ptr(k), _ptr(v), _ptr(do), t, B, Hq, Hkv, Tq,
+                                       Tk, d, int(bool(causal)), scale, _ptr(dq), _ptr(dk),
+                                       _ptr(dv), _ptr(o), _ptr(lse))
+    _check(rc)
+    return dq, dk, dv, o, lse
+
+
+def attention_backward_blocked(q, k, v, dout, o, lse, block_q, block_kv, causal=False,
+                               scale=None):
+    """Backward with the probability tiles recomputed from the saved
+    log-sum-exp, block by block.  o [B,Hq,Tq,d] and lse [B,Hq,Tq] are the
+    forward's outputs (float64).  Returns (dq, dk, dv) in float64."""
+    B, Hq, Hkv, Tq, Tk, d = _shapes(q, k, v)
+    q, k, v, t = _inputs(q, k, v)
+    do, td = _as_input(dout)
+    if td != t or do.shape != q.shape:
+        raise ValueError("dout must match q in shape and type")
+    o = np.ascontiguousarray(o, dtype=np.float64)
+    lse = np.ascontiguousarray(lse, dtype=np.float64)
+    if o.shape != (B, Hq, Tq, d) or lse.shape != (B, Hq, Tq):
+        raise ValueError("o must be [B,Hq,Tq,d] and lse [B,Hq,Tq]")
+    scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+    dq = np.empty((B, Hq, Tq, d), np.float64)
+    dk = np.empty((B, Hkv, Tk, d), np.float64)
+    dv = np.empty((B, Hkv, Tk, d), np.float64)
+    rc = _load().oracle_attn_bwd_blocked(_ptr(q), _ptr(k), _ptr(v), _ptr(do), t, _ptr(o),
+                                         _ptr(lse), B, Hq, Hkv, Tq, Tk, d, int(bool(causal)),
+                                         scale, int(block_q), int(block_kv), _ptr(dq), _ptr(dk),
+                                         _ptr(dv))
+    _check(rc)
+    return dq, dk, dv
 
 
 def online_softmax_1d(x, block):

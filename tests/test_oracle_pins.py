@@ -556,3 +556,99 @@ def test_varlen_rejects_bad_offsets(cq, ck, causal):
     q, k = _rand((8, 1, 4), 150), _rand((5, 1, 4), 151)
     with pytest.raises(ValueError):
         ora.attention_varlen(q, k, k, cq, ck, causal=causal)
+
+
+# --- backward ("4.2 FlashAttention I", "The backward pass: recomputation
+# instead of storage") -----------------------------------------------------
+
+def _fd_grad(f, x, idx, eps=1e-6):
+    """Central difference of the scalar f at x[idx]."""
+    xp, xm = x.copy(), x.copy()
+    xp[idx] += eps
+    xm[idx] -= eps
+    return (f(xp) - f(xm)) / (2 * eps)
+
+
+@pytest.mark.parametrize("causal,Tq,Tk,Hq,Hkv", [
+    (True, 9, 9, 2, 2), (True, 7, 12, 4, 2), (False, 6, 10, 3, 1)])
+def test_backward_matches_finite_differences(causal, Tq, Tk, Hq, Hkv):
+    """The page's own check: the gradients of sum(dO * O) agree with central
+    differences of the forward definition, coordinate by coordinate (every
+    entry of a small problem, GQA and Tq < Tk included)."""
+    B, d = 1, 4
+    q, k, v = _rand((B, Hq, Tq, d), 160), _rand((B, Hkv, Tk, d), 161), _rand((B, Hkv, Tk, d), 162)
+    do = _rand((B, Hq, Tq, d), 163)
+    dq, dk, dv, o, lse = ora.attention_backward(q, k, v, do, causal=causal)
+    o_fwd, lse_fwd, _ = ora.attention_dense(q, k, v, causal=causal)
+    np.testing.assert_allclose(o, o_fwd, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lse, lse_fwd, rtol=0, atol=1e-14)
+    loss = lambda qq, kk, vv: float((do * ora.attention_dense(qq, kk, vv, causal=causal)[0]).sum())
+    for idx in np.ndindex(q.shape):
+        assert abs(_fd_grad(lambda x: loss(x, k, v), q, idx) - dq[idx]) < 1e-7
+    for idx in np.ndindex(k.shape):
+        assert abs(_fd_grad(lambda x: loss(q, x, v), k, idx) - dk[idx]) < 1e-7
+        assert abs(_fd_grad(lambda x: loss(q, k, x), v, idx) - dv[idx]) < 1e-7
+
+
+def test_backward_matches_torch_autograd():
+    """Special case that reduces to a library routine: torch's float64
+    autograd through softmax(scale Q K^T + mask) V, with K/V repeated per
+    query head (GQA) and the bottom-right causal mask built explicitly."""
+    torch = pytest.importorskip("torch")
+    B, Hq, Hkv, Tq, Tk, d = 2, 4, 2, 11, 15, 8
+    q, k, v = _rand((B, Hq, Tq, d), 164), _rand((B, Hkv, Tk, d), 165), _rand((B, Hkv, Tk, d), 166)
+    do = _rand((B, Hq, Tq, d), 167)
+    dq, dk, dv, _, _ = ora.attention_backward(q, k, v, do, causal=True)
+    tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+    kk = tk.repeat_interleave(Hq // Hkv, dim=1)
+    vv = tv.repeat_interleave(Hq // Hkv, dim=1)
+    mask = torch.tril(torch.ones(Tq, Tk, dtype=torch.bool), diagonal=Tk - Tq)
+    s = (tq @ kk.transpose(-1, -2)) / math.sqrt(d)
+    out = torch.softmax(s.masked_fill(~mask, float("-inf")), dim=-1) @ vv
+    out.backward(torch.tensor(do))
+    np.testing.assert_allclose(dq, tq.grad.numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dk, tk.grad.numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(dv, tv.grad.numpy(), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("bq,bk", [(16, 16), (5, 7), (1, 1), (32, 8), (64, 64)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_blocked_recomputation_equals_dense(bq, bk, causal):
+    """The page's algorithm (P rebuilt per tile from the saved L, dK/dV
+    accumulated over query blocks) equals the dense definition."""
+    B, Hq, Hkv, Tq, Tk, d = 1, 4, 2, 29, 37, 8
+    q, k, v = _rand((B, Hq, Tq, d), 168), _rand((B, Hkv, Tk, d), 169), _rand((B, Hkv, Tk, d), 170)
+    do = _rand((B, Hq, Tq, d), 171)
+    dq, dk, dv, o, lse = ora.attention_backward(q, k, v, do, causal=causal)
+    bq_, bk_, bv_ = ora.attention_backward_blocked(q, k, v, do, o, lse, bq, bk, causal=causal)
+    for a, b in ((dq, bq_), (dk, bk_), (dv, bv_)):
+        np.testing.assert_allclose(a, b, rtol=0, atol=1e-12)
+
+
+def test_backward_invariants():
+    """Rows of dS sum to zero (the softmax Jacobian annihilates constants),
+    so the dK rows of a head sum to zero; the dV rows sum to the dO rows
+    (P rows sum to one); and with one visible key per row (causal row 0)
+    dQ vanishes."""
+    B, Hq, Hkv, T, d = 2, 6, 3, 13, 8
+    q, k, v = _rand((B, Hq, T, d), 172), _rand((B, Hkv, T, d), 173), _rand((B, Hkv, T, d), 174)
+    do = _rand((B, Hq, T, d), 175)
+    for causal in (False, True):
+        dq, dk, dv, _, _ = ora.attention_backward(q, k, v, do, causal=causal)
+        np.testing.assert_allclose(dk.sum(axis=2), 0.0, atol=1e-12)
+        want = do.reshape(B, Hkv, Hq // Hkv, T, d).sum(axis=(2, 3))
+        np.testing.assert_allclose(dv.sum(axis=2), want, rtol=0, atol=1e-12)
+        if causal:
+            np.testing.assert_allclose(dq[:, :, 0], 0.0, atol=1e-15)
+
+
+def test_backward_bf16_inputs_match_the_upcast_f64_inputs():
+    rng = np.random.default_rng(176)
+    bits = lambda shape: rng.integers(0x3c00, 0x4000, size=shape, dtype=np.uint16) ^ (
+        rng.integers(0, 2, size=shape, dtype=np.uint16) << 15)
+    up = lambda x: (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    q, k, v, do = bits((1, 2, 9, 16)), bits((1, 2, 9, 16)), bits((1, 2, 9, 16)), bits((1, 2, 9, 16))
+    a = ora.attention_backward(q, k, v, do, causal=True)
+    b = ora.attention_backward(up(q), up(k), up(v), up(do), causal=True)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
