@@ -302,7 +302,7 @@ def run_ours(args, rank, world, local_rank):
         return e0.elapsed_time(e1) / n
 
     # ---- rows beyond the specified step, each timed alone after it
-    win_ms = paged_ms = varlen_ms = None
+    win_ms = paged_ms = varlen_ms = bwd_ms = None
     varlen_flops = varlen_docs = 0
     if not args.no_extra_rows:
         # sliding-window prefill
@@ -341,6 +341,18 @@ def run_ours(args, rank, world, local_rank):
         varlen_flops = acct.varlen_flops(vlens, vlens, vw.Hq, vw.d, True)
         varlen_docs = len(vlens)
         del vq, vk, vv, vcq, vck, vo, vl, vws
+        # backward of the bench prefill (dO drawn like the inputs)
+        gdo = torch.randn(qp.shape, generator=torch.Generator(device=dev).manual_seed(1002),
+                          device=dev, dtype=torch.float32).to(torch.bfloat16)
+        binding.fwd(qp, kp, vp, causal=True, out=op, lse=lp)
+        bws = torch.empty(binding.attn_bwd_workspace_bytes(PREFILL.B, PREFILL.Hq, PREFILL.Tq,
+                                                           PREFILL.d),
+                          dtype=torch.uint8, device=dev)
+        gdq, gdk, gdv = torch.empty_like(qp), torch.empty_like(kp), torch.empty_like(vp)
+        bwd_ms = time_alone(
+            lambda: binding.bwd(qp, kp, vp, op, lp, gdo, causal=True, workspace=bws, dq=gdq,
+                                dk=gdk, dv=gdv), 20)
+        del gdo, bws, gdq, gdk, gdv
 
     agg = aggregate_ranks(
         {"pre_s": sum(pre_ms) / 1e3, "dec_s": sum(dec_ms) / 1e3, "total_ms": total_ms,
@@ -470,6 +482,17 @@ def run_ours(args, rank, world, local_rank):
             "launches": "planning kernel + prefill kernel",
             "traffic": ncu_traffic("prefill_fwd_kernel<128,varlen>/" + synth.VARLEN.name,
                                    source_sha(*PREFILL_SOURCES)),
+        },
+        "backward": None if bwd_ms is None else {
+            "workload": PREFILL.name,
+            "value": round(acct.backward_flops(PREFILL.B, PREFILL.Hq, PREFILL.Tq, PREFILL.Tk,
+                                               PREFILL.d, True) / (bwd_ms / 1e3) / 1e12, 2),
+            "unit": "TFLOP/s (5 products, causal half)",
+            "ms": round(bwd_ms, 4),
+            "frac_of_sustained_peak": round(acct.backward_flops(
+                PREFILL.B, PREFILL.Hq, PREFILL.Tq, PREFILL.Tk, PREFILL.d, True)
+                / (bwd_ms / 1e3) / 1e12 / peak_tf, 4),
+            "launches": "prep + backward kernel + dQ conversion",
         },
         "gpu_launches": K * 3,
         "clocks": clk,

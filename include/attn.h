@@ -259,6 +259,48 @@ int attn_decode_paged(const void *q, const void *k_pages, const void *v_pages,
                       int max_pages_per_seq, int max_seq_len, float scale,
                       void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * attn_bwd_workspace_bytes -- scratch needed by attn_bwd.
+ *
+ * B*Hq*Tq*d fp32 for the dQ accumulator plus two fp32 values per query row
+ * (rows padded to a multiple of 128).  Depends only on the sizes; returns 0
+ * for invalid sizes.
+ */
+size_t attn_bwd_workspace_bytes(int B, int Hq, int Tq, int d);
+
+/*
+ * attn_bwd -- gradients of attn_fwd with recomputation.
+ *
+ * Given the forward's inputs, its outputs o and lse, and the upstream
+ * gradient dout = dL/dO, computes dq, dk, dv without storing anything of
+ * size Tq x Tk: every probability tile is rebuilt from the saved
+ * log-sum-exp as P = e^(S - lse) ("4.2 FlashAttention I", section "The
+ * backward pass: recomputation instead of storage"; "Efficient attention &
+ * KV cache", section 2.2):
+ *   D_i = dout_i . o_i,  dV = P^T dout,  dS = P o (dout V^T - D),
+ *   dQ = scale dS K,  dK = scale dS^T Q.
+ *
+ *   q, k, v, causal, scale, sizes   exactly as passed to attn_fwd
+ *   o, lse        attn_fwd's outputs for those inputs (device, read only)
+ *   dout          [B, Hq, Tq, d] bf16 (device, read only)
+ *   dq            [B, Hq, Tq, d] bf16 (device, written)
+ *   dk, dv        [B, Hkv, Tk, d] bf16 (device, written); under grouped-query
+ *                 attention a K/V head's gradient sums over its query heads
+ *   workspace     device scratch of attn_bwd_workspace_bytes(B, Hq, Tq, d)
+ *                 bytes, 16-byte aligned, caller-owned (contents ignored)
+ *
+ * dQ is accumulated in fp32 across key tiles by atomic tensor reductions,
+ * so its last bits may differ from run to run (the page's note on the
+ * nondeterminism of the atomic backward); dK and dV are deterministic.
+ * Errors are those of attn_fwd, plus ATTN_ERR_INVALID_ARG for a NULL
+ * gradient pointer, ATTN_ERR_MISALIGNED for one not 16-byte aligned, and
+ * ATTN_ERR_WORKSPACE.
+ */
+int attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+             const void *dout, void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int Tq,
+             int Tk, int d, int causal, float scale, void *workspace, size_t workspace_bytes,
+             void *stream);
+
 /* Human-readable name of a status code (never NULL). */
 const char *attn_status_string(int status);
 

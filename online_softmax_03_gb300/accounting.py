@@ -29,6 +29,14 @@ def attention_flops(B: int, Hq: int, Tq: int, Tk: int, d: int, causal: bool) -> 
     return f / 2.0 if causal else f
 
 
+def backward_flops(B: int, Hq: int, Tq: int, Tk: int, d: int, causal: bool) -> float:
+    """Five Tq x Tk x d products per (batch, head) -- S recomputed, dP, dV,
+    dK, dQ -- 2*Tq*Tk*d each: 10*B*Hq*Tq*Tk*d, halved for a causal mask
+    (2.5 times the forward's count)."""
+    f = 10.0 * B * Hq * Tq * Tk * d
+    return f / 2.0 if causal else f
+
+
 def visible_pairs(Tq: int, Tk: int, causal: bool, window: int = 0) -> int:
     """(row, key) pairs inside the mask of one (batch, head): all Tq*Tk, the
     bottom-right causal triangle, or the causal band of `window` keys."""

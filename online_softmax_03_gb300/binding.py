@@ -2,7 +2,7 @@
 
 The functions named like the C entry points (attn_fwd, attn_decode, ...)
 take raw integers and pointers exactly as the C ABI does.  `fwd`,
-`fwd_varlen`, `decode` and `decode_paged` marshal torch CUDA tensors into those calls: they check dtype,
+`fwd_varlen`, `bwd`, `decode` and `decode_paged` marshal torch CUDA tensors into those calls: they check dtype,
 device, layout and shapes, allocate the outputs with torch, and pass the
 current CUDA stream.  All attention arithmetic runs in the library's
 kernels; if the library is missing these functions raise instead of
@@ -65,6 +65,11 @@ def load_library():
             lib.attn_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i,
                                               i, i, f, vp, ctypes.c_size_t, vp]
             lib.attn_decode_paged.restype = i
+            lib.attn_bwd_workspace_bytes.argtypes = [i, i, i, i]
+            lib.attn_bwd_workspace_bytes.restype = ctypes.c_size_t
+            lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f,
+                                     vp, ctypes.c_size_t, vp]
+            lib.attn_bwd.restype = i
             lib.attn_status_string.argtypes = [i]
             lib.attn_status_string.restype = ctypes.c_char_p
             lib.attn_device_status.argtypes = [vp, ctypes.POINTER(i)]
@@ -116,6 +121,16 @@ def attn_decode_paged(q, k_pages, v_pages, block_table, seq_lens, o, lse, B, Hq,
                                             B, Hq, Hkv, d, page_size, num_pages,
                                             max_pages_per_seq, max_seq_len, scale, workspace,
                                             workspace_bytes, stream)
+
+
+def attn_bwd_workspace_bytes(B, Hq, Tq, d) -> int:
+    return load_library().attn_bwd_workspace_bytes(B, Hq, Tq, d)
+
+
+def attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Tq, Tk, d, causal, scale, workspace,
+             workspace_bytes, stream) -> int:
+    return load_library().attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Tq, Tk, d,
+                                   causal, scale, workspace, workspace_bytes, stream)
 
 
 def attn_status_string(status: int) -> str:
@@ -310,3 +325,36 @@ def fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqle
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_varlen")
     return out, lse
+
+
+def bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None,
+        workspace=None, dq=None, dk=None, dv=None, stream=None):
+    """dq, dk, dv of attention through attn_bwd: q/k/v/causal/scale as given
+    to `fwd`, (o, lse) what `fwd` returned, dout = dL/dO."""
+    import torch
+
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
+        _check_tensor(t, n, 4)
+    B, Hq, Tq, d = q.shape
+    Bk, Hkv, Tk, dk_ = k.shape
+    if (Bk, dk_) != (B, d) or tuple(v.shape) != tuple(k.shape) or o.shape != q.shape \
+            or dout.shape != q.shape:
+        raise ValueError("inconsistent shapes")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, Hq, Tq) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [B, Hq, Tq] tensor")
+    if workspace is None:
+        n = attn_bwd_workspace_bytes(B, Hq, Tq, d)
+        if n == 0:
+            raise ValueError("invalid backward sizes")
+        workspace = torch.empty(n, dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    rc = attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                  dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, Tq,
+                  Tk, d, int(bool(causal)), 0.0 if scale is None else float(scale),
+                  workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                  _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_bwd")
+    return dq, dk, dv

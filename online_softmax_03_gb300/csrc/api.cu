@@ -89,6 +89,20 @@ bool encode_tmap_3d_bf16(CUtensorMap *map, const void *base, uint64_t inner,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_tmap_3d_f32(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
+                        uint64_t planes, uint32_t box_inner, uint32_t box_rows,
+                        uint32_t box_planes) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {inner, rows, planes};
+  const cuuint64_t strides[2] = {inner * 4, inner * rows * 4};
+  const cuuint32_t box[3] = {box_inner, box_rows, box_planes};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(base), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Argument checks of attn_decode (Tq = 1, no mask), for entry points that
 // supply their own scratch.  No CUDA call.
 int validate_decode_args(const void *q, const void *k, const void *v, const void *o,
@@ -273,6 +287,50 @@ ATTN_API int attn_decode_paged(const void *q, const void *k_pages, const void *v
   return attn_host::decode_launch(a);
 }
 
+ATTN_API size_t attn_bwd_workspace_bytes(int B, int Hq, int Tq, int d) {
+  if (B < 1 || Hq < 1 || Tq < 1 || (d != 32 && d != 64 && d != 128)) return 0;
+  return attn_host::bwd_workspace_bytes_for(B, Hq, Tq, d);
+}
+
+ATTN_API int attn_bwd(const void *q, const void *k, const void *v, const void *o,
+                      const float *lse, const void *dout, void *dq, void *dk, void *dv, int B,
+                      int Hq, int Hkv, int Tq, int Tk, int d, int causal, float scale,
+                      void *workspace, size_t workspace_bytes, void *stream) {
+  float sc = 0.f;
+  // q/k/v/o/lse as for attn_fwd, then the gradient tensors
+  int rc = validate(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, causal, scale, &sc);
+  if (rc != ATTN_OK) return rc;
+  if (!dout || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16))
+    return ATTN_ERR_MISALIGNED;
+  if (!workspace || !aligned(workspace, 16) ||
+      workspace_bytes < attn_bwd_workspace_bytes(B, Hq, Tq, d))
+    return ATTN_ERR_WORKSPACE;
+  attn_host::BwdArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.dout = dout;
+  a.lse = lse;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.B = B;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.Tq = Tq;
+  a.Tk = Tk;
+  a.d = d;
+  a.causal = causal;
+  a.scale = sc;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  a.stream = static_cast<cudaStream_t>(stream);
+  a.wait_ns = g_wait_ns.load();
+  return attn_host::bwd_launch(a);
+}
+
 ATTN_API const char *attn_status_string(int status) {
   switch (status) {
     case ATTN_OK: return "ATTN_OK";
@@ -288,12 +346,14 @@ ATTN_API const char *attn_status_string(int status) {
 
 ATTN_API int attn_device_status(void *stream, int *status) {
   if (!status) return ATTN_ERR_INVALID_ARG;
-  unsigned int a = 0, b = 0;
+  unsigned int a = 0, b = 0, c = 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (attn_host::prefill_take_status(st, &a) != ATTN_OK ||
-      attn_host::decode_take_status(st, &b) != ATTN_OK)
+      attn_host::decode_take_status(st, &b) != ATTN_OK ||
+      attn_host::bwd_take_status(st, &c) != ATTN_OK)
     return ATTN_ERR_CUDA;
-  *status = (int)(a > b ? a : b);
+  unsigned int m = a > b ? a : b;
+  *status = (int)(m > c ? m : c);
   return ATTN_OK;
 }
 

@@ -1,0 +1,484 @@
+// backward_kernel.cuh -- attention backward on sm_103a tensor cores.
+//
+// Gradients with recomputation ("4.2 FlashAttention I: IO-Awareness & The
+// Online Softmax", section "The backward pass: recomputation instead of
+// storage"; "Efficient attention & KV cache", section 2.2): nothing of size
+// T x T is stored; each probability tile is rebuilt from the saved row
+// log-sum-exp, P = e^(S - L), and
+//
+//   dV = P^T dO,  dP = dO V^T,  dS = P o (dP - D)  with D_i = dO_i . O_i,
+//   dQ = scale dS K,  dK = scale dS^T Q.
+//
+// Loop order: keys outer, as the page describes for FlashAttention-1's
+// backward, so a CTA finishes dK and dV of its key tile in tensor memory
+// and only dQ is accumulated across CTAs.  One CTA (320 threads, one per SM)
+// owns 128 keys of one K/V head and walks every query tile of every query
+// head of that head's group (grouped-query attention); under causal masking
+// it starts at the first query tile that sees its keys.  Per step of 128
+// queries:
+//
+//   warp 8     producer: K and V of the key tile once, then per step the Q
+//              and dO tiles (TMA) and the step's L and D values (bulk copy).
+//   warp 9     MMA issuer (one thread), tcgen05.mma kind::f16, fp32 accumulate:
+//                S^T  = K Q^T     (A = K, B = Q, both from shared memory)
+//                dP^T = V dO^T    (A = V, B = dO)
+//                dV  += P^T dO    (A = P^T from tensor memory, B = dO)
+//                dK  += dS^T Q    (A = dS^T from tensor memory, B = Q)
+//                dQ   = dS K      (A = dS from shared memory, B = K)
+//   warps 0-3  one thread per key (TMEM lane): P^T = e^(S^T scale - L) with
+//              the causal mask, dS^T = P^T o (dP^T - D), written as bf16 into
+//              tensor memory (for dV and dK) and into shared memory (for dQ);
+//              at the end dK (times scale) and dV are stored as bf16.
+//   warps 4-7  one thread per query: dQ of the step from tensor memory into
+//              a swizzled shared-memory tile, added into an fp32 buffer in
+//              global memory by TMA reduce-add (the page's "dQ is
+//              accumulated with atomics"; the order of the additions, and so
+//              the last bits of dQ, vary from run to run).
+//
+// Tensor memory (512 columns): S^T [0,128) with P^T (bf16) over its first
+// 64 columns; dP^T [128,256) with dS^T (bf16) over its first 64 columns and
+// dQ over [128,128+D) once dK has read dS^T; dV [256,256+D); dK
+// [256+D,256+2D).  MMAs of one thread run in issue order, so a later MMA
+// overwrites a region only after the earlier ones have read it.
+//
+// Every barrier wait is bounded; on expiry the kernel records
+// ATTN_ERR_DEVICE_TIMEOUT, stops, drains its own copies and MMAs, frees
+// tensor memory and returns.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "ptx.cuh"
+
+namespace attn_dev {
+
+constexpr unsigned int kBwdStatusTimeout = 6;  // ATTN_ERR_DEVICE_TIMEOUT
+
+struct BwdParams {
+  __nv_bfloat16 *dk, *dv;  // [B, Hkv, Tk, D]
+  const float *l2;         // [B*Hq, Tq_pad]: LSE * log2(e); +inf on padding rows
+  const float *dvec;       // [B*Hq, Tq_pad]: rowsum(dO o O); 0 on padding rows
+  unsigned int *status;
+  int Hq, Hkv, group;
+  int Tq, Tk, Tq_pad;
+  int n_qt;                // ceil(Tq / 128)
+  int causal;
+  float scale, scale_log2;
+  unsigned long long wait_ns;
+};
+
+template <int D>
+struct BwdCfg {
+  static constexpr int BM = 128;                      // queries per step
+  static constexpr int BN = 128;                      // keys per CTA
+  static constexpr int SPAN = (D >= 64) ? 128 : 64;   // swizzle span of Q/K/V/dO rows
+  static constexpr int CHUNK = SPAN / 2;
+  static constexpr int NCHUNK = D / CHUNK;
+  static constexpr uint32_t LAYOUT = (SPAN == 128) ? kLayoutSW128 : kLayoutSW64;
+  static constexpr int STAGES = (D == 128) ? 1 : 2;
+  static constexpr uint32_t KV_BYTES = BN * D * 2;
+  static constexpr uint32_t QT_BYTES = BM * D * 2;
+  static constexpr uint32_t VEC_BYTES = BM * 4;
+  static constexpr uint32_t STAGE_BYTES = 2 * QT_BYTES + 1024;  // Q | dO | L | D (+pad)
+  static constexpr uint32_t OFF_K = 0;
+  static constexpr uint32_t OFF_V = OFF_K + KV_BYTES;
+  static constexpr uint32_t OFF_STAGE = OFF_V + KV_BYTES;
+  static constexpr uint32_t OFF_DS = OFF_STAGE + STAGES * STAGE_BYTES;  // dS^T, bf16
+  static constexpr uint32_t DS_HALF = BN * 128;  // 64 queries x 128 keys, 128-byte rows
+  static constexpr uint32_t OFF_DQ = OFF_DS + 2 * DS_HALF;  // two 128 x 32 fp32 chunks
+  static constexpr uint32_t DQ_CHUNK = BM * 128;
+  static constexpr uint32_t OFF_BAR = OFF_DQ + 2 * DQ_CHUNK;
+  // kv_full, s_full, p_full, dq_full, dq_empty, dkdv_full, drain, q_full[ST], q_empty[ST]
+  static constexpr int NBAR = 7 + 2 * STAGES;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr uint32_t SMEM_USED = OFF_MISC + 16 + 1024;
+  // At least ~116 KB so that only one CTA (which holds all 512 tensor-memory
+  // columns) is resident per SM.
+  static constexpr uint32_t SMEM_BYTES = SMEM_USED > 118784u ? SMEM_USED : 118784u;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t TM_S = 0, TM_DP = 128, TM_DQ = 128;
+  static constexpr uint32_t TM_DV = 256, TM_DK = 256 + D;
+  static constexpr int THREADS = 320;
+  static_assert(D % CHUNK == 0 && D % 32 == 0, "head dim");
+  static_assert(TM_DK + D <= TMEM_COLS, "tensor memory budget");
+  static_assert(STAGE_BYTES % 1024 == 0 && KV_BYTES % 1024 == 0, "1 KiB regions");
+  static_assert(SMEM_USED <= 232448, "shared memory budget");
+};
+
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+    attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_do,
+                    const __grid_constant__ CUtensorMap tm_dq,
+                    const BwdParams p) {
+  using C = BwdCfg<D>;
+  constexpr int ST = C::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+  uint64_t *kv_full = bars + 0, *s_full = bars + 1, *p_full = bars + 2;
+  uint64_t *dq_full = bars + 3, *dq_empty = bars + 4, *dkdv_full = bars + 5;
+  uint64_t *drain = bars + 6;
+  uint64_t *q_full = bars + 7, *q_empty = q_full + ST;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint64_t wait_ns = p.wait_ns;
+
+  const int kt = blockIdx.x;               // key tile
+  const int bkv = blockIdx.y;              // b * Hkv + K/V head
+  const int b = bkv / p.Hkv;
+  const int g = bkv - b * p.Hkv;
+  const int delta = p.Tk - p.Tq;           // bottom-right causal alignment
+  // Query tiles that see any key of this tile: under causal masking query i
+  // sees key j iff j <= i + delta.
+  const int qt_lo = p.causal ? max(0, kt * C::BN - delta) / C::BM : 0;
+  const int n_q = p.n_qt - qt_lo;
+  const int n_steps = n_q > 0 ? p.group * n_q : 0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    mbar_init(s_full, 1);
+    mbar_init(p_full, 128);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_empty, 128);
+    mbar_init(dkdv_full, 1);
+    mbar_init(drain, 1);
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_empty[s], 1);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+    prefetch_tmap(&tm_do);
+    prefetch_tmap(&tm_dq);
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  auto fail = [&]() {
+    atomicExch(p.status, kBwdStatusTimeout);
+    *abort_flag = 1;
+  };
+  // step s -> query head and query tile
+  auto step_head = [&](int s) { return g * p.group + s / n_q; };
+  auto step_qt = [&](int s) { return qt_lo + s % n_q; };
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      bool ok = true;
+      int last[ST];
+      for (int s = 0; s < ST; ++s) last[s] = -1;
+      mbar_arrive_expect_tx(kv_full, 2 * C::KV_BYTES);
+      for (int c = 0; c < C::NCHUNK; ++c) {
+        tma_load_3d(smem + C::OFF_K + c * (C::BN * C::SPAN), &tm_k, kv_full, c * C::CHUNK,
+                    kt * C::BN, bkv);
+        tma_load_3d(smem + C::OFF_V + c * (C::BN * C::SPAN), &tm_v, kv_full, c * C::CHUNK,
+                    kt * C::BN, bkv);
+      }
+      for (int s = 0; s < n_steps && ok; ++s) {
+        const int st = s % ST, u = s / ST;
+        if (*abort_flag) { ok = false; break; }
+        if (s >= ST && !mbar_wait(&q_empty[st], (u - 1) & 1, wait_ns)) { ok = false; break; }
+        const int bh = b * p.Hq + step_head(s);
+        const int q0 = step_qt(s) * C::BM;
+        uint8_t *stage = smem + C::OFF_STAGE + st * C::STAGE_BYTES;
+        mbar_arrive_expect_tx(&q_full[st], 2 * C::QT_BYTES + 2 * C::VEC_BYTES);
+        for (int c = 0; c < C::NCHUNK; ++c) {
+          tma_load_3d(stage + c * (C::BM * C::SPAN), &tm_q, &q_full[st], c * C::CHUNK, q0, bh);
+          tma_load_3d(stage + C::QT_BYTES + c * (C::BM * C::SPAN), &tm_do, &q_full[st],
+                      c * C::CHUNK, q0, bh);
+        }
+        const size_t voff = (size_t)bh * p.Tq_pad + q0;
+        bulk_load(stage + 2 * C::QT_BYTES, p.l2 + voff, C::VEC_BYTES, &q_full[st]);
+        bulk_load(stage + 2 * C::QT_BYTES + C::VEC_BYTES, p.dvec + voff, C::VEC_BYTES,
+                  &q_full[st]);
+        last[st] = s;
+      }
+      if (!ok) fail();
+      // Drain: every copy issued has landed before shared memory is released.
+      mbar_wait(kv_full, 0, wait_ns);
+      for (int s = 0; s < ST; ++s)
+        if (last[s] >= 0) mbar_wait(&q_full[s], (last[s] / ST) & 1, wait_ns);
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t I_S = make_idesc_bf16(C::BN, C::BM, false);   // S^T, dP^T
+      constexpr uint32_t I_ACC = make_idesc_bf16(C::BN, D, true);      // dV, dK
+      constexpr uint32_t I_DQ = make_idesc_bf16_ab(C::BM, D, true, true);
+      // K-major operands (rows of D, chunks of CHUNK columns)
+      const uint64_t k_kd = make_smem_desc(sbase + C::OFF_K, 16, 8 * C::SPAN, C::LAYOUT);
+      const uint64_t v_kd = make_smem_desc(sbase + C::OFF_V, 16, 8 * C::SPAN, C::LAYOUT);
+      // MN-major views of the same tiles: LBO = next CHUNK columns, SBO = next 8 rows
+      const uint64_t k_md =
+          make_smem_desc(sbase + C::OFF_K, C::BN * C::SPAN, 8 * C::SPAN, C::LAYOUT);
+      // dS as the MN-major A of dQ: rows = keys (128 bytes = 64 queries per half)
+      const uint64_t ds_md = make_smem_desc(sbase + C::OFF_DS, C::DS_HALF, 8 * 128, kLayoutSW128);
+      auto adv = [](uint64_t desc, uint32_t bytes) { return desc + (uint64_t)(bytes >> 4); };
+      bool ok = mbar_wait(kv_full, 0, wait_ns);
+      for (int s = 0; s < n_steps && ok; ++s) {
+        const int st = s % ST, u = s / ST;
+        if (*abort_flag || !mbar_wait(&q_full[st], u & 1, wait_ns)) { ok = false; break; }
+        const uint32_t stage = sbase + C::OFF_STAGE + st * C::STAGE_BYTES;
+        const uint64_t q_kd = make_smem_desc(stage, 16, 8 * C::SPAN, C::LAYOUT);
+        const uint64_t do_kd = make_smem_desc(stage + C::QT_BYTES, 16, 8 * C::SPAN, C::LAYOUT);
+        const uint64_t q_md = make_smem_desc(stage, C::BM * C::SPAN, 8 * C::SPAN, C::LAYOUT);
+        const uint64_t do_md =
+            make_smem_desc(stage + C::QT_BYTES, C::BM * C::SPAN, 8 * C::SPAN, C::LAYOUT);
+        // S^T = K Q^T
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk * 16) / C::CHUNK) * (C::BN * C::SPAN) + ((kk * 16) % C::CHUNK) * 2;
+          mma_bf16_ss(tmem + C::TM_S, adv(k_kd, off), adv(q_kd, off), I_S, kk > 0 ? 1u : 0u);
+        }
+        // dP^T overwrites the previous step's dQ: wait until it has been read.
+        if (s > 0 && !mbar_wait(dq_empty, (s - 1) & 1, wait_ns)) { ok = false; break; }
+        // dP^T = V dO^T
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk * 16) / C::CHUNK) * (C::BN * C::SPAN) + ((kk * 16) % C::CHUNK) * 2;
+          mma_bf16_ss(tmem + C::TM_DP, adv(v_kd, off), adv(do_kd, off), I_S, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(s_full);
+        if (!mbar_wait(p_full, s & 1, wait_ns)) { ok = false; break; }
+        tc_fence_after();  // P^T and dS^T were written to tensor memory by other threads
+        // dV += P^T dO,  dK += dS^T Q   (16 queries = 8 columns of packed bf16)
+#pragma unroll
+        for (int kk = 0; kk < C::BM / 16; ++kk)
+          mma_bf16_ts(tmem + C::TM_DV, tmem + C::TM_S + kk * 8, adv(do_md, kk * 16 * C::SPAN),
+                      I_ACC, (s > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < C::BM / 16; ++kk)
+          mma_bf16_ts(tmem + C::TM_DK, tmem + C::TM_DP + kk * 8, adv(q_md, kk * 16 * C::SPAN),
+                      I_ACC, (s > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&q_empty[st]);  // Q, dO, L, D of this stage are no longer read
+        // dQ = dS K   (16 keys per MMA)
+#pragma unroll
+        for (int kk = 0; kk < C::BN / 16; ++kk)
+          mma_bf16_ss(tmem + C::TM_DQ, adv(ds_md, kk * 16 * 128), adv(k_md, kk * 16 * C::SPAN),
+                      I_DQ, kk > 0 ? 1u : 0u);
+        mma_commit(dq_full);
+      }
+      if (!ok) fail();
+      mma_commit(dkdv_full);
+      mma_commit(drain);
+      mbar_wait(drain, 0, wait_ns);
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    // ------------------------------------------- P and dS, one key per thread
+    const int r = threadIdx.x;  // key row of the tile == TMEM lane
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const int key = kt * C::BN + r;
+    const bool key_ok = key < p.Tk;
+    const float sl2 = p.scale_log2;
+    uint8_t *ds_row = smem + C::OFF_DS + r * 128;
+    bool ok = true;
+    for (int s = 0; s < n_steps; ++s) {
+      ok = __all_sync(0xffffffffu, mbar_wait(s_full, s & 1, wait_ns) && !*abort_flag);
+      if (!ok) break;
+      tc_fence_after();
+      const int st = s % ST;
+      const int q0 = step_qt(s) * C::BM;
+      const float *l2s = reinterpret_cast<const float *>(smem + C::OFF_STAGE +
+                                                         st * C::STAGE_BYTES + 2 * C::QT_BYTES);
+      const float *dvs = l2s + C::BM;
+      // keys above the diagonal of some query of the tile need the mask
+      const bool need_mask = p.causal && (kt * C::BN + C::BN - 1 > q0 + delta);
+      const int lim = key - delta - q0;  // query q (in tile) sees the key iff q >= lim
+#pragma unroll 1
+      for (int c = 0; c < C::BM / 32; ++c) {
+        float sv[32], dp[32];
+        tmem_ld32_wait(tmem + lane_base + C::TM_S + c * 32, sv);
+        tmem_ld32_wait(tmem + lane_base + C::TM_DP + c * 32, dp);
+        uint32_t pw[16], dw[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const int q = c * 32 + i;
+          float p0 = ex2_approx(fmaf(sv[i], sl2, -l2s[q]));
+          float p1 = ex2_approx(fmaf(sv[i + 1], sl2, -l2s[q + 1]));
+          if (need_mask) {
+            if (q < lim) p0 = 0.f;
+            if (q + 1 < lim) p1 = 0.f;
+          }
+          if (!key_ok) p0 = p1 = 0.f;
+          const float d0 = p0 * (dp[i] - dvs[q]);
+          const float d1 = p1 * (dp[i + 1] - dvs[q + 1]);
+          pw[i / 2] = pack_bf16x2(p0, p1);
+          dw[i / 2] = pack_bf16x2(d0, d1);
+        }
+        // P^T over S^T's columns [16c, 16c+16) and dS^T over dP^T's: those
+        // scores were loaded in this or an earlier chunk.
+        tmem_st16(tmem + lane_base + C::TM_S + c * 16, pw);
+        tmem_st16(tmem + lane_base + C::TM_DP + c * 16, dw);
+        // dS^T row into shared memory: queries [32c, 32c+32) are 16-byte
+        // units 4(c%2) .. 4(c%2)+3 of half c/2, swizzled by the row.
+        uint8_t *half = ds_row + (c >> 1) * C::DS_HALF;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int unit = (c & 1) * 4 + j;
+          *reinterpret_cast<uint4 *>(half + ((unit ^ (r & 7)) << 4)) =
+              make_uint4(dw[4 * j], dw[4 * j + 1], dw[4 * j + 2], dw[4 * j + 3]);
+        }
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();  // dS in shared memory, for the tensor core
+      tc_fence_before();
+      mbar_arrive(p_full);
+    }
+    if (!ok) fail();
+    // ---- dK (times scale) and dV of this key tile, bf16
+    if (n_steps > 0 && ok) {
+      ok = __all_sync(0xffffffffu, mbar_wait(dkdv_full, 0, wait_ns));
+      if (!ok) fail();
+    }
+    if (ok) {
+      tc_fence_after();
+      const size_t row = ((size_t)bkv * p.Tk + key) * D;
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t col = which == 0 ? C::TM_DV : C::TM_DK;
+        const float mul = which == 0 ? 1.f : p.scale;
+        __nv_bfloat16 *dst = (which == 0 ? p.dv : p.dk) + row;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          float v[32];
+          if (n_steps > 0) {
+            tmem_ld32_wait(tmem + lane_base + col + c * 32, v);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0.f;
+          }
+          if (key_ok) {
+            uint4 *o = reinterpret_cast<uint4 *>(dst + c * 32);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              o[u] = make_uint4(pack_bf16x2(v[8 * u] * mul, v[8 * u + 1] * mul),
+                                pack_bf16x2(v[8 * u + 2] * mul, v[8 * u + 3] * mul),
+                                pack_bf16x2(v[8 * u + 4] * mul, v[8 * u + 5] * mul),
+                                pack_bf16x2(v[8 * u + 6] * mul, v[8 * u + 7] * mul));
+          }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------ dQ of each step, one query per thread
+    const int r = threadIdx.x - 128;  // query row of the step == TMEM lane
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const bool elected = (r == 0);
+    bool ok = true;
+    int n = 0;  // dQ chunks staged so far
+    for (int s = 0; s < n_steps; ++s) {
+      ok = __all_sync(0xffffffffu, mbar_wait(dq_full, s & 1, wait_ns) && !*abort_flag);
+      if (!ok) break;
+      tc_fence_after();
+      const int bh = b * p.Hq + step_head(s);
+      const int q0 = step_qt(s) * C::BM;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c, ++n) {
+        float v[32];
+        tmem_ld32_wait(tmem + lane_base + C::TM_DQ + c * 32, v);
+        if (c == D / 32 - 1) {
+          tc_fence_before();
+          mbar_arrive(dq_empty);  // the step's dQ has left tensor memory
+        }
+        uint8_t *buf = smem + C::OFF_DQ + (n & 1) * C::DQ_CHUNK;
+        // the reduce that last read this buffer (two chunks ago) is done
+        if (elected && n >= 2) bulk_wait_group_read1();
+        named_barrier_sync(1, 128);
+        uint8_t *row = buf + r * 128;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<float4 *>(row + ((u ^ (r & 7)) << 4)) =
+              make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+        fence_proxy_async_smem();
+        named_barrier_sync(1, 128);
+        if (elected) {
+          tma_reduce_add_3d(&tm_dq, buf, c * 32, q0, bh);
+          bulk_commit_group();
+        }
+      }
+    }
+    if (!ok) fail();
+    if (elected) bulk_wait_group0();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// D_i = dO_i . O_i and L_i * log2(e) per query row (padding rows to a
+// multiple of 128 get +inf and 0, so their probabilities vanish), and the
+// fp32 dQ accumulator zeroed.  One warp per row.
+template <int D>
+__global__ void __launch_bounds__(256)
+    attn_bwd_prep_kernel(const __nv_bfloat16 *__restrict__ o,
+                         const __nv_bfloat16 *__restrict__ dout,
+                         const float *__restrict__ lse, float *__restrict__ dq_acc,
+                         float *__restrict__ l2, float *__restrict__ dvec, int rows_bh,
+                         int Tq, int Tq_pad) {
+  constexpr int VEC = D / 32;
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= rows_bh * Tq_pad) return;
+  const int bh = warp / Tq_pad;
+  const int i = warp - bh * Tq_pad;
+  if (i >= Tq) {
+    if (lane == 0) {
+      l2[warp] = INFINITY;
+      dvec[warp] = 0.f;
+    }
+    return;
+  }
+  const size_t row = (size_t)bh * Tq + i;
+  const __nv_bfloat16 *orow = o + row * D + lane * VEC;
+  const __nv_bfloat16 *drow = dout + row * D + lane * VEC;
+  float acc = 0.f;
+#pragma unroll
+  for (int e = 0; e < VEC; ++e)
+    acc = fmaf(__bfloat162float(orow[e]), __bfloat162float(drow[e]), acc);
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  float *qrow = dq_acc + row * D + lane * VEC;
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) qrow[e] = 0.f;
+  if (lane == 0) {
+    l2[warp] = lse[row] * 1.4426950408889634f;
+    dvec[warp] = acc;
+  }
+}
+
+// dQ = scale * accumulator, rounded to bf16.
+__global__ void __launch_bounds__(256)
+    attn_bwd_dq_kernel(const float4 *__restrict__ acc, uint2 *__restrict__ dq, size_t n4,
+                       float scale) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const float4 a = acc[i];
+    dq[i] = make_uint2(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale));
+  }
+}
+
+}  // namespace attn_dev

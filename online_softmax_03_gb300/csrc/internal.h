@@ -45,11 +45,26 @@ struct DecodeArgs {
   int page_size = 0, num_pages = 0, max_pages = 0;
 };
 
+struct BwdArgs {
+  const void *q, *k, *v, *o, *dout;
+  const float *lse;
+  void *dq, *dk, *dv;
+  int B, Hq, Hkv, Tq, Tk, d, causal;
+  float scale;
+  void *workspace;
+  size_t workspace_bytes;
+  cudaStream_t stream;
+  unsigned long long wait_ns;
+};
+
 // Return an attn_status code.
 int prefill_launch(const PrefillArgs &a);
 int decode_launch(const DecodeArgs &a);
 int prefill_take_status(cudaStream_t s, unsigned int *out);
 int decode_take_status(cudaStream_t s, unsigned int *out);
+int bwd_launch(const BwdArgs &a);
+int bwd_take_status(cudaStream_t s, unsigned int *out);
+size_t bwd_workspace_bytes_for(int B, int Hq, int Tq, int d);
 
 // Shared helpers (api.cu).
 int validate_decode_args(const void *q, const void *k, const void *v, const void *o,
@@ -61,6 +76,11 @@ int check_device_sm103(int *num_sms);
 bool encode_tmap_3d_bf16(CUtensorMap *map, const void *base, uint64_t inner,
                          uint64_t rows, uint64_t planes, uint32_t box_inner,
                          uint32_t box_rows, uint32_t box_planes, int swizzle_bytes);
+
+// The same for a 3-D fp32 tensor map with 128-byte swizzle (box_inner = 32).
+bool encode_tmap_3d_f32(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
+                        uint64_t planes, uint32_t box_inner, uint32_t box_rows,
+                        uint32_t box_planes);
 
 // Packed-batch planning list capacity and its scratch bytes.
 long long varlen_list_capacity(int B, int total_q, int max_seqlen_q);

@@ -118,6 +118,28 @@ __device__ __forceinline__ void bulk_wait_group_read0() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// Wait until at most one bulk group of this thread still reads shared memory.
+__device__ __forceinline__ void bulk_wait_group_read1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
+// Wait until every bulk group of this thread has completed.
+__device__ __forceinline__ void bulk_wait_group0() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// 3-D tiled reduce-add of one box from shared memory into global memory
+// (element type and bounds from the tensor map; bulk-group completion).
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap *m,
+                                                  const void *src, int x,
+                                                  int y, int z) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group "
+      "[%0, {%2, %3, %4}], [%1];" ::"l"(reinterpret_cast<uint64_t>(m)),
+      "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
 // Make this thread's generic-proxy shared-memory writes visible to the
 // async proxy (TMA engine, tensor cores).
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -350,6 +372,12 @@ __host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N,
          | ((b_mn_major ? 1u : 0u) << 16) // B major-ness
          | ((uint32_t)(N >> 3) << 17)     // N / 8
          | ((uint32_t)(M >> 4) << 24);    // M / 16
+}
+
+// The same with the major-ness of A given too (a_mn_major: M contiguous).
+__host__ __device__ constexpr uint32_t make_idesc_bf16_ab(int M, int N, bool a_mn_major,
+                                                          bool b_mn_major) {
+  return make_idesc_bf16(M, N, b_mn_major) | ((a_mn_major ? 1u : 0u) << 15);
 }
 
 // Byte offset of the 16-byte unit at linear offset `off` inside a region laid

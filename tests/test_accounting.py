@@ -70,3 +70,9 @@ def test_varlen_flops_counts_each_document_alone():
         assert acc.varlen_flops(lq, lk, 6, 8, causal) == want
     # one document of T tokens is the dense causal count, T(T+1)/2 pairs
     assert acc.varlen_flops([4096], [4096], 32, 128, True) == 4.0 * 128 * 32 * 4096 * 4097 // 2
+
+
+def test_backward_flops_are_five_products():
+    assert acc.backward_flops(4, 32, 4096, 4096, 128, True) == 2.5 * acc.attention_flops(
+        4, 32, 4096, 4096, 128, True)
+    assert acc.backward_flops(1, 1, 3, 5, 2, False) == 5 * 2 * 3 * 5 * 2
