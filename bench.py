@@ -58,6 +58,7 @@ def source_sha(*names):
 
 
 PREFILL_SOURCES = ("ptx.cuh", "prefill_kernel.cuh", "prefill.cu")
+BACKWARD_SOURCES = ("ptx.cuh", "backward_kernel.cuh", "backward.cu")
 DECODE_SOURCES = ("ptx.cuh", "decode_kernel.cuh", "decode.cu")
 
 
@@ -493,6 +494,8 @@ def run_ours(args, rank, world, local_rank):
                 PREFILL.B, PREFILL.Hq, PREFILL.Tq, PREFILL.Tk, PREFILL.d, True)
                 / (bwd_ms / 1e3) / 1e12 / peak_tf, 4),
             "launches": "prep + backward kernel + dQ conversion",
+            "traffic_main_kernel": ncu_traffic("attn_bwd_kernel<128>/" + PREFILL.name,
+                                               source_sha(*BACKWARD_SOURCES)),
         },
         "gpu_launches": K * 3,
         "clocks": clk,
