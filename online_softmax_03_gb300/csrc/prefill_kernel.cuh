@@ -27,7 +27,8 @@
 //   warp 8     TMA producer: Q tiles (as soon as the previous item's last
 //              S_t no longer needs them) and K and V tiles into a ring of
 //              STAGES shared-memory slots (swizzled boxes), across items.
-//   warp 9     MMA issuer (one thread), tcgen05.mma kind::f16, bf16 operands,
+//   warp 9     MMA issuer (the warp runs converged; one elected lane issues),
+//              tcgen05.mma kind::f16, bf16 operands,
 //              fp32 accumulation in tensor memory:
 //                S_t = Q_t K_j^T    A and B from shared memory,
 //                O_t += P_t V_j     A = P_t from tensor memory, B = V_j.
@@ -443,13 +444,21 @@ __global__ void __launch_bounds__(320, 1)
     __syncwarp();
   } else if (warp == C::MMA_WARP) {
     // ------------------------------------------------------- MMA issuer
-    // The tensor core's instruction queue is short, so every instruction this
-    // thread runs between MMAs can leave it idle: descriptors are built once
-    // and advanced by compile-time byte offsets (the start address sits in
-    // the low bits in 16-byte units), the two tiles are unrolled, and only
-    // waits on barriers that other threads' tensor-memory writes complete are
-    // followed by a tcgen05 fence.
-    if (lane == 0) {
+    // The tensor core's instruction queue is short, so every instruction the
+    // issuer runs between MMAs can leave it idle.  The whole warp runs this
+    // loop converged and one elected lane issues each MMA and commit: the
+    // descriptors (built once, advanced by compile-time byte offsets; the
+    // start address sits in the low bits in 16-byte units) then stay in
+    // uniform registers, which keeps the issue stream short even while the
+    // softmax warps on the same sub-partition compete for issue slots.  Every
+    // wait is a warp vote so the lanes cannot diverge.  Only waits on barriers
+    // that other threads' tensor-memory writes complete are followed by a
+    // tcgen05 fence.
+    {
+      auto wait_all = [&](uint64_t *bar, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity, wait_ns));
+      };
+      auto aborted = [&]() -> bool { return __any_sync(0xffffffffu, *abort_flag != 0); };
       constexpr uint32_t IDESC_QK = make_idesc_bf16(C::BM, C::BN, false);
       constexpr uint32_t IDESC_PV = make_idesc_bf16(C::BM, D, true);
       const uint64_t q_desc = make_smem_desc(sbase + C::OFF_Q, 16, 8 * C::SPAN, C::LAYOUT);
@@ -463,7 +472,7 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk * 16) / C::CHUNK) * (C::BM * C::SPAN) + ((kk * 16) % C::CHUNK) * 2;
-          mma_bf16_ss(tmem + C::tm_s(t), adv(q_desc, t * C::Q_BYTES + off), adv(kd, off),
+          mma_bf16_ss_elect(tmem + C::tm_s(t), adv(q_desc, t * C::Q_BYTES + off), adv(kd, off),
                       IDESC_QK, kk > 0 ? 1u : 0u);
         }
       };
@@ -471,7 +480,7 @@ __global__ void __launch_bounds__(320, 1)
         const uint64_t vd = adv(v_desc, s * C::KV_BYTES);
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)  // 16 keys = 8 TMEM columns of P
-          mma_bf16_ts(tmem + C::tm_o(t), tmem + C::tm_s(t) + kk * 8, adv(vd, kk * 16 * C::SPAN),
+          mma_bf16_ts_elect(tmem + C::tm_o(t), tmem + C::tm_s(t) + kk * 8, adv(vd, kk * 16 * C::SPAN),
                       IDESC_PV, (acc || kk > 0) ? 1u : 0u);
       };
       bool ok = true;
@@ -481,27 +490,27 @@ __global__ void __launch_bounds__(320, 1)
       for (int fetch = 0; ok;) {
         int idx = -1;
         VarlenItem vi;
-        if (!take_item(fetch, idx, vi)) { ok = false; break; }
-        mbar_arrive(&item_empty[(fetch - 1) & 1]);
+        if (!__all_sync(0xffffffffu, take_item(fetch, idx, vi))) { ok = false; break; }
+        if (lane == 0) mbar_arrive(&item_empty[(fetch - 1) & 1]);
         if (idx < 0) break;
         const PrefillItem it = kVarlen ? varlen_prefill_item(p, vi) : prefill_item<kWindow>(p, idx);
         const int jb = kWindow ? it.jbeg() : 0, je = it.jend();
         // S_t of K/V tile jj in stage sj, the first S of tile t's range.
         auto start_tile = [&](const int t, int &q_cnt, const int sj, const int jj) -> bool {
-          if (!mbar_wait(&q_full[t], q_cnt & 1, wait_ns)) return false;
+          if (!wait_all(&q_full[t], q_cnt & 1)) return false;
           ++q_cnt;
           issue_s(t, sj);
-          mma_commit(&s_full[t]);
-          if (jj + 1 == it.hi(t)) mma_commit(&q_empty[t]);  // its only S
+          mma_commit_elect(&s_full[t]);
+          if (jj + 1 == it.hi(t)) mma_commit_elect(&q_empty[t]);  // its only S
           return true;
         };
         {
           // First S of the tiles whose range starts at the item's first tile.
           const int s0 = kv % ST;
-          if (*abort_flag || !mbar_wait(&k_full[s0], (kv / ST) & 1, wait_ns)) { ok = false; break; }
+          if (aborted() || !wait_all(&k_full[s0], (kv / ST) & 1)) { ok = false; break; }
           if (it.has(0) && it.lo0 == jb && !start_tile(0, q_cnt0, s0, jb)) { ok = false; break; }
           if (it.has(1) && it.lo1 == jb && !start_tile(1, q_cnt1, s0, jb)) { ok = false; break; }
-          mma_commit(&k_empty[s0]);
+          mma_commit_elect(&k_empty[s0]);
         }
         for (int j = jb; j < je; ++j) {
           const int c = kv + (j - jb);  // ring position of K/V tile j
@@ -510,7 +519,7 @@ __global__ void __launch_bounds__(320, 1)
           bool v_ready = false, k_ready = false;
           auto need_k = [&]() -> bool {
             if (k_ready) return true;
-            if (!mbar_wait(&k_full[s1], u1 & 1, wait_ns)) return false;
+            if (!wait_all(&k_full[s1], u1 & 1)) return false;
             k_ready = true;
             return true;
           };
@@ -518,14 +527,14 @@ __global__ void __launch_bounds__(320, 1)
           // S_t if the tile's range starts with the next K/V tile.
           auto tile_step = [&](const int t, int &p_cnt, int &q_cnt) -> bool {
             // Without a window every range starts at 0 and this reduces to
-            // "j < hi": the issuing thread is the kernel's bottleneck, so the
+            // "j < hi": the issuing warp is the kernel's bottleneck, so the
             // plain case carries none of the range logic.
             const int lo = kWindow ? it.lo(t) : 0, hi = it.hi(t);
             if ((!kWindow || lo <= j) && j < hi) {
-              if (!mbar_wait(&p_full[t], p_cnt & 1, wait_ns)) return false;
+              if (!wait_all(&p_full[t], p_cnt & 1)) return false;
               ++p_cnt;
               if (!v_ready) {
-                if (!mbar_wait(&v_full[s], u & 1, wait_ns)) return false;
+                if (!wait_all(&v_full[s], u & 1)) return false;
                 v_ready = true;
               }
               tc_fence_after();  // P_t was written to tensor memory by the softmax threads
@@ -533,30 +542,30 @@ __global__ void __launch_bounds__(320, 1)
               if (j + 1 < hi) {
                 if (!need_k()) return false;
                 issue_s(t, s1);
-                mma_commit(&s_full[t]);
-                if (j + 2 == hi) mma_commit(&q_empty[t]);  // last S_t of the item
+                mma_commit_elect(&s_full[t]);
+                if (j + 2 == hi) mma_commit_elect(&q_empty[t]);  // last S_t of the item
               } else {
-                mma_commit(&o_done[t]);
+                mma_commit_elect(&o_done[t]);
               }
             } else if (kWindow && j + 1 == lo && lo < hi) {
               if (!need_k() || !start_tile(t, q_cnt, s1, j + 1)) return false;
             }
             return true;
           };
-          if (*abort_flag || !tile_step(0, p_cnt0, q_cnt0) || !tile_step(1, p_cnt1, q_cnt1)) {
+          if (aborted() || !tile_step(0, p_cnt0, q_cnt0) || !tile_step(1, p_cnt1, q_cnt1)) {
             ok = false;
             break;
           }
-          mma_commit(&v_empty[s]);
-          if (k_ready) mma_commit(&k_empty[s1]);
+          mma_commit_elect(&v_empty[s]);
+          if (k_ready) mma_commit_elect(&k_empty[s1]);
         }
         kv += je - jb;
       }
       if (!ok) fail();
-      // Drain: all MMAs issued by this thread have completed before tensor
+      // Drain: all MMAs issued by this warp have completed before tensor
       // memory is freed.
-      mma_commit(drain);
-      mbar_wait(drain, 0, wait_ns);
+      mma_commit_elect(drain);
+      wait_all(drain, 0);
     }
     __syncwarp();
   } else {
