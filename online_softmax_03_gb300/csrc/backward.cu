@@ -38,6 +38,16 @@ int launch_bwd(const attn_host::BwdArgs &a, unsigned int *status) {
   }
   // 2. dK, dV per key tile; dQ accumulated
   attn_dev::BwdParams p{};
+  constexpr bool kPipelined = (D == 128);
+  if (kPipelined) {
+    // 64-query steps: Q/dO boxes of 64 rows, dQ staged 64 rows at a time
+    using P = attn_dev::BwdPipeCfg;
+    if (!attn_host::encode_tmap_3d_bf16(&tq, a.q, D, a.Tq, bhq, P::CHUNK, P::BM, 1, P::SPAN) ||
+        !attn_host::encode_tmap_3d_bf16(&tdo, a.dout, D, a.Tq, bhq, P::CHUNK, P::BM, 1,
+                                        P::SPAN) ||
+        !attn_host::encode_tmap_3d_f32(&tdq, dq_acc, D, a.Tq, bhq, 32, P::BM, 1))
+      return ATTN_ERR_CUDA;
+  }
   p.dk = static_cast<__nv_bfloat16 *>(a.dk);
   p.dv = static_cast<__nv_bfloat16 *>(a.dv);
   p.l2 = l2;
@@ -54,12 +64,12 @@ int launch_bwd(const attn_host::BwdArgs &a, unsigned int *status) {
   p.scale = a.scale;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.wait_ns = a.wait_ns;
-  auto kern = attn_dev::attn_bwd_kernel<D>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)C::SMEM_BYTES) != cudaSuccess)
+  auto kern = kPipelined ? attn_dev::attn_bwd_pipelined_kernel : attn_dev::attn_bwd_kernel<D>;
+  const uint32_t smem = kPipelined ? attn_dev::BwdPipeCfg::SMEM_BYTES : C::SMEM_BYTES;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
     return ATTN_ERR_CUDA;
-  kern<<<dim3(n_kt, (unsigned)bhk), C::THREADS, C::SMEM_BYTES, a.stream>>>(tq, tk, tv, tdo, tdq,
-                                                                          p);
+  kern<<<dim3(n_kt, (unsigned)bhk), C::THREADS, smem, a.stream>>>(tq, tk, tv, tdo, tdq, p);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   // 3. dQ = scale * accumulator in bf16
   {

@@ -19,7 +19,8 @@
 //
 //   warp 8     producer: K and V of the key tile once, then per step the Q
 //              and dO tiles (TMA) and the step's L and D values (bulk copy).
-//   warp 9     MMA issuer (one thread), tcgen05.mma kind::f16, fp32 accumulate:
+//   warp 9     MMA issuer (converged warp, one elected lane issues), tcgen05.mma
+//              kind::f16, fp32 accumulate:
 //                S^T  = K Q^T     (A = K, B = Q, both from shared memory)
 //                dP^T = V dO^T    (A = V, B = dO)
 //                dV  += P^T dO    (A = P^T from tensor memory, B = dO)
@@ -34,6 +35,10 @@
 //              global memory by TMA reduce-add (the page's "dQ is
 //              accumulated with atomics"; the order of the additions, and so
 //              the last bits of dQ, vary from run to run).
+//
+// Shared memory: K and V of the tile, two stages of (Q, dO, L, D), and the
+// dS tile, which also stages dQ for the reduction once the dQ MMA has read
+// dS (the next step's dS waits for that reduction to have read it).
 //
 // Tensor memory (512 columns): S^T [0,128) with P^T (bf16) over its first
 // 64 columns; dP^T [128,256) with dS^T (bf16) over its first 64 columns and
@@ -52,7 +57,8 @@
 
 namespace attn_dev {
 
-constexpr unsigned int kBwdStatusTimeout = 6;  // ATTN_ERR_DEVICE_TIMEOUT
+constexpr unsigned int kBwdStatusTimeout = 6;     // ATTN_ERR_DEVICE_TIMEOUT
+constexpr unsigned int kBwdStatusMisaligned = 3;  // ATTN_ERR_MISALIGNED
 
 struct BwdParams {
   __nv_bfloat16 *dk, *dv;  // [B, Hkv, Tk, D]
@@ -75,7 +81,7 @@ struct BwdCfg {
   static constexpr int CHUNK = SPAN / 2;
   static constexpr int NCHUNK = D / CHUNK;
   static constexpr uint32_t LAYOUT = (SPAN == 128) ? kLayoutSW128 : kLayoutSW64;
-  static constexpr int STAGES = (D == 128) ? 1 : 2;
+  static constexpr int STAGES = 2;
   static constexpr uint32_t KV_BYTES = BN * D * 2;
   static constexpr uint32_t QT_BYTES = BM * D * 2;
   static constexpr uint32_t VEC_BYTES = BM * 4;
@@ -85,13 +91,18 @@ struct BwdCfg {
   static constexpr uint32_t OFF_STAGE = OFF_V + KV_BYTES;
   static constexpr uint32_t OFF_DS = OFF_STAGE + STAGES * STAGE_BYTES;  // dS^T, bf16
   static constexpr uint32_t DS_HALF = BN * 128;  // 64 queries x 128 keys, 128-byte rows
-  static constexpr uint32_t OFF_DQ = OFF_DS + 2 * DS_HALF;  // two 128 x 32 fp32 chunks
+  // dQ is staged, in two 128 x 32 fp32 chunks (128-byte swizzled rows),
+  // in the dS region once the step's dQ MMA has read dS.
   static constexpr uint32_t DQ_CHUNK = BM * 128;
-  static constexpr uint32_t OFF_BAR = OFF_DQ + 2 * DQ_CHUNK;
-  // kv_full, s_full, p_full, dq_full, dq_empty, dkdv_full, drain, q_full[ST], q_empty[ST]
-  static constexpr int NBAR = 7 + 2 * STAGES;
+  static_assert(2 * DQ_CHUNK <= 2 * DS_HALF, "dQ staging fits the dS region");
+  static constexpr uint32_t OFF_BAR = OFF_DS + 2 * DS_HALF;
+  // kv_full, s_full, p_full, dq_full, dq_empty, dkdv_full, drain, ds_free,
+  // q_full[ST], q_empty[ST]
+  static constexpr int NBAR = 8 + 2 * STAGES;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr uint32_t SMEM_USED = OFF_MISC + 16 + 1024;
+  // The dynamic shared-memory window starts 1024-byte aligned (the kernel
+  // checks this), so no alignment slack is added.
+  static constexpr uint32_t SMEM_USED = OFF_MISC + 16;
   // At least ~116 KB so that only one CTA (which holds all 512 tensor-memory
   // columns) is resident per SM.
   static constexpr uint32_t SMEM_BYTES = SMEM_USED > 118784u ? SMEM_USED : 118784u;
@@ -116,14 +127,17 @@ __global__ void __launch_bounds__(320, 1)
   using C = BwdCfg<D>;
   constexpr int ST = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *smem = smem_raw;
   const uint32_t sbase = smem_u32(smem);
+  if (sbase & 1023u) {  // the swizzled tiles need 1024-byte alignment
+    if (threadIdx.x == 0) atomicExch(p.status, kBwdStatusMisaligned);
+    return;
+  }
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
   uint64_t *kv_full = bars + 0, *s_full = bars + 1, *p_full = bars + 2;
   uint64_t *dq_full = bars + 3, *dq_empty = bars + 4, *dkdv_full = bars + 5;
-  uint64_t *drain = bars + 6;
-  uint64_t *q_full = bars + 7, *q_empty = q_full + ST;
+  uint64_t *drain = bars + 6, *ds_free = bars + 7;
+  uint64_t *q_full = bars + 8, *q_empty = q_full + ST;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
 
@@ -150,6 +164,7 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(dq_empty, 128);
     mbar_init(dkdv_full, 1);
     mbar_init(drain, 1);
+    mbar_init(ds_free, 1);
     for (int s = 0; s < ST; ++s) {
       mbar_init(&q_full[s], 1);
       mbar_init(&q_empty[s], 1);
@@ -220,7 +235,12 @@ __global__ void __launch_bounds__(320, 1)
     __syncwarp();
   } else if (warp == 9) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    // The warp runs converged and one elected lane issues each MMA and commit
+    // (descriptors stay in uniform registers); every wait is a warp vote.
+    {
+      auto wait_all = [&](uint64_t *bar, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity, wait_ns));
+      };
       constexpr uint32_t I_S = make_idesc_bf16(C::BN, C::BM, false);   // S^T, dP^T
       constexpr uint32_t I_ACC = make_idesc_bf16(C::BN, D, true);      // dV, dK
       constexpr uint32_t I_DQ = make_idesc_bf16_ab(C::BM, D, true, true);
@@ -233,10 +253,13 @@ __global__ void __launch_bounds__(320, 1)
       // dS as the MN-major A of dQ: rows = keys (128 bytes = 64 queries per half)
       const uint64_t ds_md = make_smem_desc(sbase + C::OFF_DS, C::DS_HALF, 8 * 128, kLayoutSW128);
       auto adv = [](uint64_t desc, uint32_t bytes) { return desc + (uint64_t)(bytes >> 4); };
-      bool ok = mbar_wait(kv_full, 0, wait_ns);
+      bool ok = wait_all(kv_full, 0);
       for (int s = 0; s < n_steps && ok; ++s) {
         const int st = s % ST, u = s / ST;
-        if (*abort_flag || !mbar_wait(&q_full[st], u & 1, wait_ns)) { ok = false; break; }
+        if (__any_sync(0xffffffffu, *abort_flag != 0) || !wait_all(&q_full[st], u & 1)) {
+          ok = false;
+          break;
+        }
         const uint32_t stage = sbase + C::OFF_STAGE + st * C::STAGE_BYTES;
         const uint64_t q_kd = make_smem_desc(stage, 16, 8 * C::SPAN, C::LAYOUT);
         const uint64_t do_kd = make_smem_desc(stage + C::QT_BYTES, 16, 8 * C::SPAN, C::LAYOUT);
@@ -247,40 +270,40 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk * 16) / C::CHUNK) * (C::BN * C::SPAN) + ((kk * 16) % C::CHUNK) * 2;
-          mma_bf16_ss(tmem + C::TM_S, adv(k_kd, off), adv(q_kd, off), I_S, kk > 0 ? 1u : 0u);
+          mma_bf16_ss_elect(tmem + C::TM_S, adv(k_kd, off), adv(q_kd, off), I_S, kk > 0 ? 1u : 0u);
         }
         // dP^T overwrites the previous step's dQ: wait until it has been read.
-        if (s > 0 && !mbar_wait(dq_empty, (s - 1) & 1, wait_ns)) { ok = false; break; }
+        if (s > 0 && !wait_all(dq_empty, (s - 1) & 1)) { ok = false; break; }
         // dP^T = V dO^T
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk * 16) / C::CHUNK) * (C::BN * C::SPAN) + ((kk * 16) % C::CHUNK) * 2;
-          mma_bf16_ss(tmem + C::TM_DP, adv(v_kd, off), adv(do_kd, off), I_S, kk > 0 ? 1u : 0u);
+          mma_bf16_ss_elect(tmem + C::TM_DP, adv(v_kd, off), adv(do_kd, off), I_S, kk > 0 ? 1u : 0u);
         }
-        mma_commit(s_full);
-        if (!mbar_wait(p_full, s & 1, wait_ns)) { ok = false; break; }
+        mma_commit_elect(s_full);
+        if (!wait_all(p_full, s & 1)) { ok = false; break; }
         tc_fence_after();  // P^T and dS^T were written to tensor memory by other threads
         // dV += P^T dO,  dK += dS^T Q   (16 queries = 8 columns of packed bf16)
 #pragma unroll
         for (int kk = 0; kk < C::BM / 16; ++kk)
-          mma_bf16_ts(tmem + C::TM_DV, tmem + C::TM_S + kk * 8, adv(do_md, kk * 16 * C::SPAN),
+          mma_bf16_ts_elect(tmem + C::TM_DV, tmem + C::TM_S + kk * 8, adv(do_md, kk * 16 * C::SPAN),
                       I_ACC, (s > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < C::BM / 16; ++kk)
-          mma_bf16_ts(tmem + C::TM_DK, tmem + C::TM_DP + kk * 8, adv(q_md, kk * 16 * C::SPAN),
+          mma_bf16_ts_elect(tmem + C::TM_DK, tmem + C::TM_DP + kk * 8, adv(q_md, kk * 16 * C::SPAN),
                       I_ACC, (s > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&q_empty[st]);  // Q, dO, L, D of this stage are no longer read
+        mma_commit_elect(&q_empty[st]);  // Q, dO, L, D of this stage are no longer read
         // dQ = dS K   (16 keys per MMA)
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
-          mma_bf16_ss(tmem + C::TM_DQ, adv(ds_md, kk * 16 * 128), adv(k_md, kk * 16 * C::SPAN),
+          mma_bf16_ss_elect(tmem + C::TM_DQ, adv(ds_md, kk * 16 * 128), adv(k_md, kk * 16 * C::SPAN),
                       I_DQ, kk > 0 ? 1u : 0u);
-        mma_commit(dq_full);
+        mma_commit_elect(dq_full);
       }
       if (!ok) fail();
-      mma_commit(dkdv_full);
-      mma_commit(drain);
-      mbar_wait(drain, 0, wait_ns);
+      mma_commit_elect(dkdv_full);
+      mma_commit_elect(drain);
+      wait_all(drain, 0);
     }
     __syncwarp();
   } else if (warp < 4) {
@@ -329,6 +352,12 @@ __global__ void __launch_bounds__(320, 1)
         // scores were loaded in this or an earlier chunk.
         tmem_st16(tmem + lane_base + C::TM_S + c * 16, pw);
         tmem_st16(tmem + lane_base + C::TM_DP + c * 16, dw);
+        // The dS region held the previous step's dQ staging: wait until the
+        // reduction has read it.
+        if (c == 0 && s > 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait(ds_free, (s - 1) & 1, wait_ns));
+          if (!ok) break;
+        }
         // dS^T row into shared memory: queries [32c, 32c+32) are 16-byte
         // units 4(c%2) .. 4(c%2)+3 of half c/2, swizzled by the row.
         uint8_t *half = ds_row + (c >> 1) * C::DS_HALF;
@@ -339,11 +368,13 @@ __global__ void __launch_bounds__(320, 1)
               make_uint4(dw[4 * j], dw[4 * j + 1], dw[4 * j + 2], dw[4 * j + 3]);
         }
       }
+      if (!ok) break;
       tmem_st_wait();
       fence_proxy_async_smem();  // dS in shared memory, for the tensor core
       tc_fence_before();
       mbar_arrive(p_full);
     }
+    tmem_st_wait();  // no store to tensor memory is in flight past this point
     if (!ok) fail();
     // ---- dK (times scale) and dV of this key tile, bf16
     if (n_steps > 0 && ok) {
@@ -392,15 +423,22 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_after();
       const int bh = b * p.Hq + step_head(s);
       const int q0 = step_qt(s) * C::BM;
-#pragma unroll 1
-      for (int c = 0; c < D / 32; ++c, ++n) {
+      // Read the whole row first so that tensor memory is released (and the
+      // next dP^T may start) before the shared-memory staging.
+      float vall[D];
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
         float v[32];
         tmem_ld32_wait(tmem + lane_base + C::TM_DQ + c * 32, v);
-        if (c == D / 32 - 1) {
-          tc_fence_before();
-          mbar_arrive(dq_empty);  // the step's dQ has left tensor memory
-        }
-        uint8_t *buf = smem + C::OFF_DQ + (n & 1) * C::DQ_CHUNK;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) vall[c * 32 + i] = v[i];
+      }
+      tc_fence_before();
+      mbar_arrive(dq_empty);  // the step's dQ has left tensor memory
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c, ++n) {
+        const float *v = vall + c * 32;
+        uint8_t *buf = smem + C::OFF_DS + (n & 1) * C::DQ_CHUNK;
         // the reduce that last read this buffer (two chunks ago) is done
         if (elected && n >= 2) bulk_wait_group_read1();
         named_barrier_sync(1, 128);
@@ -413,6 +451,425 @@ __global__ void __launch_bounds__(320, 1)
         named_barrier_sync(1, 128);
         if (elected) {
           tma_reduce_add_3d(&tm_dq, buf, c * 32, q0, bh);
+          bulk_commit_group();
+        }
+      }
+      // the next step's dS may overwrite the staging once it has been read
+      if (elected) {
+        bulk_wait_group_read0();
+        mbar_arrive(ds_free);
+      }
+    }
+    if (!ok) fail();
+    if (elected) bulk_wait_group0();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// d = 128: steps of 64 queries with S^T and dP^T double-buffered in tensor
+// memory, so the tensor core computes the next step's S^T and dP^T while
+// the P/dS threads work on this step, and three stages of Q and dO.  dQ is
+// computed transposed, dQ^T = K^T dS^T (M = d = 128 lanes, one per head-dim
+// column), over the dP^T columns of its buffer once dK has read dS^T, and is
+// staged in its own shared-memory tile, 32 columns x 2 at a time, for the
+// reduction.
+//
+// Tensor memory: buffer b in {0,1}: S^T_b [128b, 128b+64) with P^T_b over its
+// first 32 columns, dP^T_b [128b+64, 128b+128) with dS^T_b over its first 32
+// and dQ^T_b over all 64; dV [256,384); dK [384,512).
+struct BwdPipeCfg {
+  static constexpr int D = 128;
+  static constexpr int BM = 64;                       // queries per step
+  static constexpr int BN = 128;                      // keys per CTA
+  static constexpr int SPAN = 128;
+  static constexpr int CHUNK = 64;
+  static constexpr int NCHUNK = 2;
+  static constexpr uint32_t KV_BYTES = BN * D * 2;    // 32 KB
+  static constexpr uint32_t QT_BYTES = BM * D * 2;    // 16 KB
+  static constexpr uint32_t VEC_BYTES = BM * 4;       // 256 B
+  static constexpr uint32_t STAGE_BYTES = 2 * QT_BYTES + 1024;
+  static constexpr int STAGES = 3;
+  static constexpr uint32_t OFF_K = 0;
+  static constexpr uint32_t OFF_V = OFF_K + KV_BYTES;
+  static constexpr uint32_t OFF_STAGE = OFF_V + KV_BYTES;
+  static constexpr uint32_t OFF_DS = OFF_STAGE + STAGES * STAGE_BYTES;  // 2 x [128 keys x 128 B]
+  static constexpr uint32_t DS_BYTES = BN * 128;
+  // dQ staged two [64 rows x 32 fp32] chunks at a time
+  static constexpr uint32_t OFF_DQ = OFF_DS + 2 * DS_BYTES;
+  static constexpr uint32_t DQ_CHUNK = BM * 128;
+  static constexpr uint32_t OFF_BAR = OFF_DQ + 2 * DQ_CHUNK;
+  // kv_full, dkdv_full, drain, then per stage q_full, q_empty, then per
+  // buffer s_full, p_full, dq_full, dq_empty, ds_free
+  static constexpr int NBAR = 3 + 2 * STAGES + 5 * 2;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
+  static constexpr uint32_t TMEM_COLS = 512;
+  __host__ __device__ static constexpr uint32_t tm_s(int b) { return 128 * b; }
+  __host__ __device__ static constexpr uint32_t tm_dp(int b) { return 128 * b + 64; }
+  static constexpr uint32_t TM_DV = 256, TM_DK = 384;
+  static constexpr int THREADS = 320;
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert(OFF_STAGE % 1024 == 0 && OFF_DS % 1024 == 0 && OFF_DQ % 1024 == 0, "alignment");
+};
+
+__global__ void __launch_bounds__(320, 1)
+    attn_bwd_pipelined_kernel(const __grid_constant__ CUtensorMap tm_q,
+                              const __grid_constant__ CUtensorMap tm_k,
+                              const __grid_constant__ CUtensorMap tm_v,
+                              const __grid_constant__ CUtensorMap tm_do,
+                              const __grid_constant__ CUtensorMap tm_dq,
+                              const BwdParams p) {
+  using C = BwdPipeCfg;
+  constexpr int D = C::D;
+  constexpr int ST = C::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+  uint64_t *kv_full = bars + 0, *dkdv_full = bars + 1, *drain = bars + 2;
+  uint64_t *q_full = bars + 3, *q_empty = q_full + ST;
+  uint64_t *s_full = q_empty + ST, *p_full = s_full + 2, *dq_full = p_full + 2;
+  uint64_t *dq_empty = dq_full + 2, *ds_free = dq_empty + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint64_t wait_ns = p.wait_ns;
+
+  const int kt = blockIdx.x;
+  const int bkv = blockIdx.y;
+  const int b = bkv / p.Hkv;
+  const int g = bkv - b * p.Hkv;
+  const int delta = p.Tk - p.Tq;
+  const int n_qt = p.Tq_pad / C::BM;  // 64-query tiles
+  const int qt_lo = p.causal ? max(0, kt * C::BN - delta) / C::BM : 0;
+  const int n_q = n_qt - qt_lo;
+  const int n_steps = n_q > 0 ? p.group * n_q : 0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    mbar_init(dkdv_full, 1);
+    mbar_init(drain, 1);
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_empty[s], 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&s_full[x], 1);
+      mbar_init(&p_full[x], 128);
+      mbar_init(&dq_full[x], 1);
+      mbar_init(&dq_empty[x], 128);
+      mbar_init(&ds_free[x], 1);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+    prefetch_tmap(&tm_do);
+    prefetch_tmap(&tm_dq);
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  auto fail = [&]() {
+    atomicExch(p.status, kBwdStatusTimeout);
+    *abort_flag = 1;
+  };
+  auto step_head = [&](int s) { return g * p.group + s / n_q; };
+  auto step_qt = [&](int s) { return qt_lo + s % n_q; };
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      bool ok = true;
+      int last[ST];
+      for (int s = 0; s < ST; ++s) last[s] = -1;
+      mbar_arrive_expect_tx(kv_full, 2 * C::KV_BYTES);
+      for (int c = 0; c < C::NCHUNK; ++c) {
+        tma_load_3d(smem + C::OFF_K + c * (C::BN * C::SPAN), &tm_k, kv_full, c * C::CHUNK,
+                    kt * C::BN, bkv);
+        tma_load_3d(smem + C::OFF_V + c * (C::BN * C::SPAN), &tm_v, kv_full, c * C::CHUNK,
+                    kt * C::BN, bkv);
+      }
+      for (int s = 0; s < n_steps && ok; ++s) {
+        const int st = s % ST, u = s / ST;
+        if (*abort_flag) { ok = false; break; }
+        if (s >= ST && !mbar_wait(&q_empty[st], (u - 1) & 1, wait_ns)) { ok = false; break; }
+        const int bh = b * p.Hq + step_head(s);
+        const int q0 = step_qt(s) * C::BM;
+        uint8_t *stage = smem + C::OFF_STAGE + st * C::STAGE_BYTES;
+        mbar_arrive_expect_tx(&q_full[st], 2 * C::QT_BYTES + 2 * C::VEC_BYTES);
+        for (int c = 0; c < C::NCHUNK; ++c) {
+          tma_load_3d(stage + c * (C::BM * C::SPAN), &tm_q, &q_full[st], c * C::CHUNK, q0, bh);
+          tma_load_3d(stage + C::QT_BYTES + c * (C::BM * C::SPAN), &tm_do, &q_full[st],
+                      c * C::CHUNK, q0, bh);
+        }
+        const size_t voff = (size_t)bh * p.Tq_pad + q0;
+        bulk_load(stage + 2 * C::QT_BYTES, p.l2 + voff, C::VEC_BYTES, &q_full[st]);
+        bulk_load(stage + 2 * C::QT_BYTES + 512, p.dvec + voff, C::VEC_BYTES, &q_full[st]);
+        last[st] = s;
+      }
+      if (!ok) fail();
+      mbar_wait(kv_full, 0, wait_ns);
+      for (int s = 0; s < ST; ++s)
+        if (last[s] >= 0) mbar_wait(&q_full[s], (last[s] / ST) & 1, wait_ns);
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ------------------------------------- MMA issuer (converged, elected lane)
+    {
+      auto wait_all = [&](uint64_t *bar, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity, wait_ns));
+      };
+      constexpr uint32_t I_S = make_idesc_bf16(C::BN, C::BM, false);          // S^T, dP^T
+      constexpr uint32_t I_ACC = make_idesc_bf16(C::BN, D, true);             // dV, dK
+      constexpr uint32_t I_DQ = make_idesc_bf16_ab(D, C::BM, true, true);     // dQ^T
+      const uint64_t k_kd = make_smem_desc(sbase + C::OFF_K, 16, 8 * C::SPAN, kLayoutSW128);
+      const uint64_t v_kd = make_smem_desc(sbase + C::OFF_V, 16, 8 * C::SPAN, kLayoutSW128);
+      // K^T as the MN-major A of dQ^T: M = head dim (next 64 columns at +BN*SPAN)
+      const uint64_t k_md =
+          make_smem_desc(sbase + C::OFF_K, C::BN * C::SPAN, 8 * C::SPAN, kLayoutSW128);
+      auto adv = [](uint64_t desc, uint32_t bytes) { return desc + (uint64_t)(bytes >> 4); };
+      // S^T(s) and dP^T(s) into buffer s & 1
+      auto issue_sdp = [&](int s) {
+        const int x = s & 1;
+        const uint32_t stage = sbase + C::OFF_STAGE + (s % ST) * C::STAGE_BYTES;
+        const uint64_t q_kd = make_smem_desc(stage, 16, 8 * C::SPAN, kLayoutSW128);
+        const uint64_t do_kd = make_smem_desc(stage + C::QT_BYTES, 16, 8 * C::SPAN, kLayoutSW128);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t a_off = ((kk * 16) / C::CHUNK) * (C::BN * C::SPAN) + ((kk * 16) % C::CHUNK) * 2;
+          const uint32_t b_off = ((kk * 16) / C::CHUNK) * (C::BM * C::SPAN) + ((kk * 16) % C::CHUNK) * 2;
+          mma_bf16_ss_elect(tmem + C::tm_s(x), adv(k_kd, a_off), adv(q_kd, b_off), I_S,
+                            kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t a_off = ((kk * 16) / C::CHUNK) * (C::BN * C::SPAN) + ((kk * 16) % C::CHUNK) * 2;
+          const uint32_t b_off = ((kk * 16) / C::CHUNK) * (C::BM * C::SPAN) + ((kk * 16) % C::CHUNK) * 2;
+          mma_bf16_ss_elect(tmem + C::tm_dp(x), adv(v_kd, a_off), adv(do_kd, b_off), I_S,
+                            kk > 0 ? 1u : 0u);
+        }
+        mma_commit_elect(&s_full[x]);
+      };
+      bool ok = wait_all(kv_full, 0);
+      if (ok && n_steps > 0) {
+        ok = wait_all(&q_full[0], 0);
+        if (ok) issue_sdp(0);
+      }
+      for (int s = 0; s < n_steps && ok; ++s) {
+        const int x = s & 1;
+        const int st = s % ST;
+        if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
+        // the next step's S^T and dP^T into the other buffer, once its
+        // previous dQ^T (step s - 1) has been drained
+        if (s + 1 < n_steps) {
+          if (!wait_all(&q_full[(s + 1) % ST], ((s + 1) / ST) & 1)) { ok = false; break; }
+          if (s >= 1 && !wait_all(&dq_empty[x ^ 1], ((s - 1) >> 1) & 1)) { ok = false; break; }
+          issue_sdp(s + 1);
+        }
+        if (!wait_all(&p_full[x], (s >> 1) & 1)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t stage = sbase + C::OFF_STAGE + st * C::STAGE_BYTES;
+        const uint64_t q_md = make_smem_desc(stage, C::BM * C::SPAN, 8 * C::SPAN, kLayoutSW128);
+        const uint64_t do_md =
+            make_smem_desc(stage + C::QT_BYTES, C::BM * C::SPAN, 8 * C::SPAN, kLayoutSW128);
+        // dV += P^T dO, dK += dS^T Q   (16 queries = 8 columns of packed bf16)
+#pragma unroll
+        for (int kk = 0; kk < C::BM / 16; ++kk)
+          mma_bf16_ts_elect(tmem + C::TM_DV, tmem + C::tm_s(x) + kk * 8,
+                            adv(do_md, kk * 16 * C::SPAN), I_ACC, (s > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < C::BM / 16; ++kk)
+          mma_bf16_ts_elect(tmem + C::TM_DK, tmem + C::tm_dp(x) + kk * 8,
+                            adv(q_md, kk * 16 * C::SPAN), I_ACC, (s > 0 || kk > 0) ? 1u : 0u);
+        mma_commit_elect(&q_empty[st]);
+        // dQ^T = K^T dS^T   (16 keys per MMA; B = dS^T rows of 64 queries)
+        const uint64_t ds_md = make_smem_desc(sbase + C::OFF_DS + x * C::DS_BYTES, C::DS_BYTES,
+                                              8 * 128, kLayoutSW128);
+#pragma unroll
+        for (int kk = 0; kk < C::BN / 16; ++kk)
+          mma_bf16_ss_elect(tmem + C::tm_dp(x), adv(k_md, kk * 16 * C::SPAN),
+                            adv(ds_md, kk * 16 * 128), I_DQ, kk > 0 ? 1u : 0u);
+        mma_commit_elect(&dq_full[x]);
+        mma_commit_elect(&ds_free[x]);
+      }
+      if (!ok) fail();
+      mma_commit_elect(dkdv_full);
+      mma_commit_elect(drain);
+      wait_all(drain, 0);
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    // ------------------------------------------- P and dS, one key per thread
+    const int r = threadIdx.x;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const int key = kt * C::BN + r;
+    const bool key_ok = key < p.Tk;
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int s = 0; s < n_steps; ++s) {
+      const int x = s & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[x], (s >> 1) & 1, wait_ns) && !*abort_flag);
+      if (!ok) break;
+      tc_fence_after();
+      const int st = s % ST;
+      const int q0 = step_qt(s) * C::BM;
+      const float4 *l2v = reinterpret_cast<const float4 *>(smem + C::OFF_STAGE +
+                                                           st * C::STAGE_BYTES + 2 * C::QT_BYTES);
+      const float4 *dvv = l2v + 32;  // D values at +512 bytes
+      const bool need_mask = p.causal && (kt * C::BN + C::BN - 1 > q0 + delta);
+      const int lim = key - delta - q0;  // query q (in tile) sees the key iff q >= lim
+      uint8_t *ds_row = smem + C::OFF_DS + x * C::DS_BYTES + r * 128;
+#pragma unroll 1
+      for (int c = 0; c < C::BM / 32; ++c) {
+        float sv[32], dp[32];
+        tmem_ld32_wait(tmem + lane_base + C::tm_s(x) + c * 32, sv);
+        tmem_ld32_wait(tmem + lane_base + C::tm_dp(x) + c * 32, dp);
+        uint32_t pw[16], dw[16];
+#pragma unroll
+        for (int i4 = 0; i4 < 8; ++i4) {
+          const float4 lv = l2v[c * 8 + i4];
+          const float4 dd = dvv[c * 8 + i4];
+          const float la[4] = {lv.x, lv.y, lv.z, lv.w};
+          const float da[4] = {dd.x, dd.y, dd.z, dd.w};
+#pragma unroll
+          for (int e = 0; e < 4; e += 2) {
+            const int i = i4 * 4 + e;
+            const int q = c * 32 + i;
+            float p0 = ex2_approx(fmaf(sv[i], sl2, -la[e]));
+            float p1 = ex2_approx(fmaf(sv[i + 1], sl2, -la[e + 1]));
+            if (need_mask) {
+              if (q < lim) p0 = 0.f;
+              if (q + 1 < lim) p1 = 0.f;
+            }
+            if (!key_ok) p0 = p1 = 0.f;
+            pw[i / 2] = pack_bf16x2(p0, p1);
+            dw[i / 2] = pack_bf16x2(p0 * (dp[i] - da[e]), p1 * (dp[i + 1] - da[e + 1]));
+          }
+        }
+        tmem_st16(tmem + lane_base + C::tm_s(x) + c * 16, pw);
+        tmem_st16(tmem + lane_base + C::tm_dp(x) + c * 16, dw);
+        // dS^T row: queries [32c, 32c+32) are 16-byte units 4c .. 4c+3 of the
+        // 128-byte row, swizzled by the row; the buffer is free once the dQ^T
+        // MMA of step s - 2 has read it.
+        if (c == 0 && s >= 2) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&ds_free[x], ((s - 2) >> 1) & 1, wait_ns));
+          if (!ok) break;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int unit = c * 4 + j;
+          *reinterpret_cast<uint4 *>(ds_row + ((unit ^ (r & 7)) << 4)) =
+              make_uint4(dw[4 * j], dw[4 * j + 1], dw[4 * j + 2], dw[4 * j + 3]);
+        }
+      }
+      if (!ok) break;
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&p_full[x]);
+    }
+    tmem_st_wait();
+    if (!ok) fail();
+    if (n_steps > 0 && ok) {
+      ok = __all_sync(0xffffffffu, mbar_wait(dkdv_full, 0, wait_ns));
+      if (!ok) fail();
+    }
+    if (ok) {
+      tc_fence_after();
+      const size_t row = ((size_t)bkv * p.Tk + key) * D;
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t col = which == 0 ? C::TM_DV : C::TM_DK;
+        const float mul = which == 0 ? 1.f : p.scale;
+        __nv_bfloat16 *dst = (which == 0 ? p.dv : p.dk) + row;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          float v[32];
+          if (n_steps > 0) {
+            tmem_ld32_wait(tmem + lane_base + col + c * 32, v);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0.f;
+          }
+          if (key_ok) {
+            uint4 *o = reinterpret_cast<uint4 *>(dst + c * 32);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              o[u] = make_uint4(pack_bf16x2(v[8 * u] * mul, v[8 * u + 1] * mul),
+                                pack_bf16x2(v[8 * u + 2] * mul, v[8 * u + 3] * mul),
+                                pack_bf16x2(v[8 * u + 4] * mul, v[8 * u + 5] * mul),
+                                pack_bf16x2(v[8 * u + 6] * mul, v[8 * u + 7] * mul));
+          }
+        }
+      }
+    }
+  } else {
+    // --------------------------- dQ^T of each step, one head-dim column per thread
+    const int cdim = threadIdx.x - 128;  // head-dim column == TMEM lane
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const bool elected = (cdim == 0);
+    // column cdim of the staged [64 queries x 32] fp32 chunk cdim / 32 (two
+    // chunks per round, in buffers (cdim / 32) % 2): 16-byte unit
+    // (cdim % 32) / 4 of each 128-byte row, swizzled by the row
+    uint8_t *stage_col = smem + C::OFF_DQ + ((cdim >> 5) & 1) * C::DQ_CHUNK + (cdim & 3) * 4;
+    const int unit = (cdim & 31) >> 2;
+    const int round_of_col = cdim >> 6;  // chunks 0-1 in round 0, 2-3 in round 1
+    bool ok = true;
+    for (int s = 0; s < n_steps; ++s) {
+      const int x = s & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(&dq_full[x], (s >> 1) & 1, wait_ns) && !*abort_flag);
+      if (!ok) break;
+      tc_fence_after();
+      float v[64];
+      {
+        float a[32], bb[32];
+        tmem_ld32_wait(tmem + lane_base + C::tm_dp(x), a);
+        tmem_ld32_wait(tmem + lane_base + C::tm_dp(x) + 32, bb);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          v[i] = a[i];
+          v[32 + i] = bb[i];
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&dq_empty[x]);  // the step's dQ^T has left tensor memory
+      const int bh = b * p.Hq + step_head(s);
+      const int q0 = step_qt(s) * C::BM;
+#pragma unroll 1
+      for (int round = 0; round < 2; ++round) {
+        // the reductions issued last round have read the staging buffers
+        if (elected && (s > 0 || round > 0)) bulk_wait_group_read0();
+        named_barrier_sync(1, 128);
+        if (round_of_col == round) {
+#pragma unroll
+          for (int q = 0; q < C::BM; ++q)
+            *reinterpret_cast<float *>(stage_col + q * 128 + ((unit ^ (q & 7)) << 4)) = v[q];
+          fence_proxy_async_smem();
+        }
+        named_barrier_sync(1, 128);
+        if (elected) {
+#pragma unroll
+          for (int k2 = 0; k2 < 2; ++k2)
+            tma_reduce_add_3d(&tm_dq, smem + C::OFF_DQ + k2 * C::DQ_CHUNK, (round * 2 + k2) * 32,
+                              q0, bh);
           bulk_commit_group();
         }
       }
