@@ -393,17 +393,7 @@ def run_ours(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {
-            "workload": f"{PREFILL.name} + {DECODE.name}",
-            "prefill": {"B": PREFILL.B, "Hq": PREFILL.Hq, "Hkv": PREFILL.Hkv, "Tq": PREFILL.Tq,
-                        "Tk": PREFILL.Tk, "d": PREFILL.d, "causal": PREFILL.causal,
-                        "dist": PREFILL.dist, "seed": PREFILL.seed},
-            "decode": {"B": DECODE.B, "Hq": DECODE.Hq, "Hkv": DECODE.Hkv, "Tq": 1,
-                       "Tk": DECODE.Tk, "d": DECODE.d, "causal": False,
-                       "dist": DECODE.dist, "seed": DECODE.seed},
-            "l2": "no flush: inputs exceed the 129 MB L2 (prefill q+k+v 403 MB, decode cache 2.1 GB)",
-            "parallelism": f"replicas x{world} (each rank runs the full workload)",
-        },
+        "config": workload_config(world),
         "prefill_ms": round(pre_s * 1e3 / K, 4),
         "roofline": {
             "kernel": "prefill_fwd_kernel<128>",
@@ -515,6 +505,22 @@ def _reference_rows(n, T, heads, offset):
     return np.zeros(n, np.int32), (idx // T).astype(np.int32), (idx % T).astype(np.int32)
 
 
+def workload_config(world):
+    """The workload both arms report (the reference arm times a bounded
+    sample of it, described in its cpu_baseline)."""
+    return {
+        "workload": f"{PREFILL.name} + {DECODE.name}",
+        "prefill": {"B": PREFILL.B, "Hq": PREFILL.Hq, "Hkv": PREFILL.Hkv, "Tq": PREFILL.Tq,
+                    "Tk": PREFILL.Tk, "d": PREFILL.d, "causal": PREFILL.causal,
+                    "dist": PREFILL.dist, "seed": PREFILL.seed},
+        "decode": {"B": DECODE.B, "Hq": DECODE.Hq, "Hkv": DECODE.Hkv, "Tq": 1,
+                   "Tk": DECODE.Tk, "d": DECODE.d, "causal": False,
+                   "dist": DECODE.dist, "seed": DECODE.seed},
+        "l2": "no flush: inputs exceed the 129 MB L2 (prefill q+k+v 403 MB, decode cache 2.1 GB)",
+        "parallelism": f"replicas x{world} (each rank runs the full workload)",
+    }
+
+
 def run_reference(args, rank, world):
     """Time the fp64 oracle (the only reference for this path) on the host
     cores: each step evaluates a bounded, evenly spread sample of rows of the
@@ -561,7 +567,7 @@ def run_reference(args, rank, world):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": f"{PREFILL.name} (sampled rows)"},
+        "config": workload_config(world),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": omp_threads(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
