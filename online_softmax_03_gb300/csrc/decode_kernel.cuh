@@ -70,7 +70,7 @@ struct DecodeCfg {
   static constexpr int CW = 4;                  // consumer warps
   static constexpr int THREADS = (CW + 1) * 32;
   static constexpr int TILE = 32;               // keys per stage
-  static constexpr int STAGES = 4;
+  static constexpr int STAGES = 3;   // 48 KB of ring: four CTAs per SM
   static constexpr int KG = 32 / GP;            // keys per reduce-scatter
   static constexpr int NGRP = TILE / KG;
   static constexpr int VEC = D / 32;            // head-dim columns per lane
