@@ -18,6 +18,8 @@ int launch_bwd(const attn_host::BwdArgs &a, unsigned int *status) {
   float *dq_acc = static_cast<float *>(a.workspace);
   float *l2 = dq_acc + bhq * (uint64_t)a.Tq * D;
   float *dvec = l2 + bhq * (uint64_t)Tq_pad;
+  // per 64-query tile, 16 bf16 per row (the d = 128 kernel's aux operand)
+  uint8_t *aux = reinterpret_cast<uint8_t *>(dvec + bhq * (uint64_t)Tq_pad);
   CUtensorMap tq, tk, tv, tdo, tdq;
   if (!attn_host::encode_tmap_3d_bf16(&tq, a.q, D, a.Tq, bhq, C::CHUNK, C::BM, 1, C::SPAN) ||
       !attn_host::encode_tmap_3d_bf16(&tdo, a.dout, D, a.Tq, bhq, C::CHUNK, C::BM, 1, C::SPAN) ||
@@ -33,7 +35,8 @@ int launch_bwd(const attn_host::BwdArgs &a, unsigned int *status) {
     if (blocks > 0x7fffffffull) return ATTN_ERR_INVALID_ARG;
     attn_dev::attn_bwd_prep_kernel<D><<<(unsigned)blocks, 256, 0, a.stream>>>(
         static_cast<const __nv_bfloat16 *>(a.o), static_cast<const __nv_bfloat16 *>(a.dout),
-        a.lse, dq_acc, l2, dvec, (int)bhq, a.Tq, Tq_pad);
+        a.lse, dq_acc, l2, dvec, D == 128 ? aux : nullptr, 1.f / a.scale, (int)bhq, a.Tq,
+        Tq_pad);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   }
   // 2. dK, dV per key tile; dQ accumulated
@@ -52,6 +55,7 @@ int launch_bwd(const attn_host::BwdArgs &a, unsigned int *status) {
   p.dv = static_cast<__nv_bfloat16 *>(a.dv);
   p.l2 = l2;
   p.dvec = dvec;
+  p.aux = aux;
   p.status = status;
   p.Hq = a.Hq;
   p.Hkv = a.Hkv;
@@ -87,7 +91,8 @@ namespace attn_host {
 size_t bwd_workspace_bytes_for(int B, int Hq, int Tq, int d) {
   const size_t tq_pad = ((size_t)Tq + 127) / 128 * 128;
   const size_t rows = (size_t)B * Hq;
-  return (rows * (size_t)Tq * d + 2 * rows * tq_pad) * sizeof(float);
+  // dQ accumulator, L and D per padded row, and 32 bytes of aux per padded row
+  return (rows * (size_t)Tq * d + 2 * rows * tq_pad) * sizeof(float) + rows * tq_pad * 32;
 }
 
 int bwd_launch(const BwdArgs &a) {

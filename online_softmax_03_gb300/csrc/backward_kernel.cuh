@@ -64,6 +64,9 @@ struct BwdParams {
   __nv_bfloat16 *dk, *dv;  // [B, Hkv, Tk, D]
   const float *l2;         // [B*Hq, Tq_pad]: LSE * log2(e); +inf on padding rows
   const float *dvec;       // [B*Hq, Tq_pad]: rowsum(dO o O); 0 on padding rows
+  // d = 128 kernel: per 64-query tile a 2 KB block of 16 bf16 per row,
+  // [-L/scale (hi, lo), -D (hi, lo), 0 x 12], in 8 x 16-byte core matrices
+  const uint8_t *aux;
   unsigned int *status;
   int Hq, Hkv, group;
   int Tq, Tk, Tq_pad;
@@ -493,8 +496,8 @@ struct BwdPipeCfg {
   static constexpr int NCHUNK = 2;
   static constexpr uint32_t KV_BYTES = BN * D * 2;    // 32 KB
   static constexpr uint32_t QT_BYTES = BM * D * 2;    // 16 KB
-  static constexpr uint32_t VEC_BYTES = BM * 4;       // 256 B
-  static constexpr uint32_t STAGE_BYTES = 2 * QT_BYTES + 1024;
+  static constexpr uint32_t AUX_BYTES = BM * 32;      // 2 KB: 16 bf16 per query
+  static constexpr uint32_t STAGE_BYTES = 2 * QT_BYTES + AUX_BYTES;  // Q | dO | aux
   static constexpr int STAGES = 3;
   static constexpr uint32_t OFF_K = 0;
   static constexpr uint32_t OFF_V = OFF_K + KV_BYTES;
@@ -504,7 +507,10 @@ struct BwdPipeCfg {
   // dQ staged two [64 rows x 32 fp32] chunks at a time
   static constexpr uint32_t OFF_DQ = OFF_DS + 2 * DS_BYTES;
   static constexpr uint32_t DQ_CHUNK = BM * 128;
-  static constexpr uint32_t OFF_BAR = OFF_DQ + 2 * DQ_CHUNK;
+  // constant key-side aux operands: [1, 1, 0, ...] (S^T) and [0, 0, 1, 1, 0, ...] (dP^T)
+  static constexpr uint32_t OFF_KAUX = OFF_DQ + 2 * DQ_CHUNK;
+  static constexpr uint32_t OFF_VAUX = OFF_KAUX + BN * 32;
+  static constexpr uint32_t OFF_BAR = OFF_VAUX + BN * 32;
   // kv_full, dkdv_full, drain, then per stage q_full, q_empty, then per
   // buffer s_full, p_full, dq_full, dq_empty, ds_free
   static constexpr int NBAR = 3 + 2 * STAGES + 5 * 2;
@@ -578,6 +584,18 @@ __global__ void __launch_bounds__(320, 1)
     prefetch_tmap(&tm_do);
     prefetch_tmap(&tm_dq);
   }
+  if (threadIdx.x < C::BN) {
+    // row r of the key-side aux operands, in 8-row x 16-byte core matrices
+    // (core matrix (r / 8, k-half) at (r / 8) * 256 + k-half * 128, row r % 8
+    // at + (r % 8) * 16); bf16 1.0 is 0x3f80
+    const int r = threadIdx.x;
+    const uint32_t off = (r >> 3) * 256 + (r & 7) * 16;
+    *reinterpret_cast<uint4 *>(smem + C::OFF_KAUX + off) = make_uint4(0x3f803f80u, 0u, 0u, 0u);
+    *reinterpret_cast<uint4 *>(smem + C::OFF_KAUX + off + 128) = make_uint4(0u, 0u, 0u, 0u);
+    *reinterpret_cast<uint4 *>(smem + C::OFF_VAUX + off) = make_uint4(0u, 0x3f803f80u, 0u, 0u);
+    *reinterpret_cast<uint4 *>(smem + C::OFF_VAUX + off + 128) = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+  }
   if (warp == 0) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);
     tmem_relinquish();
@@ -614,15 +632,14 @@ __global__ void __launch_bounds__(320, 1)
         const int bh = b * p.Hq + step_head(s);
         const int q0 = step_qt(s) * C::BM;
         uint8_t *stage = smem + C::OFF_STAGE + st * C::STAGE_BYTES;
-        mbar_arrive_expect_tx(&q_full[st], 2 * C::QT_BYTES + 2 * C::VEC_BYTES);
+        mbar_arrive_expect_tx(&q_full[st], 2 * C::QT_BYTES + C::AUX_BYTES);
         for (int c = 0; c < C::NCHUNK; ++c) {
           tma_load_3d(stage + c * (C::BM * C::SPAN), &tm_q, &q_full[st], c * C::CHUNK, q0, bh);
           tma_load_3d(stage + C::QT_BYTES + c * (C::BM * C::SPAN), &tm_do, &q_full[st],
                       c * C::CHUNK, q0, bh);
         }
-        const size_t voff = (size_t)bh * p.Tq_pad + q0;
-        bulk_load(stage + 2 * C::QT_BYTES, p.l2 + voff, C::VEC_BYTES, &q_full[st]);
-        bulk_load(stage + 2 * C::QT_BYTES + 512, p.dvec + voff, C::VEC_BYTES, &q_full[st]);
+        const size_t aoff = ((size_t)bh * (p.Tq_pad / C::BM) + q0 / C::BM) * C::AUX_BYTES;
+        bulk_load(stage + 2 * C::QT_BYTES, p.aux + aoff, C::AUX_BYTES, &q_full[st]);
         last[st] = s;
       }
       if (!ok) fail();
@@ -646,12 +663,16 @@ __global__ void __launch_bounds__(320, 1)
       const uint64_t k_md =
           make_smem_desc(sbase + C::OFF_K, C::BN * C::SPAN, 8 * C::SPAN, kLayoutSW128);
       auto adv = [](uint64_t desc, uint32_t bytes) { return desc + (uint64_t)(bytes >> 4); };
+      // aux K-step: S^T gains -L/scale per query column, dP^T gains -D
+      const uint64_t kaux_d = make_smem_desc(sbase + C::OFF_KAUX, 128, 256, kLayoutNone);
+      const uint64_t vaux_d = make_smem_desc(sbase + C::OFF_VAUX, 128, 256, kLayoutNone);
       // S^T(s) and dP^T(s) into buffer s & 1
       auto issue_sdp = [&](int s) {
         const int x = s & 1;
         const uint32_t stage = sbase + C::OFF_STAGE + (s % ST) * C::STAGE_BYTES;
         const uint64_t q_kd = make_smem_desc(stage, 16, 8 * C::SPAN, kLayoutSW128);
         const uint64_t do_kd = make_smem_desc(stage + C::QT_BYTES, 16, 8 * C::SPAN, kLayoutSW128);
+        const uint64_t qaux_d = make_smem_desc(stage + 2 * C::QT_BYTES, 128, 256, kLayoutNone);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t a_off = ((kk * 16) / C::CHUNK) * (C::BN * C::SPAN) + ((kk * 16) % C::CHUNK) * 2;
@@ -659,6 +680,7 @@ __global__ void __launch_bounds__(320, 1)
           mma_bf16_ss_elect(tmem + C::tm_s(x), adv(k_kd, a_off), adv(q_kd, b_off), I_S,
                             kk > 0 ? 1u : 0u);
         }
+        mma_bf16_ss_elect(tmem + C::tm_s(x), kaux_d, qaux_d, I_S, 1u);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t a_off = ((kk * 16) / C::CHUNK) * (C::BN * C::SPAN) + ((kk * 16) % C::CHUNK) * 2;
@@ -666,6 +688,7 @@ __global__ void __launch_bounds__(320, 1)
           mma_bf16_ss_elect(tmem + C::tm_dp(x), adv(v_kd, a_off), adv(do_kd, b_off), I_S,
                             kk > 0 ? 1u : 0u);
         }
+        mma_bf16_ss_elect(tmem + C::tm_dp(x), vaux_d, qaux_d, I_S, 1u);
         mma_commit_elect(&s_full[x]);
       };
       bool ok = wait_all(kv_full, 0);
@@ -729,11 +752,7 @@ __global__ void __launch_bounds__(320, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(&s_full[x], (s >> 1) & 1, wait_ns) && !*abort_flag);
       if (!ok) break;
       tc_fence_after();
-      const int st = s % ST;
       const int q0 = step_qt(s) * C::BM;
-      const float4 *l2v = reinterpret_cast<const float4 *>(smem + C::OFF_STAGE +
-                                                           st * C::STAGE_BYTES + 2 * C::QT_BYTES);
-      const float4 *dvv = l2v + 32;  // D values at +512 bytes
       const bool need_mask = p.causal && (kt * C::BN + C::BN - 1 > q0 + delta);
       const int lim = key - delta - q0;  // query q (in tile) sees the key iff q >= lim
       uint8_t *ds_row = smem + C::OFF_DS + x * C::DS_BYTES + r * 128;
@@ -743,26 +762,21 @@ __global__ void __launch_bounds__(320, 1)
         tmem_ld32_wait(tmem + lane_base + C::tm_s(x) + c * 32, sv);
         tmem_ld32_wait(tmem + lane_base + C::tm_dp(x) + c * 32, dp);
         uint32_t pw[16], dw[16];
+        // S^T already holds S - L/scale and dP^T holds dP - D (the aux K-step)
 #pragma unroll
-        for (int i4 = 0; i4 < 8; ++i4) {
-          const float4 lv = l2v[c * 8 + i4];
-          const float4 dd = dvv[c * 8 + i4];
-          const float la[4] = {lv.x, lv.y, lv.z, lv.w};
-          const float da[4] = {dd.x, dd.y, dd.z, dd.w};
-#pragma unroll
-          for (int e = 0; e < 4; e += 2) {
-            const int i = i4 * 4 + e;
-            const int q = c * 32 + i;
-            float p0 = ex2_approx(fmaf(sv[i], sl2, -la[e]));
-            float p1 = ex2_approx(fmaf(sv[i + 1], sl2, -la[e + 1]));
-            if (need_mask) {
-              if (q < lim) p0 = 0.f;
-              if (q + 1 < lim) p1 = 0.f;
-            }
-            if (!key_ok) p0 = p1 = 0.f;
-            pw[i / 2] = pack_bf16x2(p0, p1);
-            dw[i / 2] = pack_bf16x2(p0 * (dp[i] - da[e]), p1 * (dp[i + 1] - da[e + 1]));
+        for (int i = 0; i < 32; i += 2) {
+          const int q = c * 32 + i;
+          const float2 x = __fmul2_rn(make_float2(sv[i], sv[i + 1]), make_float2(sl2, sl2));
+          float p0 = ex2_approx(x.x);
+          float p1 = ex2_approx(x.y);
+          if (need_mask) {
+            if (q < lim) p0 = 0.f;
+            if (q + 1 < lim) p1 = 0.f;
           }
+          if (!key_ok) p0 = p1 = 0.f;
+          const float2 d = __fmul2_rn(make_float2(p0, p1), make_float2(dp[i], dp[i + 1]));
+          pw[i / 2] = pack_bf16x2(p0, p1);
+          dw[i / 2] = pack_bf16x2(d.x, d.y);
         }
         tmem_st16(tmem + lane_base + C::tm_s(x) + c * 16, pw);
         tmem_st16(tmem + lane_base + C::tm_dp(x) + c * 16, dw);
@@ -894,18 +908,35 @@ __global__ void __launch_bounds__(256)
     attn_bwd_prep_kernel(const __nv_bfloat16 *__restrict__ o,
                          const __nv_bfloat16 *__restrict__ dout,
                          const float *__restrict__ lse, float *__restrict__ dq_acc,
-                         float *__restrict__ l2, float *__restrict__ dvec, int rows_bh,
-                         int Tq, int Tq_pad) {
+                         float *__restrict__ l2, float *__restrict__ dvec,
+                         uint8_t *__restrict__ aux, float inv_scale, int rows_bh, int Tq,
+                         int Tq_pad) {
   constexpr int VEC = D / 32;
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= rows_bh * Tq_pad) return;
   const int bh = warp / Tq_pad;
   const int i = warp - bh * Tq_pad;
+  // aux row i of its 64-row block: core matrix (r / 8, k-half 0) holds
+  // [-L/scale hi, lo, -D hi, lo, 0 x 4]; k-half 1 is zero
+  auto write_aux = [&](float a, float dd) {
+    if (!aux) return;
+    const int r = i & 63;
+    uint8_t *blk = aux + ((size_t)bh * (Tq_pad / 64) + i / 64) * 2048 + (r >> 3) * 256 + (r & 7) * 16;
+    const __nv_bfloat16 ah = __float2bfloat16_rn(a);
+    const __nv_bfloat16 al = __float2bfloat16_rn(a - __bfloat162float(ah));
+    const __nv_bfloat16 dh = __float2bfloat16_rn(dd);
+    const __nv_bfloat16 dl = __float2bfloat16_rn(dd - __bfloat162float(dh));
+    const uint32_t w0 = (uint32_t)__bfloat16_as_ushort(ah) | ((uint32_t)__bfloat16_as_ushort(al) << 16);
+    const uint32_t w1 = (uint32_t)__bfloat16_as_ushort(dh) | ((uint32_t)__bfloat16_as_ushort(dl) << 16);
+    *reinterpret_cast<uint4 *>(blk) = make_uint4(w0, w1, 0u, 0u);
+    *reinterpret_cast<uint4 *>(blk + 128) = make_uint4(0u, 0u, 0u, 0u);
+  };
   if (i >= Tq) {
     if (lane == 0) {
       l2[warp] = INFINITY;
       dvec[warp] = 0.f;
+      write_aux(-1e30f, 0.f);  // a probability of exactly 0, and finite products
     }
     return;
   }
@@ -924,6 +955,7 @@ __global__ void __launch_bounds__(256)
   if (lane == 0) {
     l2[warp] = lse[row] * 1.4426950408889634f;
     dvec[warp] = acc;
+    write_aux(-lse[row] * inv_scale, -acc);
   }
 }
 

@@ -385,7 +385,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 // ------------------------------------------------- UMMA operand descriptors
 
-// Swizzle modes as encoded in the shared-memory matrix descriptor.
+// Swizzle modes as encoded in the shared-memory matrix descriptor.  Without
+// swizzling a K-major operand is made of 8-row x 16-byte core matrices: LBO
+// is the byte distance between core matrices adjacent along K, SBO between
+// core matrices adjacent along M or N.
+constexpr uint32_t kLayoutNone = 0;
 constexpr uint32_t kLayoutSW128 = 2;
 constexpr uint32_t kLayoutSW64 = 4;
 
