@@ -263,7 +263,8 @@ int attn_decode_paged(const void *q, const void *k_pages, const void *v_pages,
  * attn_bwd_workspace_bytes -- scratch needed by attn_bwd.
  *
  * B*Hq*Tq*d fp32 for the dQ accumulator plus, per query row padded to a
- * multiple of 128, two fp32 values and 32 bytes of derived operands.
+ * multiple of 128, 32 bytes of derived operands (the row's LSE and
+ * D = dout . o).
  * Depends only on the sizes; returns 0 for invalid sizes.
  */
 size_t attn_bwd_workspace_bytes(int B, int Hq, int Tq, int d);

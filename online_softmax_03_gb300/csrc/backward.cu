@@ -8,18 +8,11 @@
 namespace {
 __device__ unsigned int g_bwd_status;
 
-template <int D>
-int launch_bwd(const attn_host::BwdArgs &a, unsigned int *status) {
-  using C = attn_dev::BwdCfg<D>;
-  const int Tq_pad = (a.Tq + C::BM - 1) / C::BM * C::BM;
-  const uint64_t bhq = (uint64_t)a.B * a.Hq, bhk = (uint64_t)a.B * a.Hkv;
-  const int n_kt = (a.Tk + C::BN - 1) / C::BN;
-  if (bhk > 65535) return ATTN_ERR_INVALID_ARG;
-  float *dq_acc = static_cast<float *>(a.workspace);
-  float *l2 = dq_acc + bhq * (uint64_t)a.Tq * D;
-  float *dvec = l2 + bhq * (uint64_t)Tq_pad;
-  // per 64-query tile, 16 bf16 per row (the d = 128 kernel's aux operand)
-  uint8_t *aux = reinterpret_cast<uint8_t *>(dvec + bhq * (uint64_t)Tq_pad);
+// The kernel for head dim D: 64-query steps with double-buffered S^T/dP^T at
+// d = 128, 128-query steps otherwise.
+template <int D, typename C, typename Kern>
+int launch_main(const attn_host::BwdArgs &a, Kern kern, const attn_dev::BwdParams &p,
+                float *dq_acc, uint64_t bhq, uint64_t bhk) {
   CUtensorMap tq, tk, tv, tdo, tdq;
   if (!attn_host::encode_tmap_3d_bf16(&tq, a.q, D, a.Tq, bhq, C::CHUNK, C::BM, 1, C::SPAN) ||
       !attn_host::encode_tmap_3d_bf16(&tdo, a.dout, D, a.Tq, bhq, C::CHUNK, C::BM, 1, C::SPAN) ||
@@ -27,34 +20,40 @@ int launch_bwd(const attn_host::BwdArgs &a, unsigned int *status) {
       !attn_host::encode_tmap_3d_bf16(&tv, a.v, D, a.Tk, bhk, C::CHUNK, C::BN, 1, C::SPAN) ||
       !attn_host::encode_tmap_3d_f32(&tdq, dq_acc, D, a.Tq, bhq, 32, C::BM, 1))
     return ATTN_ERR_CUDA;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)C::SMEM_BYTES) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  const int n_kt = (a.Tk + C::BN - 1) / C::BN;
+  kern<<<dim3(n_kt, (unsigned)bhk), C::THREADS, C::SMEM_BYTES, a.stream>>>(tq, tk, tv, tdo, tdq,
+                                                                          p);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
 
-  // 1. D = rowsum(dO o O), L * log2(e), zero the dQ accumulator
+template <int D>
+int launch_bwd(const attn_host::BwdArgs &a, unsigned int *status) {
+  constexpr int kRowPad = 128;  // query rows are padded to whole 128-row tiles
+  const int Tq_pad = (a.Tq + kRowPad - 1) / kRowPad * kRowPad;
+  const uint64_t bhq = (uint64_t)a.B * a.Hq, bhk = (uint64_t)a.B * a.Hkv;
+  if (bhk > 65535) return ATTN_ERR_INVALID_ARG;
+  float *dq_acc = static_cast<float *>(a.workspace);
+  // per 64-query block, 16 bf16 per row: the aux operand that folds L and D
+  // into S^T and dP^T
+  uint8_t *aux = reinterpret_cast<uint8_t *>(dq_acc + bhq * (uint64_t)a.Tq * D);
+
+  // 1. the aux rows (L and D = rowsum(dO o O)); zero the dQ accumulator
   {
     const uint64_t warps = bhq * (uint64_t)Tq_pad;
     const uint64_t blocks = (warps * 32 + 255) / 256;
     if (blocks > 0x7fffffffull) return ATTN_ERR_INVALID_ARG;
     attn_dev::attn_bwd_prep_kernel<D><<<(unsigned)blocks, 256, 0, a.stream>>>(
         static_cast<const __nv_bfloat16 *>(a.o), static_cast<const __nv_bfloat16 *>(a.dout),
-        a.lse, dq_acc, l2, dvec, D == 128 ? aux : nullptr, 1.f / a.scale, (int)bhq, a.Tq,
-        Tq_pad);
+        a.lse, dq_acc, aux, 1.f / a.scale, (int)bhq, a.Tq, Tq_pad);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   }
   // 2. dK, dV per key tile; dQ accumulated
   attn_dev::BwdParams p{};
-  constexpr bool kPipelined = (D == 128);
-  if (kPipelined) {
-    // 64-query steps: Q/dO boxes of 64 rows, dQ staged 64 rows at a time
-    using P = attn_dev::BwdPipeCfg;
-    if (!attn_host::encode_tmap_3d_bf16(&tq, a.q, D, a.Tq, bhq, P::CHUNK, P::BM, 1, P::SPAN) ||
-        !attn_host::encode_tmap_3d_bf16(&tdo, a.dout, D, a.Tq, bhq, P::CHUNK, P::BM, 1,
-                                        P::SPAN) ||
-        !attn_host::encode_tmap_3d_f32(&tdq, dq_acc, D, a.Tq, bhq, 32, P::BM, 1))
-      return ATTN_ERR_CUDA;
-  }
   p.dk = static_cast<__nv_bfloat16 *>(a.dk);
   p.dv = static_cast<__nv_bfloat16 *>(a.dv);
-  p.l2 = l2;
-  p.dvec = dvec;
   p.aux = aux;
   p.status = status;
   p.Hq = a.Hq;
@@ -63,18 +62,19 @@ int launch_bwd(const attn_host::BwdArgs &a, unsigned int *status) {
   p.Tq = a.Tq;
   p.Tk = a.Tk;
   p.Tq_pad = Tq_pad;
-  p.n_qt = Tq_pad / C::BM;
+  p.n_qt = Tq_pad / 128;
   p.causal = a.causal;
   p.scale = a.scale;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.wait_ns = a.wait_ns;
-  auto kern = kPipelined ? attn_dev::attn_bwd_pipelined_kernel : attn_dev::attn_bwd_kernel<D>;
-  const uint32_t smem = kPipelined ? attn_dev::BwdPipeCfg::SMEM_BYTES : C::SMEM_BYTES;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-      cudaSuccess)
-    return ATTN_ERR_CUDA;
-  kern<<<dim3(n_kt, (unsigned)bhk), C::THREADS, smem, a.stream>>>(tq, tk, tv, tdo, tdq, p);
-  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+  int rc;
+  if constexpr (D == 128)
+    rc = launch_main<D, attn_dev::BwdPipeCfg>(a, attn_dev::attn_bwd_pipelined_kernel, p, dq_acc,
+                                              bhq, bhk);
+  else
+    rc = launch_main<D, attn_dev::BwdCfg<D>>(a, attn_dev::attn_bwd_kernel<D>, p, dq_acc, bhq,
+                                             bhk);
+  if (rc != ATTN_OK) return rc;
   // 3. dQ = scale * accumulator in bf16
   {
     const size_t n4 = bhq * (size_t)a.Tq * D / 4;
@@ -91,8 +91,8 @@ namespace attn_host {
 size_t bwd_workspace_bytes_for(int B, int Hq, int Tq, int d) {
   const size_t tq_pad = ((size_t)Tq + 127) / 128 * 128;
   const size_t rows = (size_t)B * Hq;
-  // dQ accumulator, L and D per padded row, and 32 bytes of aux per padded row
-  return (rows * (size_t)Tq * d + 2 * rows * tq_pad) * sizeof(float) + rows * tq_pad * 32;
+  // fp32 dQ accumulator, then 32 bytes of aux operand per padded query row
+  return rows * (size_t)Tq * d * sizeof(float) + rows * tq_pad * 32;
 }
 
 int bwd_launch(const BwdArgs &a) {

@@ -18,7 +18,7 @@
 // queries:
 //
 //   warp 8     producer: K and V of the key tile once, then per step the Q
-//              and dO tiles (TMA) and the step's L and D values (bulk copy).
+//              and dO tiles (TMA) and the step's aux rows (bulk copy).
 //   warp 9     MMA issuer (converged warp, one elected lane issues), tcgen05.mma
 //              kind::f16, fp32 accumulate:
 //                S^T  = K Q^T     (A = K, B = Q, both from shared memory)
@@ -26,7 +26,7 @@
 //                dV  += P^T dO    (A = P^T from tensor memory, B = dO)
 //                dK  += dS^T Q    (A = dS^T from tensor memory, B = Q)
 //                dQ   = dS K      (A = dS from shared memory, B = K)
-//   warps 0-3  one thread per key (TMEM lane): P^T = e^(S^T scale - L) with
+//   warps 0-3  one thread per key (TMEM lane): P^T = e^(scale (S^T - L/scale)) with
 //              the causal mask, dS^T = P^T o (dP^T - D), written as bf16 into
 //              tensor memory (for dV and dK) and into shared memory (for dQ);
 //              at the end dK (times scale) and dV are stored as bf16.
@@ -36,7 +36,13 @@
 //              accumulated with atomics"; the order of the additions, and so
 //              the last bits of dQ, vary from run to run).
 //
-// Shared memory: K and V of the tile, two stages of (Q, dO, L, D), and the
+// The row statistics enter through the products: one more K-step multiplies
+// a constant key-side operand ([1, 1, 0, ...] for S^T, [0, 0, 1, 1, 0, ...]
+// for dP^T) by per-query aux rows [-L/scale, -D] (each split into a bf16
+// high and low part), so S^T arrives as S - L/scale and dP^T as dP - D and
+// the P/dS threads read no per-query values.
+//
+// Shared memory: K and V of the tile, two stages of (Q, dO, aux), and the
 // dS tile, which also stages dQ for the reduction once the dQ MMA has read
 // dS (the next step's dS waits for that reduction to have read it).
 //
@@ -62,10 +68,9 @@ constexpr unsigned int kBwdStatusMisaligned = 3;  // ATTN_ERR_MISALIGNED
 
 struct BwdParams {
   __nv_bfloat16 *dk, *dv;  // [B, Hkv, Tk, D]
-  const float *l2;         // [B*Hq, Tq_pad]: LSE * log2(e); +inf on padding rows
-  const float *dvec;       // [B*Hq, Tq_pad]: rowsum(dO o O); 0 on padding rows
-  // d = 128 kernel: per 64-query tile a 2 KB block of 16 bf16 per row,
-  // [-L/scale (hi, lo), -D (hi, lo), 0 x 12], in 8 x 16-byte core matrices
+  // per 64-query block of a (batch, head), 2 KB: 16 bf16 per query row,
+  // [-L/scale (hi, lo), -D (hi, lo), 0 x 12] with D = rowsum(dO o O), laid out
+  // as 8-row x 16-byte core matrices; padding rows carry -1e30 and 0
   const uint8_t *aux;
   unsigned int *status;
   int Hq, Hkv, group;
@@ -87,8 +92,8 @@ struct BwdCfg {
   static constexpr int STAGES = 2;
   static constexpr uint32_t KV_BYTES = BN * D * 2;
   static constexpr uint32_t QT_BYTES = BM * D * 2;
-  static constexpr uint32_t VEC_BYTES = BM * 4;
-  static constexpr uint32_t STAGE_BYTES = 2 * QT_BYTES + 1024;  // Q | dO | L | D (+pad)
+  static constexpr uint32_t AUX_BYTES = BM * 32;  // 16 bf16 per query (see BwdParams::aux)
+  static constexpr uint32_t STAGE_BYTES = 2 * QT_BYTES + AUX_BYTES;  // Q | dO | aux
   static constexpr uint32_t OFF_K = 0;
   static constexpr uint32_t OFF_V = OFF_K + KV_BYTES;
   static constexpr uint32_t OFF_STAGE = OFF_V + KV_BYTES;
@@ -98,7 +103,10 @@ struct BwdCfg {
   // in the dS region once the step's dQ MMA has read dS.
   static constexpr uint32_t DQ_CHUNK = BM * 128;
   static_assert(2 * DQ_CHUNK <= 2 * DS_HALF, "dQ staging fits the dS region");
-  static constexpr uint32_t OFF_BAR = OFF_DS + 2 * DS_HALF;
+  // constant key-side aux operands: [1, 1, 0, ...] (S^T) and [0, 0, 1, 1, 0, ...] (dP^T)
+  static constexpr uint32_t OFF_KAUX = OFF_DS + 2 * DS_HALF;
+  static constexpr uint32_t OFF_VAUX = OFF_KAUX + BN * 32;
+  static constexpr uint32_t OFF_BAR = OFF_VAUX + BN * 32;
   // kv_full, s_full, p_full, dq_full, dq_empty, dkdv_full, drain, ds_free,
   // q_full[ST], q_empty[ST]
   static constexpr int NBAR = 8 + 2 * STAGES;
@@ -180,6 +188,17 @@ __global__ void __launch_bounds__(320, 1)
     prefetch_tmap(&tm_do);
     prefetch_tmap(&tm_dq);
   }
+  if (threadIdx.x < C::BN) {
+    // row r of the key-side aux operands, in 8-row x 16-byte core matrices
+    // (bf16 1.0 is 0x3f80)
+    const int r = threadIdx.x;
+    const uint32_t off = (r >> 3) * 256 + (r & 7) * 16;
+    *reinterpret_cast<uint4 *>(smem + C::OFF_KAUX + off) = make_uint4(0x3f803f80u, 0u, 0u, 0u);
+    *reinterpret_cast<uint4 *>(smem + C::OFF_KAUX + off + 128) = make_uint4(0u, 0u, 0u, 0u);
+    *reinterpret_cast<uint4 *>(smem + C::OFF_VAUX + off) = make_uint4(0u, 0x3f803f80u, 0u, 0u);
+    *reinterpret_cast<uint4 *>(smem + C::OFF_VAUX + off + 128) = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+  }
   if (warp == 0) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);
     tmem_relinquish();
@@ -217,16 +236,15 @@ __global__ void __launch_bounds__(320, 1)
         const int bh = b * p.Hq + step_head(s);
         const int q0 = step_qt(s) * C::BM;
         uint8_t *stage = smem + C::OFF_STAGE + st * C::STAGE_BYTES;
-        mbar_arrive_expect_tx(&q_full[st], 2 * C::QT_BYTES + 2 * C::VEC_BYTES);
+        mbar_arrive_expect_tx(&q_full[st], 2 * C::QT_BYTES + C::AUX_BYTES);
         for (int c = 0; c < C::NCHUNK; ++c) {
           tma_load_3d(stage + c * (C::BM * C::SPAN), &tm_q, &q_full[st], c * C::CHUNK, q0, bh);
           tma_load_3d(stage + C::QT_BYTES + c * (C::BM * C::SPAN), &tm_do, &q_full[st],
                       c * C::CHUNK, q0, bh);
         }
-        const size_t voff = (size_t)bh * p.Tq_pad + q0;
-        bulk_load(stage + 2 * C::QT_BYTES, p.l2 + voff, C::VEC_BYTES, &q_full[st]);
-        bulk_load(stage + 2 * C::QT_BYTES + C::VEC_BYTES, p.dvec + voff, C::VEC_BYTES,
-                  &q_full[st]);
+        // the aux rows of the step's 128 queries: two consecutive 64-row blocks
+        const size_t aoff = ((size_t)bh * (p.Tq_pad / 64) + q0 / 64) * 2048;
+        bulk_load(stage + 2 * C::QT_BYTES, p.aux + aoff, C::AUX_BYTES, &q_full[st]);
         last[st] = s;
       }
       if (!ok) fail();
@@ -256,6 +274,9 @@ __global__ void __launch_bounds__(320, 1)
       // dS as the MN-major A of dQ: rows = keys (128 bytes = 64 queries per half)
       const uint64_t ds_md = make_smem_desc(sbase + C::OFF_DS, C::DS_HALF, 8 * 128, kLayoutSW128);
       auto adv = [](uint64_t desc, uint32_t bytes) { return desc + (uint64_t)(bytes >> 4); };
+      // aux K-step: S^T gains -L/scale per query column, dP^T gains -D
+      const uint64_t kaux_d = make_smem_desc(sbase + C::OFF_KAUX, 128, 256, kLayoutNone);
+      const uint64_t vaux_d = make_smem_desc(sbase + C::OFF_VAUX, 128, 256, kLayoutNone);
       bool ok = wait_all(kv_full, 0);
       for (int s = 0; s < n_steps && ok; ++s) {
         const int st = s % ST, u = s / ST;
@@ -267,6 +288,7 @@ __global__ void __launch_bounds__(320, 1)
         const uint64_t q_kd = make_smem_desc(stage, 16, 8 * C::SPAN, C::LAYOUT);
         const uint64_t do_kd = make_smem_desc(stage + C::QT_BYTES, 16, 8 * C::SPAN, C::LAYOUT);
         const uint64_t q_md = make_smem_desc(stage, C::BM * C::SPAN, 8 * C::SPAN, C::LAYOUT);
+        const uint64_t qaux_d = make_smem_desc(stage + 2 * C::QT_BYTES, 128, 256, kLayoutNone);
         const uint64_t do_md =
             make_smem_desc(stage + C::QT_BYTES, C::BM * C::SPAN, 8 * C::SPAN, C::LAYOUT);
         // S^T = K Q^T
@@ -275,6 +297,7 @@ __global__ void __launch_bounds__(320, 1)
           const uint32_t off = ((kk * 16) / C::CHUNK) * (C::BN * C::SPAN) + ((kk * 16) % C::CHUNK) * 2;
           mma_bf16_ss_elect(tmem + C::TM_S, adv(k_kd, off), adv(q_kd, off), I_S, kk > 0 ? 1u : 0u);
         }
+        mma_bf16_ss_elect(tmem + C::TM_S, kaux_d, qaux_d, I_S, 1u);
         // dP^T overwrites the previous step's dQ: wait until it has been read.
         if (s > 0 && !wait_all(dq_empty, (s - 1) & 1)) { ok = false; break; }
         // dP^T = V dO^T
@@ -283,6 +306,7 @@ __global__ void __launch_bounds__(320, 1)
           const uint32_t off = ((kk * 16) / C::CHUNK) * (C::BN * C::SPAN) + ((kk * 16) % C::CHUNK) * 2;
           mma_bf16_ss_elect(tmem + C::TM_DP, adv(v_kd, off), adv(do_kd, off), I_S, kk > 0 ? 1u : 0u);
         }
+        mma_bf16_ss_elect(tmem + C::TM_DP, vaux_d, qaux_d, I_S, 1u);
         mma_commit_elect(s_full);
         if (!wait_all(p_full, s & 1)) { ok = false; break; }
         tc_fence_after();  // P^T and dS^T were written to tensor memory by other threads
@@ -295,7 +319,7 @@ __global__ void __launch_bounds__(320, 1)
         for (int kk = 0; kk < C::BM / 16; ++kk)
           mma_bf16_ts_elect(tmem + C::TM_DK, tmem + C::TM_DP + kk * 8, adv(q_md, kk * 16 * C::SPAN),
                       I_ACC, (s > 0 || kk > 0) ? 1u : 0u);
-        mma_commit_elect(&q_empty[st]);  // Q, dO, L, D of this stage are no longer read
+        mma_commit_elect(&q_empty[st]);  // Q, dO and aux of this stage are no longer read
         // dQ = dS K   (16 keys per MMA)
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)
@@ -322,11 +346,7 @@ __global__ void __launch_bounds__(320, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(s_full, s & 1, wait_ns) && !*abort_flag);
       if (!ok) break;
       tc_fence_after();
-      const int st = s % ST;
       const int q0 = step_qt(s) * C::BM;
-      const float *l2s = reinterpret_cast<const float *>(smem + C::OFF_STAGE +
-                                                         st * C::STAGE_BYTES + 2 * C::QT_BYTES);
-      const float *dvs = l2s + C::BM;
       // keys above the diagonal of some query of the tile need the mask
       const bool need_mask = p.causal && (kt * C::BN + C::BN - 1 > q0 + delta);
       const int lim = key - delta - q0;  // query q (in tile) sees the key iff q >= lim
@@ -336,20 +356,21 @@ __global__ void __launch_bounds__(320, 1)
         tmem_ld32_wait(tmem + lane_base + C::TM_S + c * 32, sv);
         tmem_ld32_wait(tmem + lane_base + C::TM_DP + c * 32, dp);
         uint32_t pw[16], dw[16];
+        // S^T already holds S - L/scale and dP^T holds dP - D (the aux K-step)
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
           const int q = c * 32 + i;
-          float p0 = ex2_approx(fmaf(sv[i], sl2, -l2s[q]));
-          float p1 = ex2_approx(fmaf(sv[i + 1], sl2, -l2s[q + 1]));
+          const float2 x = __fmul2_rn(make_float2(sv[i], sv[i + 1]), make_float2(sl2, sl2));
+          float p0 = ex2_approx(x.x);
+          float p1 = ex2_approx(x.y);
           if (need_mask) {
             if (q < lim) p0 = 0.f;
             if (q + 1 < lim) p1 = 0.f;
           }
           if (!key_ok) p0 = p1 = 0.f;
-          const float d0 = p0 * (dp[i] - dvs[q]);
-          const float d1 = p1 * (dp[i + 1] - dvs[q + 1]);
+          const float2 d = __fmul2_rn(make_float2(p0, p1), make_float2(dp[i], dp[i + 1]));
           pw[i / 2] = pack_bf16x2(p0, p1);
-          dw[i / 2] = pack_bf16x2(d0, d1);
+          dw[i / 2] = pack_bf16x2(d.x, d.y);
         }
         // P^T over S^T's columns [16c, 16c+16) and dS^T over dP^T's: those
         // scores were loaded in this or an earlier chunk.
@@ -900,15 +921,16 @@ __global__ void __launch_bounds__(320, 1)
   }
 }
 
-// D_i = dO_i . O_i and L_i * log2(e) per query row (padding rows to a
-// multiple of 128 get +inf and 0, so their probabilities vanish), and the
-// fp32 dQ accumulator zeroed.  One warp per row.
+// Per query row D_i = dO_i . O_i and the aux row [-L_i/scale, -D_i] (each as
+// a bf16 high and low part) that the backward kernels fold into S^T and dP^T;
+// padding rows (to a multiple of 128) get -1e30 and 0, so their
+// probabilities vanish.  Also zeroes the fp32 dQ accumulator.  One warp per
+// row.
 template <int D>
 __global__ void __launch_bounds__(256)
     attn_bwd_prep_kernel(const __nv_bfloat16 *__restrict__ o,
                          const __nv_bfloat16 *__restrict__ dout,
                          const float *__restrict__ lse, float *__restrict__ dq_acc,
-                         float *__restrict__ l2, float *__restrict__ dvec,
                          uint8_t *__restrict__ aux, float inv_scale, int rows_bh, int Tq,
                          int Tq_pad) {
   constexpr int VEC = D / 32;
@@ -920,7 +942,6 @@ __global__ void __launch_bounds__(256)
   // aux row i of its 64-row block: core matrix (r / 8, k-half 0) holds
   // [-L/scale hi, lo, -D hi, lo, 0 x 4]; k-half 1 is zero
   auto write_aux = [&](float a, float dd) {
-    if (!aux) return;
     const int r = i & 63;
     uint8_t *blk = aux + ((size_t)bh * (Tq_pad / 64) + i / 64) * 2048 + (r >> 3) * 256 + (r & 7) * 16;
     const __nv_bfloat16 ah = __float2bfloat16_rn(a);
@@ -933,11 +954,7 @@ __global__ void __launch_bounds__(256)
     *reinterpret_cast<uint4 *>(blk + 128) = make_uint4(0u, 0u, 0u, 0u);
   };
   if (i >= Tq) {
-    if (lane == 0) {
-      l2[warp] = INFINITY;
-      dvec[warp] = 0.f;
-      write_aux(-1e30f, 0.f);  // a probability of exactly 0, and finite products
-    }
+    if (lane == 0) write_aux(-1e30f, 0.f);  // a probability of exactly 0, finite products
     return;
   }
   const size_t row = (size_t)bh * Tq + i;
@@ -952,11 +969,7 @@ __global__ void __launch_bounds__(256)
   float *qrow = dq_acc + row * D + lane * VEC;
 #pragma unroll
   for (int e = 0; e < VEC; ++e) qrow[e] = 0.f;
-  if (lane == 0) {
-    l2[warp] = lse[row] * 1.4426950408889634f;
-    dvec[warp] = acc;
-    write_aux(-lse[row] * inv_scale, -acc);
-  }
+  if (lane == 0) write_aux(-lse[row] * inv_scale, -acc);
 }
 
 // dQ = scale * accumulator, rounded to bf16.
