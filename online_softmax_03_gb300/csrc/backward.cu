@@ -1,5 +1,6 @@
 // backward.cu -- launcher for the attention backward kernels.
 #include <cmath>
+#include <type_traits>
 
 #include "../../include/attn.h"
 #include "backward_kernel.cuh"
@@ -8,24 +9,28 @@
 namespace {
 __device__ unsigned int g_bwd_status;
 
-// The kernel for head dim D: 64-query steps with double-buffered S^T/dP^T at
-// d = 128, 128-query steps otherwise.
+// Launch the key-tile kernel with its tensor maps: K, V (128-key boxes), Q
+// and dO (C::BM-query boxes), and, for the 128-query kernel, the fp32 dQ
+// accumulator it reduces into by TMA.
 template <int D, typename C, typename Kern>
 int launch_main(const attn_host::BwdArgs &a, Kern kern, const attn_dev::BwdParams &p,
-                float *dq_acc, uint64_t bhq, uint64_t bhk) {
+                float *dq_acc, uint64_t bhq, uint64_t bhk, bool dq_map) {
   CUtensorMap tq, tk, tv, tdo, tdq;
   if (!attn_host::encode_tmap_3d_bf16(&tq, a.q, D, a.Tq, bhq, C::CHUNK, C::BM, 1, C::SPAN) ||
       !attn_host::encode_tmap_3d_bf16(&tdo, a.dout, D, a.Tq, bhq, C::CHUNK, C::BM, 1, C::SPAN) ||
       !attn_host::encode_tmap_3d_bf16(&tk, a.k, D, a.Tk, bhk, C::CHUNK, C::BN, 1, C::SPAN) ||
       !attn_host::encode_tmap_3d_bf16(&tv, a.v, D, a.Tk, bhk, C::CHUNK, C::BN, 1, C::SPAN) ||
-      !attn_host::encode_tmap_3d_f32(&tdq, dq_acc, D, a.Tq, bhq, 32, C::BM, 1))
+      (dq_map && !attn_host::encode_tmap_3d_f32(&tdq, dq_acc, D, a.Tq, bhq, 32, C::BM, 1)))
     return ATTN_ERR_CUDA;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)C::SMEM_BYTES) != cudaSuccess)
     return ATTN_ERR_CUDA;
   const int n_kt = (a.Tk + C::BN - 1) / C::BN;
-  kern<<<dim3(n_kt, (unsigned)bhk), C::THREADS, C::SMEM_BYTES, a.stream>>>(tq, tk, tv, tdo, tdq,
-                                                                          p);
+  const dim3 grid(n_kt, (unsigned)bhk);
+  if constexpr (std::is_same<C, attn_dev::BwdPipeCfg>::value)
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(tq, tk, tv, tdo, p);
+  else
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(tq, tk, tv, tdo, tdq, p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -55,6 +60,7 @@ int launch_bwd(const attn_host::BwdArgs &a, unsigned int *status) {
   p.dk = static_cast<__nv_bfloat16 *>(a.dk);
   p.dv = static_cast<__nv_bfloat16 *>(a.dv);
   p.aux = aux;
+  p.dq_acc = dq_acc;
   p.status = status;
   p.Hq = a.Hq;
   p.Hkv = a.Hkv;
@@ -70,10 +76,10 @@ int launch_bwd(const attn_host::BwdArgs &a, unsigned int *status) {
   int rc;
   if constexpr (D == 128)
     rc = launch_main<D, attn_dev::BwdPipeCfg>(a, attn_dev::attn_bwd_pipelined_kernel, p, dq_acc,
-                                              bhq, bhk);
+                                              bhq, bhk, false);
   else
     rc = launch_main<D, attn_dev::BwdCfg<D>>(a, attn_dev::attn_bwd_kernel<D>, p, dq_acc, bhq,
-                                             bhk);
+                                             bhk, true);
   if (rc != ATTN_OK) return rc;
   // 3. dQ = scale * accumulator in bf16
   {

@@ -72,6 +72,7 @@ struct BwdParams {
   // [-L/scale (hi, lo), -D (hi, lo), 0 x 12] with D = rowsum(dO o O), laid out
   // as 8-row x 16-byte core matrices; padding rows carry -1e30 and 0
   const uint8_t *aux;
+  float *dq_acc;           // [B*Hq, Tq, D] fp32 dQ accumulator (d = 128 kernel)
   unsigned int *status;
   int Hq, Hkv, group;
   int Tq, Tk, Tq_pad;
@@ -501,9 +502,9 @@ __global__ void __launch_bounds__(320, 1)
 // memory, so the tensor core computes the next step's S^T and dP^T while
 // the P/dS threads work on this step, and three stages of Q and dO.  dQ is
 // computed transposed, dQ^T = K^T dS^T (M = d = 128 lanes, one per head-dim
-// column), over the dP^T columns of its buffer once dK has read dS^T, and is
-// staged in its own shared-memory tile, 32 columns x 2 at a time, for the
-// reduction.
+// column), over the dP^T columns of its buffer once dK has read dS^T; the
+// thread of each head-dim column adds its 64 values straight into the fp32
+// accumulator (one coalesced 128-byte reduction per warp instruction).
 //
 // Tensor memory: buffer b in {0,1}: S^T_b [128b, 128b+64) with P^T_b over its
 // first 32 columns, dP^T_b [128b+64, 128b+128) with dS^T_b over its first 32
@@ -525,11 +526,8 @@ struct BwdPipeCfg {
   static constexpr uint32_t OFF_STAGE = OFF_V + KV_BYTES;
   static constexpr uint32_t OFF_DS = OFF_STAGE + STAGES * STAGE_BYTES;  // 2 x [128 keys x 128 B]
   static constexpr uint32_t DS_BYTES = BN * 128;
-  // dQ staged two [64 rows x 32 fp32] chunks at a time
-  static constexpr uint32_t OFF_DQ = OFF_DS + 2 * DS_BYTES;
-  static constexpr uint32_t DQ_CHUNK = BM * 128;
   // constant key-side aux operands: [1, 1, 0, ...] (S^T) and [0, 0, 1, 1, 0, ...] (dP^T)
-  static constexpr uint32_t OFF_KAUX = OFF_DQ + 2 * DQ_CHUNK;
+  static constexpr uint32_t OFF_KAUX = OFF_DS + 2 * DS_BYTES;
   static constexpr uint32_t OFF_VAUX = OFF_KAUX + BN * 32;
   static constexpr uint32_t OFF_BAR = OFF_VAUX + BN * 32;
   // kv_full, dkdv_full, drain, then per stage q_full, q_empty, then per
@@ -543,7 +541,7 @@ struct BwdPipeCfg {
   static constexpr uint32_t TM_DV = 256, TM_DK = 384;
   static constexpr int THREADS = 320;
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-  static_assert(OFF_STAGE % 1024 == 0 && OFF_DS % 1024 == 0 && OFF_DQ % 1024 == 0, "alignment");
+  static_assert(OFF_STAGE % 1024 == 0 && OFF_DS % 1024 == 0, "alignment");
 };
 
 __global__ void __launch_bounds__(320, 1)
@@ -551,7 +549,6 @@ __global__ void __launch_bounds__(320, 1)
                               const __grid_constant__ CUtensorMap tm_k,
                               const __grid_constant__ CUtensorMap tm_v,
                               const __grid_constant__ CUtensorMap tm_do,
-                              const __grid_constant__ CUtensorMap tm_dq,
                               const BwdParams p) {
   using C = BwdPipeCfg;
   constexpr int D = C::D;
@@ -603,7 +600,6 @@ __global__ void __launch_bounds__(320, 1)
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
     prefetch_tmap(&tm_do);
-    prefetch_tmap(&tm_dq);
   }
   if (threadIdx.x < C::BN) {
     // row r of the key-side aux operands, in 8-row x 16-byte core matrices
@@ -858,15 +854,12 @@ __global__ void __launch_bounds__(320, 1)
     }
   } else {
     // --------------------------- dQ^T of each step, one head-dim column per thread
+    // Thread cdim holds column cdim of the step's dQ (64 queries) and adds it
+    // into the fp32 accumulator with one reduction per query: a warp covers
+    // 32 consecutive head-dim columns, so each instruction is one coalesced
+    // 128-byte reduction, with no shared-memory staging.
     const int cdim = threadIdx.x - 128;  // head-dim column == TMEM lane
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const bool elected = (cdim == 0);
-    // column cdim of the staged [64 queries x 32] fp32 chunk cdim / 32 (two
-    // chunks per round, in buffers (cdim / 32) % 2): 16-byte unit
-    // (cdim % 32) / 4 of each 128-byte row, swizzled by the row
-    uint8_t *stage_col = smem + C::OFF_DQ + ((cdim >> 5) & 1) * C::DQ_CHUNK + (cdim & 3) * 4;
-    const int unit = (cdim & 31) >> 2;
-    const int round_of_col = cdim >> 6;  // chunks 0-1 in round 0, 2-3 in round 1
     bool ok = true;
     for (int s = 0; s < n_steps; ++s) {
       const int x = s & 1;
@@ -875,42 +868,31 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_after();
       float v[64];
       {
-        float a[32], bb[32];
-        tmem_ld32_wait(tmem + lane_base + C::tm_dp(x), a);
-        tmem_ld32_wait(tmem + lane_base + C::tm_dp(x) + 32, bb);
+        float a0[32], a1[32];
+        tmem_ld32_wait(tmem + lane_base + C::tm_dp(x), a0);
+        tmem_ld32_wait(tmem + lane_base + C::tm_dp(x) + 32, a1);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          v[i] = a[i];
-          v[32 + i] = bb[i];
+          v[i] = a0[i];
+          v[32 + i] = a1[i];
         }
       }
       tc_fence_before();
       mbar_arrive(&dq_empty[x]);  // the step's dQ^T has left tensor memory
       const int bh = b * p.Hq + step_head(s);
       const int q0 = step_qt(s) * C::BM;
-#pragma unroll 1
-      for (int round = 0; round < 2; ++round) {
-        // the reductions issued last round have read the staging buffers
-        if (elected && (s > 0 || round > 0)) bulk_wait_group_read0();
-        named_barrier_sync(1, 128);
-        if (round_of_col == round) {
+      const int nq = min(C::BM, p.Tq - q0);
+      float *dst = p.dq_acc + ((size_t)bh * p.Tq + q0) * D + cdim;
+      if (nq == C::BM) {
 #pragma unroll
-          for (int q = 0; q < C::BM; ++q)
-            *reinterpret_cast<float *>(stage_col + q * 128 + ((unit ^ (q & 7)) << 4)) = v[q];
-          fence_proxy_async_smem();
-        }
-        named_barrier_sync(1, 128);
-        if (elected) {
+        for (int q = 0; q < C::BM; ++q) atomicAdd(dst + (size_t)q * D, v[q]);
+      } else {
 #pragma unroll
-          for (int k2 = 0; k2 < 2; ++k2)
-            tma_reduce_add_3d(&tm_dq, smem + C::OFF_DQ + k2 * C::DQ_CHUNK, (round * 2 + k2) * 32,
-                              q0, bh);
-          bulk_commit_group();
-        }
+        for (int q = 0; q < C::BM; ++q)
+          if (q < nq) atomicAdd(dst + (size_t)q * D, v[q]);
       }
     }
     if (!ok) fail();
-    if (elected) bulk_wait_group0();
   }
 
   tc_fence_before();
