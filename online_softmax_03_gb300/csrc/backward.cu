@@ -27,9 +27,14 @@ int launch_main(const attn_host::BwdArgs &a, Kern kern, const attn_dev::BwdParam
     return ATTN_ERR_CUDA;
   const int n_kt = (a.Tk + C::BN - 1) / C::BN;
   const dim3 grid(n_kt, (unsigned)bhk);
-  if constexpr (std::is_same<C, attn_dev::BwdPipeCfg>::value)
-    kern<<<grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(tq, tk, tv, tdo, p);
-  else
+  if constexpr (std::is_same<C, attn_dev::BwdPipeCfg>::value) {
+    // dK and dV leave by TMA stores of the same boxes as K and V
+    CUtensorMap tdk, tdv;
+    if (!attn_host::encode_tmap_3d_bf16(&tdk, a.dk, D, a.Tk, bhk, C::CHUNK, C::BN, 1, C::SPAN) ||
+        !attn_host::encode_tmap_3d_bf16(&tdv, a.dv, D, a.Tk, bhk, C::CHUNK, C::BN, 1, C::SPAN))
+      return ATTN_ERR_CUDA;
+    kern<<<grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(tq, tk, tv, tdo, tdk, tdv, p);
+  } else
     kern<<<grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(tq, tk, tv, tdo, tdq, p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }

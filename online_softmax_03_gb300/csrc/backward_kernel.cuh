@@ -542,6 +542,7 @@ struct BwdPipeCfg {
   static constexpr int THREADS = 320;
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(OFF_STAGE % 1024 == 0 && OFF_DS % 1024 == 0, "alignment");
+  static_assert(4 * BN * SPAN <= STAGES * STAGE_BYTES, "dK/dV staging fits the Q/dO stages");
 };
 
 __global__ void __launch_bounds__(320, 1)
@@ -549,6 +550,8 @@ __global__ void __launch_bounds__(320, 1)
                               const __grid_constant__ CUtensorMap tm_k,
                               const __grid_constant__ CUtensorMap tm_v,
                               const __grid_constant__ CUtensorMap tm_do,
+                              const __grid_constant__ CUtensorMap tm_dk,
+                              const __grid_constant__ CUtensorMap tm_dv,
                               const BwdParams p) {
   using C = BwdPipeCfg;
   constexpr int D = C::D;
@@ -824,13 +827,16 @@ __global__ void __launch_bounds__(320, 1)
       if (!ok) fail();
     }
     if (ok) {
+      // All MMAs have completed (dkdv_full), so the Q/dO stages are free: dV
+      // and dK (times scale) go there as bf16 in the 128-byte-swizzled layout
+      // of the K/V tiles (per tile two 64-column chunks of 128 rows x 128 B),
+      // and leave by TMA stores, which also drop rows past the sequence end.
       tc_fence_after();
-      const size_t row = ((size_t)bkv * p.Tk + key) * D;
+      uint8_t *out = smem + C::OFF_STAGE;  // dV chunk 0, 1, then dK chunk 0, 1
 #pragma unroll 1
       for (int which = 0; which < 2; ++which) {
         const uint32_t col = which == 0 ? C::TM_DV : C::TM_DK;
         const float mul = which == 0 ? 1.f : p.scale;
-        __nv_bfloat16 *dst = (which == 0 ? p.dv : p.dk) + row;
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           float v[32];
@@ -840,16 +846,30 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = 0.f;
           }
-          if (key_ok) {
-            uint4 *o = reinterpret_cast<uint4 *>(dst + c * 32);
+          // columns [32c, 32c+32) are 16-byte units 4(c%2) .. 4(c%2)+3 of row
+          // r in chunk c/2, swizzled by the row
+          uint8_t *row = out + (which * 2 + c / 2) * (C::BN * C::SPAN) + r * C::SPAN;
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-              o[u] = make_uint4(pack_bf16x2(v[8 * u] * mul, v[8 * u + 1] * mul),
-                                pack_bf16x2(v[8 * u + 2] * mul, v[8 * u + 3] * mul),
-                                pack_bf16x2(v[8 * u + 4] * mul, v[8 * u + 5] * mul),
-                                pack_bf16x2(v[8 * u + 6] * mul, v[8 * u + 7] * mul));
+          for (int u = 0; u < 4; ++u) {
+            const int unit = (c & 1) * 4 + u;
+            *reinterpret_cast<uint4 *>(row + ((unit ^ (r & 7)) << 4)) =
+                make_uint4(pack_bf16x2(v[8 * u] * mul, v[8 * u + 1] * mul),
+                           pack_bf16x2(v[8 * u + 2] * mul, v[8 * u + 3] * mul),
+                           pack_bf16x2(v[8 * u + 4] * mul, v[8 * u + 5] * mul),
+                           pack_bf16x2(v[8 * u + 6] * mul, v[8 * u + 7] * mul));
           }
         }
+      }
+      fence_proxy_async_smem();
+      named_barrier_sync(1, C::BN);
+      if (threadIdx.x == 0) {
+        for (int c = 0; c < C::NCHUNK; ++c) {
+          tma_store_3d(&tm_dv, out + c * (C::BN * C::SPAN), c * C::CHUNK, kt * C::BN, bkv);
+          tma_store_3d(&tm_dk, out + (C::NCHUNK + c) * (C::BN * C::SPAN), c * C::CHUNK,
+                       kt * C::BN, bkv);
+        }
+        bulk_commit_group();
+        bulk_wait_group0();
       }
     }
   } else {
