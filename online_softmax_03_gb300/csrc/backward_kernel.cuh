@@ -506,9 +506,11 @@ __global__ void __launch_bounds__(320, 1)
 // thread of each head-dim column adds its 64 values straight into the fp32
 // accumulator (one coalesced 128-byte reduction per warp instruction).
 //
-// Tensor memory: buffer b in {0,1}: S^T_b [128b, 128b+64) with P^T_b over its
-// first 32 columns, dP^T_b [128b+64, 128b+128) with dS^T_b over its first 32
-// and dQ^T_b over all 64; dV [256,384); dK [384,512).
+// Tensor memory: buffer b in {0,1}: S^T_b [128b, 128b+64), dP^T_b [128b+64,
+// 128b+128) with dQ^T_b over all 64 columns; the bf16 P^T_b (dS^T_b) of queries
+// [32c, 32c+32) is packed into the 16 columns at 32c of S^T_b (dP^T_b), the
+// columns the fp32 values of those queries came from; dV [256,384); dK
+// [384,512).
 struct BwdPipeCfg {
   static constexpr int D = 128;
   static constexpr int BM = 64;                       // queries per step
@@ -539,13 +541,17 @@ struct BwdPipeCfg {
   __host__ __device__ static constexpr uint32_t tm_s(int b) { return 128 * b; }
   __host__ __device__ static constexpr uint32_t tm_dp(int b) { return 128 * b + 64; }
   static constexpr uint32_t TM_DV = 256, TM_DK = 384;
-  static constexpr int THREADS = 320;
+  // column of the packed bf16 queries [16kk, 16kk+16) within S^T_b / dP^T_b
+  __host__ __device__ static constexpr uint32_t packed_col(int kk) {
+    return (kk / 2) * 32 + (kk % 2) * 8;
+  }
+  static constexpr int THREADS = 448;
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(OFF_STAGE % 1024 == 0 && OFF_DS % 1024 == 0, "alignment");
   static_assert(4 * BN * SPAN <= STAGES * STAGE_BYTES, "dK/dV staging fits the Q/dO stages");
 };
 
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(448, 1)
     attn_bwd_pipelined_kernel(const __grid_constant__ CUtensorMap tm_q,
                               const __grid_constant__ CUtensorMap tm_k,
                               const __grid_constant__ CUtensorMap tm_v,
@@ -592,7 +598,7 @@ __global__ void __launch_bounds__(320, 1)
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&s_full[x], 1);
-      mbar_init(&p_full[x], 128);
+      mbar_init(&p_full[x], 2 * C::BN);
       mbar_init(&dq_full[x], 1);
       mbar_init(&dq_empty[x], 128);
       mbar_init(&ds_free[x], 1);
@@ -632,7 +638,7 @@ __global__ void __launch_bounds__(320, 1)
   auto step_head = [&](int s) { return g * p.group + s / n_q; };
   auto step_qt = [&](int s) { return qt_lo + s % n_q; };
 
-  if (warp == 8) {
+  if (warp == 12) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       bool ok = true;
@@ -668,7 +674,7 @@ __global__ void __launch_bounds__(320, 1)
         if (last[s] >= 0) mbar_wait(&q_full[s], (last[s] / ST) & 1, wait_ns);
     }
     __syncwarp();
-  } else if (warp == 9) {
+  } else if (warp == 13) {
     // ------------------------------------- MMA issuer (converged, elected lane)
     {
       auto wait_all = [&](uint64_t *bar, uint32_t parity) -> bool {
@@ -736,11 +742,11 @@ __global__ void __launch_bounds__(320, 1)
         // dV += P^T dO, dK += dS^T Q   (16 queries = 8 columns of packed bf16)
 #pragma unroll
         for (int kk = 0; kk < C::BM / 16; ++kk)
-          mma_bf16_ts_elect(tmem + C::TM_DV, tmem + C::tm_s(x) + kk * 8,
+          mma_bf16_ts_elect(tmem + C::TM_DV, tmem + C::tm_s(x) + C::packed_col(kk),
                             adv(do_md, kk * 16 * C::SPAN), I_ACC, (s > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < C::BM / 16; ++kk)
-          mma_bf16_ts_elect(tmem + C::TM_DK, tmem + C::tm_dp(x) + kk * 8,
+          mma_bf16_ts_elect(tmem + C::TM_DK, tmem + C::tm_dp(x) + C::packed_col(kk),
                             adv(q_md, kk * 16 * C::SPAN), I_ACC, (s > 0 || kk > 0) ? 1u : 0u);
         mma_commit_elect(&q_empty[st]);
         // dQ^T = K^T dS^T   (16 keys per MMA; B = dS^T rows of 64 queries)
@@ -759,10 +765,12 @@ __global__ void __launch_bounds__(320, 1)
       wait_all(drain, 0);
     }
     __syncwarp();
-  } else if (warp < 4) {
+  } else if (warp < 8) {
     // ------------------------------------------- P and dS, one key per thread
-    const int r = threadIdx.x;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    // Two warpgroups: warpgroup c takes queries [32c, 32c+32) of each step.
+    const int r = threadIdx.x & (C::BN - 1);
+    const int c = warp >> 2;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const int key = kt * C::BN + r;
     const bool key_ok = key < p.Tk;
     const float sl2 = p.scale_log2;
@@ -776,8 +784,7 @@ __global__ void __launch_bounds__(320, 1)
       const bool need_mask = p.causal && (kt * C::BN + C::BN - 1 > q0 + delta);
       const int lim = key - delta - q0;  // query q (in tile) sees the key iff q >= lim
       uint8_t *ds_row = smem + C::OFF_DS + x * C::DS_BYTES + r * 128;
-#pragma unroll 1
-      for (int c = 0; c < C::BM / 32; ++c) {
+      {
         float sv[32], dp[32];
         tmem_ld32_wait(tmem + lane_base + C::tm_s(x) + c * 32, sv);
         tmem_ld32_wait(tmem + lane_base + C::tm_dp(x) + c * 32, dp);
@@ -798,12 +805,12 @@ __global__ void __launch_bounds__(320, 1)
           pw[i / 2] = pack_bf16x2(p0, p1);
           dw[i / 2] = pack_bf16x2(d.x, d.y);
         }
-        tmem_st16(tmem + lane_base + C::tm_s(x) + c * 16, pw);
-        tmem_st16(tmem + lane_base + C::tm_dp(x) + c * 16, dw);
+        tmem_st16(tmem + lane_base + C::tm_s(x) + c * 32, pw);
+        tmem_st16(tmem + lane_base + C::tm_dp(x) + c * 32, dw);
         // dS^T row: queries [32c, 32c+32) are 16-byte units 4c .. 4c+3 of the
         // 128-byte row, swizzled by the row; the buffer is free once the dQ^T
         // MMA of step s - 2 has read it.
-        if (c == 0 && s >= 2) {
+        if (s >= 2) {
           ok = __all_sync(0xffffffffu, mbar_wait(&ds_free[x], ((s - 2) >> 1) & 1, wait_ns));
           if (!ok) break;
         }
@@ -833,25 +840,25 @@ __global__ void __launch_bounds__(320, 1)
       // and leave by TMA stores, which also drop rows past the sequence end.
       tc_fence_after();
       uint8_t *out = smem + C::OFF_STAGE;  // dV chunk 0, 1, then dK chunk 0, 1
-#pragma unroll 1
-      for (int which = 0; which < 2; ++which) {
+      {
+        const int which = c;  // warpgroup 0 writes dV, warpgroup 1 dK
         const uint32_t col = which == 0 ? C::TM_DV : C::TM_DK;
         const float mul = which == 0 ? 1.f : p.scale;
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
+        for (int cg = 0; cg < D / 32; ++cg) {
           float v[32];
           if (n_steps > 0) {
-            tmem_ld32_wait(tmem + lane_base + col + c * 32, v);
+            tmem_ld32_wait(tmem + lane_base + col + cg * 32, v);
           } else {
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = 0.f;
           }
-          // columns [32c, 32c+32) are 16-byte units 4(c%2) .. 4(c%2)+3 of row
-          // r in chunk c/2, swizzled by the row
-          uint8_t *row = out + (which * 2 + c / 2) * (C::BN * C::SPAN) + r * C::SPAN;
+          // columns [32cg, 32cg+32) are 16-byte units 4(cg%2) .. 4(cg%2)+3 of
+          // row r in chunk cg/2, swizzled by the row
+          uint8_t *row = out + (which * 2 + cg / 2) * (C::BN * C::SPAN) + r * C::SPAN;
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const int unit = (c & 1) * 4 + u;
+            const int unit = (cg & 1) * 4 + u;
             *reinterpret_cast<uint4 *>(row + ((unit ^ (r & 7)) << 4)) =
                 make_uint4(pack_bf16x2(v[8 * u] * mul, v[8 * u + 1] * mul),
                            pack_bf16x2(v[8 * u + 2] * mul, v[8 * u + 3] * mul),
@@ -861,7 +868,7 @@ __global__ void __launch_bounds__(320, 1)
         }
       }
       fence_proxy_async_smem();
-      named_barrier_sync(1, C::BN);
+      named_barrier_sync(1, 2 * C::BN);
       if (threadIdx.x == 0) {
         for (int c = 0; c < C::NCHUNK; ++c) {
           tma_store_3d(&tm_dv, out + c * (C::BN * C::SPAN), c * C::CHUNK, kt * C::BN, bkv);
@@ -878,7 +885,7 @@ __global__ void __launch_bounds__(320, 1)
     // into the fp32 accumulator with one reduction per query: a warp covers
     // 32 consecutive head-dim columns, so each instruction is one coalesced
     // 128-byte reduction, with no shared-memory staging.
-    const int cdim = threadIdx.x - 128;  // head-dim column == TMEM lane
+    const int cdim = threadIdx.x - 2 * C::BN;  // head-dim column == TMEM lane
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     bool ok = true;
     for (int s = 0; s < n_steps; ++s) {
