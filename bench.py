@@ -197,6 +197,13 @@ def whole_job_rate(units_per_rank: float, seconds_max: float, world: int) -> flo
 
 # ------------------------------------------------------------------ GPU arm
 
+def percentiles(ms):
+    """10th, 50th and 90th percentile of this rank's per-launch times (ms)."""
+    xs = sorted(ms)
+    pick = lambda f: xs[min(len(xs) - 1, int(f * (len(xs) - 1) + 0.5))]
+    return [round(pick(0.1), 4), round(pick(0.5), 4), round(pick(0.9), 4)]
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
 
@@ -395,6 +402,7 @@ def run_ours(args, rank, world, local_rank):
         "data": "synthetic",
         "config": workload_config(world),
         "prefill_ms": round(pre_s * 1e3 / K, 4),
+        "prefill_ms_p10_p50_p90": percentiles(pre_ms),
         "roofline": {
             "kernel": "prefill_fwd_kernel<128>",
             "bound": "tensor",
@@ -412,6 +420,7 @@ def run_ours(args, rank, world, local_rank):
             "value": round(dec_gbs, 1),
             "unit": "GB/s",
             "ms": round(dec_s * 1e3 / K, 4),
+            "ms_p10_p50_p90": percentiles(dec_ms),
             "frac_of_8TBs": round(per_launch_gbs / 8000.0, 4),
             "roofline": {
                 "kernel": "decode_split_kernel<128,4> + decode_combine_kernel<128>",
