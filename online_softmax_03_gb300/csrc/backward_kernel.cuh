@@ -930,6 +930,452 @@ __global__ void __launch_bounds__(448, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// d = 128, 128-query steps: every product is an M = 128, N = 128 MMA (an
+// N = 64 product costs about 50 cycles of the tensor pipe for 32 cycles of
+// work, N = 128 costs its 64).  Tensor memory holds one step: region A
+// [0,128) S^T, then the bf16 P^T packed in place; region B [128,256) dP^T,
+// then the packed dS^T, then dQ^T; dV [256,384); dK [384,512).  Per step the
+// tensor pipe runs, in issue order,
+//     dP(s)  dV(s)  S(s+1)  dK(s)  dQ^T(s)
+// dP(s) goes first (once dQ^T(s-1) has left region B), so the P/dS threads
+// form dS(s) right after P(s); S(s+1) runs while they do.  Q (with its aux
+// rows) is double-buffered, dO single-buffered.
+//
+// Warps 0-7: P and dS, one key per thread, warpgroup c owning queries
+// [64c, 64c+64); warps 8-15: dQ^T drain, warp w owning TMEM lanes
+// 32(w%4).. (head-dim columns) for queries [64h, 64h+64), h = (w-8)/4;
+// warp 16: TMA producer; warp 17: MMA issuer (converged, elected lane).
+struct BwdBm128Cfg {
+  static constexpr int D = 128;
+  static constexpr int BM = 128;                      // queries per step
+  static constexpr int BN = 128;                      // keys per CTA
+  static constexpr int SPAN = 128;
+  static constexpr int CHUNK = 64;
+  static constexpr int NCHUNK = 2;
+  static constexpr uint32_t KV_BYTES = BN * D * 2;    // 32 KB
+  static constexpr uint32_t QT_BYTES = BM * D * 2;    // 32 KB
+  static constexpr uint32_t AUX_BYTES = BM * 32;      // 4 KB: 16 bf16 per query
+  static constexpr uint32_t QBUF_BYTES = QT_BYTES + AUX_BYTES;  // Q | aux, 36 KB
+  static constexpr uint32_t OFF_K = 0;
+  static constexpr uint32_t OFF_V = OFF_K + KV_BYTES;
+  static constexpr uint32_t OFF_Q = OFF_V + KV_BYTES;               // 2 buffers
+  static constexpr uint32_t OFF_DO = OFF_Q + 2 * QBUF_BYTES;        // 1 buffer
+  static constexpr uint32_t OFF_DS = OFF_DO + QT_BYTES;             // dS^T, 2 x 16 KB
+  static constexpr uint32_t DS_CHUNK = BN * 128;                    // 64 queries x 128 keys
+  static constexpr uint32_t OFF_KAUX = OFF_DS + 2 * DS_CHUNK;
+  static constexpr uint32_t OFF_VAUX = OFF_KAUX + BN * 32;
+  static constexpr uint32_t OFF_BAR = OFF_VAUX + BN * 32;
+  // kv_full, do_full, do_empty, s_full, p_full, dp_full, ds_full, dq_full,
+  // dq_empty, ds_free, dkdv_full, drain, q_full[2], q_empty[2]
+  static constexpr int NBAR = 16;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t TM_A = 0, TM_B = 128, TM_DV = 256, TM_DK = 384;
+  static constexpr int THREADS = 576;
+  // column of the packed bf16 queries [16kk, 16kk+16) within region A / B
+  __host__ __device__ static constexpr uint32_t packed_col(int kk) {
+    return (kk / 4) * 64 + (kk % 4) * 8;
+  }
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert(OFF_Q % 1024 == 0 && QBUF_BYTES % 1024 == 0 && OFF_DO % 1024 == 0 &&
+                    OFF_DS % 1024 == 0,
+                "1 KiB aligned swizzled tiles");
+  static_assert(4 * BN * SPAN <= 2 * QBUF_BYTES, "dK/dV staging fits the Q buffers");
+};
+
+__global__ void __launch_bounds__(576, 1)
+    attn_bwd_bm128_kernel(const __grid_constant__ CUtensorMap tm_q,
+                          const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_v,
+                          const __grid_constant__ CUtensorMap tm_do,
+                          const __grid_constant__ CUtensorMap tm_dk,
+                          const __grid_constant__ CUtensorMap tm_dv,
+                          const BwdParams p) {
+  using C = BwdBm128Cfg;
+  constexpr int D = C::D;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+  uint64_t *kv_full = bars + 0, *do_full = bars + 1, *do_empty = bars + 2;
+  uint64_t *s_full = bars + 3, *p_full = bars + 4, *dp_full = bars + 5, *ds_full = bars + 6;
+  uint64_t *dq_full = bars + 7, *dq_empty = bars + 8, *ds_free = bars + 9;
+  uint64_t *dkdv_full = bars + 10, *drain = bars + 11;
+  uint64_t *q_full = bars + 12, *q_empty = bars + 14;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint64_t wait_ns = p.wait_ns;
+
+  const int kt = blockIdx.x;
+  const int bkv = blockIdx.y;
+  const int b = bkv / p.Hkv;
+  const int g = bkv - b * p.Hkv;
+  const int delta = p.Tk - p.Tq;
+  const int n_qt = p.Tq_pad / C::BM;  // 128-query tiles
+  const int qt_lo = p.causal ? max(0, kt * C::BN - delta) / C::BM : 0;
+  const int n_q = n_qt - qt_lo;
+  const int n_steps = n_q > 0 ? p.group * n_q : 0;
+
+  if (threadIdx.x == 0) {
+    // p_full and ds_full: all 256 P/dS threads; dq_empty: all 256 dQ threads
+    for (int i = 0; i < C::NBAR; ++i)
+      mbar_init(&bars[i], (i == 4 || i == 6) ? 2 * C::BN : i == 8 ? 2 * C::D : 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+    prefetch_tmap(&tm_do);
+  }
+  if (threadIdx.x < C::BN) {
+    // row r of the key-side aux operands, in 8-row x 16-byte core matrices
+    // (core matrix (r / 8, k-half) at (r / 8) * 256 + k-half * 128, row r % 8
+    // at + (r % 8) * 16); bf16 1.0 is 0x3f80
+    const int r = threadIdx.x;
+    const uint32_t off = (r >> 3) * 256 + (r & 7) * 16;
+    *reinterpret_cast<uint4 *>(smem + C::OFF_KAUX + off) = make_uint4(0x3f803f80u, 0u, 0u, 0u);
+    *reinterpret_cast<uint4 *>(smem + C::OFF_KAUX + off + 128) = make_uint4(0u, 0u, 0u, 0u);
+    *reinterpret_cast<uint4 *>(smem + C::OFF_VAUX + off) = make_uint4(0u, 0x3f803f80u, 0u, 0u);
+    *reinterpret_cast<uint4 *>(smem + C::OFF_VAUX + off + 128) = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  auto fail = [&]() {
+    atomicExch(p.status, kBwdStatusTimeout);
+    *abort_flag = 1;
+  };
+  auto step_head = [&](int s) { return g * p.group + s / n_q; };
+  auto step_qt = [&](int s) { return qt_lo + s % n_q; };
+
+  if (warp == 16) {
+    // ------------------------------------------------------------ producer
+    // Loads in the order the tensor pipe frees their buffers: Q(s) once
+    // dK(s-2) has read Q(s-2), dO(s) once dV(s-1) and dP(s-1) have read dO(s-1).
+    if (lane == 0) {
+      bool ok = true;
+      int last_q[2] = {-1, -1};
+      mbar_arrive_expect_tx(kv_full, 2 * C::KV_BYTES);
+      for (int c = 0; c < C::NCHUNK; ++c) {
+        tma_load_3d(smem + C::OFF_K + c * (C::BN * C::SPAN), &tm_k, kv_full, c * C::CHUNK,
+                    kt * C::BN, bkv);
+        tma_load_3d(smem + C::OFF_V + c * (C::BN * C::SPAN), &tm_v, kv_full, c * C::CHUNK,
+                    kt * C::BN, bkv);
+      }
+      for (int s = 0; s < n_steps && ok; ++s) {
+        if (*abort_flag) { ok = false; break; }
+        const int bh = b * p.Hq + step_head(s);
+        const int q0 = step_qt(s) * C::BM;
+        const int qb = s & 1;
+        if (s >= 2 && !mbar_wait(&q_empty[qb], ((s >> 1) - 1) & 1, wait_ns)) { ok = false; break; }
+        uint8_t *qbuf = smem + C::OFF_Q + qb * C::QBUF_BYTES;
+        mbar_arrive_expect_tx(&q_full[qb], C::QT_BYTES + C::AUX_BYTES);
+        for (int c = 0; c < C::NCHUNK; ++c)
+          tma_load_3d(qbuf + c * (C::BM * C::SPAN), &tm_q, &q_full[qb], c * C::CHUNK, q0, bh);
+        // aux rows of 64-row blocks are 2 KB each and contiguous
+        const size_t aoff = ((size_t)bh * (p.Tq_pad / 64) + q0 / 64) * 2048;
+        bulk_load(qbuf + C::QT_BYTES, p.aux + aoff, C::AUX_BYTES, &q_full[qb]);
+        last_q[qb] = s;
+        if (s >= 1 && !mbar_wait(do_empty, (s - 1) & 1, wait_ns)) { ok = false; break; }
+        mbar_arrive_expect_tx(do_full, C::QT_BYTES);
+        for (int c = 0; c < C::NCHUNK; ++c)
+          tma_load_3d(smem + C::OFF_DO + c * (C::BM * C::SPAN), &tm_do, do_full, c * C::CHUNK,
+                      q0, bh);
+      }
+      if (!ok) fail();
+      // Drain: every copy issued has landed before shared memory is released.
+      mbar_wait(kv_full, 0, wait_ns);
+      for (int qb = 0; qb < 2; ++qb)
+        if (last_q[qb] >= 0) mbar_wait(&q_full[qb], (last_q[qb] >> 1) & 1, wait_ns);
+      if (n_steps > 0) mbar_wait(do_full, (n_steps - 1) & 1, wait_ns);
+    }
+    __syncwarp();
+  } else if (warp == 17) {
+    // ------------------------------------- MMA issuer (converged, elected lane)
+    auto wait_all = [&](uint64_t *bar, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, wait_ns));
+    };
+    constexpr uint32_t I_S = make_idesc_bf16(C::BN, C::BM, false);       // S^T, dP^T
+    constexpr uint32_t I_ACC = make_idesc_bf16(C::BN, D, true);          // dV, dK
+    constexpr uint32_t I_DQ = make_idesc_bf16_ab(D, C::BM, true, true);  // dQ^T
+    const uint64_t k_kd = make_smem_desc(sbase + C::OFF_K, 16, 8 * C::SPAN, kLayoutSW128);
+    const uint64_t v_kd = make_smem_desc(sbase + C::OFF_V, 16, 8 * C::SPAN, kLayoutSW128);
+    // K^T as the MN-major A of dQ^T: M = head dim (next 64 columns at +BN*SPAN)
+    const uint64_t k_md =
+        make_smem_desc(sbase + C::OFF_K, C::BN * C::SPAN, 8 * C::SPAN, kLayoutSW128);
+    const uint64_t do_kd = make_smem_desc(sbase + C::OFF_DO, 16, 8 * C::SPAN, kLayoutSW128);
+    const uint64_t do_md =
+        make_smem_desc(sbase + C::OFF_DO, C::BM * C::SPAN, 8 * C::SPAN, kLayoutSW128);
+    // dS^T as the MN-major B of dQ^T: N = queries (next 64 at +DS_CHUNK)
+    const uint64_t ds_md =
+        make_smem_desc(sbase + C::OFF_DS, C::DS_CHUNK, 8 * 128, kLayoutSW128);
+    auto adv = [](uint64_t desc, uint32_t bytes) { return desc + (uint64_t)(bytes >> 4); };
+    // aux K-step: S^T gains -L/scale per query column, dP^T gains -D
+    const uint64_t kaux_d = make_smem_desc(sbase + C::OFF_KAUX, 128, 256, kLayoutNone);
+    const uint64_t vaux_d = make_smem_desc(sbase + C::OFF_VAUX, 128, 256, kLayoutNone);
+    auto qbuf = [&](int s) { return sbase + C::OFF_Q + (s & 1) * C::QBUF_BYTES; };
+    auto k_off = [](int kk, uint32_t rows) {
+      return ((kk * 16) / C::CHUNK) * (rows * C::SPAN) + ((kk * 16) % C::CHUNK) * 2;
+    };
+    // S^T(s) into region A; dP^T(s) into region B (both with the aux K-step)
+    auto issue_s = [&](int s) {
+      const uint64_t q_kd = make_smem_desc(qbuf(s), 16, 8 * C::SPAN, kLayoutSW128);
+      const uint64_t qaux_d = make_smem_desc(qbuf(s) + C::QT_BYTES, 128, 256, kLayoutNone);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_bf16_ss_elect(tmem + C::TM_A, adv(k_kd, k_off(kk, C::BN)),
+                          adv(q_kd, k_off(kk, C::BM)), I_S, kk > 0 ? 1u : 0u);
+      mma_bf16_ss_elect(tmem + C::TM_A, kaux_d, qaux_d, I_S, 1u);
+      mma_commit_elect(s_full);
+    };
+    auto issue_dp = [&](int s) {
+      const uint64_t qaux_d = make_smem_desc(qbuf(s) + C::QT_BYTES, 128, 256, kLayoutNone);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_bf16_ss_elect(tmem + C::TM_B, adv(v_kd, k_off(kk, C::BN)),
+                          adv(do_kd, k_off(kk, C::BM)), I_S, kk > 0 ? 1u : 0u);
+      mma_bf16_ss_elect(tmem + C::TM_B, vaux_d, qaux_d, I_S, 1u);
+      mma_commit_elect(dp_full);
+    };
+    bool ok = wait_all(kv_full, 0);
+    if (ok && n_steps > 0) {
+      ok = wait_all(&q_full[0], 0) && wait_all(do_full, 0);
+      if (ok) {
+        issue_s(0);
+        issue_dp(0);
+      }
+    }
+    for (int s = 0; s < n_steps && ok; ++s) {
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
+      // ---- dV(s) += P^T(s) dO(s)  (dP^T(s) was issued before P(s) was formed)
+      if (!wait_all(p_full, s & 1)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < C::BM / 16; ++kk)
+        mma_bf16_ts_elect(tmem + C::TM_DV, tmem + C::TM_A + C::packed_col(kk),
+                          adv(do_md, kk * 16 * C::SPAN), I_ACC, (s > 0 || kk > 0) ? 1u : 0u);
+      mma_commit_elect(do_empty);  // dO(s) has been read by dP^T(s) and dV(s)
+      // ---- S^T(s+1): region A is free once dV(s) has read P^T(s)
+      if (s + 1 < n_steps) {
+        if (!wait_all(&q_full[(s + 1) & 1], ((s + 1) >> 1) & 1)) { ok = false; break; }
+        issue_s(s + 1);
+      }
+      // ---- dK(s) += dS^T(s) Q(s), then dQ^T(s) = K^T dS^T(s) into region B
+      if (!wait_all(ds_full, s & 1)) { ok = false; break; }
+      tc_fence_after();
+      const uint64_t q_md = make_smem_desc(qbuf(s), C::BM * C::SPAN, 8 * C::SPAN, kLayoutSW128);
+#pragma unroll
+      for (int kk = 0; kk < C::BM / 16; ++kk)
+        mma_bf16_ts_elect(tmem + C::TM_DK, tmem + C::TM_B + C::packed_col(kk),
+                          adv(q_md, kk * 16 * C::SPAN), I_ACC, (s > 0 || kk > 0) ? 1u : 0u);
+      mma_commit_elect(&q_empty[s & 1]);  // Q(s) and its aux rows have been read
+#pragma unroll
+      for (int kk = 0; kk < C::BN / 16; ++kk)
+        mma_bf16_ss_elect(tmem + C::TM_B, adv(k_md, kk * 16 * C::SPAN),
+                          adv(ds_md, kk * 16 * 128), I_DQ, kk > 0 ? 1u : 0u);
+      mma_commit_elect(dq_full);
+      mma_commit_elect(ds_free);
+      // ---- dP^T(s+1) into region B once dQ^T(s) has left it, so that dS(s+1)
+      // can follow P(s+1) without waiting for dV(s+1)
+      if (s + 1 < n_steps) {
+        if (!wait_all(do_full, (s + 1) & 1) || !wait_all(dq_empty, s & 1)) { ok = false; break; }
+        tc_fence_after();
+        issue_dp(s + 1);
+      }
+    }
+    if (!ok) fail();
+    mma_commit_elect(dkdv_full);
+    mma_commit_elect(drain);
+    wait_all(drain, 0);
+    __syncwarp();
+  } else if (warp < 8) {
+    // ------------------------------------------- P and dS, one key per thread
+    // Warpgroup c owns queries [64c, 64c+64) of each step, in two 32-query
+    // halves; each half's bf16 pairs go to the 16 columns at 64c + 16h, inside
+    // the 64 columns this warpgroup read, so neither warpgroup overwrites
+    // columns the other still reads.  P is kept packed for dS = P (dP - D).
+    const int r = threadIdx.x & (C::BN - 1);
+    const int c = warp >> 2;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const int key = kt * C::BN + r;
+    const bool key_ok = key < p.Tk;
+    const float sl2 = p.scale_log2;
+    // dS^T row r of this warpgroup's 64 queries: 128 bytes in chunk c
+    uint8_t *ds_row = smem + C::OFF_DS + c * C::DS_CHUNK + r * 128;
+    bool ok = true;
+    for (int s = 0; s < n_steps; ++s) {
+      ok = __all_sync(0xffffffffu, mbar_wait(s_full, s & 1, wait_ns) && !*abort_flag);
+      if (!ok) break;
+      tc_fence_after();
+      const int q0 = step_qt(s) * C::BM;
+      const bool need_mask = p.causal && (kt * C::BN + C::BN - 1 > q0 + delta);
+      const int lim = key - delta - q0;  // query q (in tile) sees the key iff q >= lim
+      uint32_t pk[32];                   // P of the 64 queries, bf16 pairs
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float sv[32];
+        tmem_ld32_wait(tmem + lane_base + C::TM_A + 64 * c + 32 * h, sv);
+        // S^T already holds S - L/scale (the aux K-step)
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const int q = 64 * c + 32 * h + i;
+          const float2 x = __fmul2_rn(make_float2(sv[i], sv[i + 1]), make_float2(sl2, sl2));
+          float p0 = ex2_approx(x.x);
+          float p1 = ex2_approx(x.y);
+          if (need_mask) {
+            if (q < lim) p0 = 0.f;
+            if (q + 1 < lim) p1 = 0.f;
+          }
+          if (!key_ok) p0 = p1 = 0.f;
+          pk[16 * h + i / 2] = pack_bf16x2(p0, p1);
+        }
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) w[i] = pk[16 * h + i];
+        tmem_st16(tmem + lane_base + C::TM_A + 64 * c + 16 * h, w);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(p_full);
+      // ---- dS = P (dP - D); dP^T already holds dP - D (the aux K-step)
+      ok = __all_sync(0xffffffffu, mbar_wait(dp_full, s & 1, wait_ns) && !*abort_flag);
+      if (!ok) break;
+      tc_fence_after();
+      // the dS^T tile is free once dQ^T(s-1) has read it
+      if (s >= 1) {
+        ok = __all_sync(0xffffffffu, mbar_wait(ds_free, (s - 1) & 1, wait_ns));
+        if (!ok) break;
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float dp[32];
+        tmem_ld32_wait(tmem + lane_base + C::TM_B + 64 * c + 32 * h, dp);
+        uint32_t dw[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const float2 pp = unpack_bf16x2(pk[16 * h + i / 2]);
+          const float2 d = __fmul2_rn(pp, make_float2(dp[i], dp[i + 1]));
+          dw[i / 2] = pack_bf16x2(d.x, d.y);
+        }
+        tmem_st16(tmem + lane_base + C::TM_B + 64 * c + 16 * h, dw);
+        // queries [32h, 32h+32) of this warpgroup are 16-byte units 4h .. 4h+3
+        // of the 128-byte row, swizzled by the row
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int unit = 4 * h + j;
+          *reinterpret_cast<uint4 *>(ds_row + ((unit ^ (r & 7)) << 4)) =
+              make_uint4(dw[4 * j], dw[4 * j + 1], dw[4 * j + 2], dw[4 * j + 3]);
+        }
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(ds_full);
+    }
+    tmem_st_wait();
+    if (!ok) fail();
+    if (n_steps > 0 && ok) {
+      ok = __all_sync(0xffffffffu, mbar_wait(dkdv_full, 0, wait_ns));
+      if (!ok) fail();
+    }
+    if (ok) {
+      // All MMAs have completed (dkdv_full), so the Q buffers are free: dV
+      // (warpgroup 0) and dK times scale (warpgroup 1) go there as bf16 in the
+      // 128-byte-swizzled layout of the K/V tiles (per tile two 64-column
+      // chunks of 128 rows x 128 B) and leave by TMA stores, which also drop
+      // rows past the sequence end.
+      tc_fence_after();
+      uint8_t *out = smem + C::OFF_Q;  // dV chunk 0, 1, then dK chunk 0, 1
+      const uint32_t col = c == 0 ? C::TM_DV : C::TM_DK;
+      const float mul = c == 0 ? 1.f : p.scale;
+#pragma unroll 1
+      for (int cg = 0; cg < D / 32; ++cg) {
+        float v[32];
+        if (n_steps > 0) {
+          tmem_ld32_wait(tmem + lane_base + col + cg * 32, v);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0.f;
+        }
+        // columns [32cg, 32cg+32) are 16-byte units 4(cg%2) .. 4(cg%2)+3 of
+        // row r in chunk cg/2, swizzled by the row
+        uint8_t *row = out + (c * 2 + cg / 2) * (C::BN * C::SPAN) + r * C::SPAN;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int unit = (cg & 1) * 4 + u;
+          *reinterpret_cast<uint4 *>(row + ((unit ^ (r & 7)) << 4)) =
+              make_uint4(pack_bf16x2(v[8 * u] * mul, v[8 * u + 1] * mul),
+                         pack_bf16x2(v[8 * u + 2] * mul, v[8 * u + 3] * mul),
+                         pack_bf16x2(v[8 * u + 4] * mul, v[8 * u + 5] * mul),
+                         pack_bf16x2(v[8 * u + 6] * mul, v[8 * u + 7] * mul));
+        }
+      }
+      fence_proxy_async_smem();
+      named_barrier_sync(1, 2 * C::BN);
+      if (threadIdx.x == 0) {
+        for (int cc = 0; cc < C::NCHUNK; ++cc) {
+          tma_store_3d(&tm_dv, out + cc * (C::BN * C::SPAN), cc * C::CHUNK, kt * C::BN, bkv);
+          tma_store_3d(&tm_dk, out + (C::NCHUNK + cc) * (C::BN * C::SPAN), cc * C::CHUNK,
+                       kt * C::BN, bkv);
+        }
+        bulk_commit_group();
+        bulk_wait_group0();
+      }
+    }
+  } else {
+    // --------------------------- dQ^T of each step, one head-dim column per thread
+    // Warp w drains head-dim columns 32(w%4) .. +31 (its TMEM lanes) for the
+    // queries [64h, 64h+64) of the step and adds each into the fp32
+    // accumulator: one coalesced 128-byte reduction per warp instruction.
+    const int cdim = (warp & 3) * 32 + lane;  // head-dim column == TMEM lane
+    const int h = (warp - 8) >> 2;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    bool ok = true;
+    for (int s = 0; s < n_steps; ++s) {
+      ok = __all_sync(0xffffffffu, mbar_wait(dq_full, s & 1, wait_ns) && !*abort_flag);
+      if (!ok) break;
+      tc_fence_after();
+      float v[64];
+      tmem_ld64_wait(tmem + lane_base + C::TM_B + 64 * h, v);
+      tc_fence_before();
+      mbar_arrive(dq_empty);  // this part of dQ^T(s) has left tensor memory
+      const int bh = b * p.Hq + step_head(s);
+      const int q0 = step_qt(s) * C::BM + 64 * h;
+      const int nq = min(64, p.Tq - q0);
+      float *dst = p.dq_acc + ((size_t)bh * p.Tq + q0) * D + cdim;
+      if (nq == 64) {
+#pragma unroll
+        for (int q = 0; q < 64; ++q) atomicAdd(dst + (size_t)q * D, v[q]);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 64; ++q)
+          if (q < nq) atomicAdd(dst + (size_t)q * D, v[q]);
+      }
+    }
+    if (!ok) fail();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
 // Per query row D_i = dO_i . O_i and the aux row [-L_i/scale, -D_i] (each as
 // a bf16 high and low part) that the backward kernels fold into S^T and dP^T;
 // padding rows (to a multiple of 128) get -1e30 and 0, so their
