@@ -493,7 +493,7 @@ def run_ours(args, rank, world, local_rank):
                 PREFILL.B, PREFILL.Hq, PREFILL.Tq, PREFILL.Tk, PREFILL.d, True)
                 / (bwd_ms / 1e3) / 1e12 / peak_tf, 4),
             "launches": "prep + backward kernel + dQ conversion",
-            "traffic_main_kernel": ncu_traffic("attn_bwd_pipelined_kernel/" + PREFILL.name,
+            "traffic_main_kernel": ncu_traffic("attn_bwd_bm128_kernel/" + PREFILL.name,
                                                source_sha(*BACKWARD_SOURCES)),
         },
         "gpu_launches": K * 3,

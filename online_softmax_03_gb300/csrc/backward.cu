@@ -27,8 +27,7 @@ int launch_main(const attn_host::BwdArgs &a, Kern kern, const attn_dev::BwdParam
     return ATTN_ERR_CUDA;
   const int n_kt = (a.Tk + C::BN - 1) / C::BN;
   const dim3 grid(n_kt, (unsigned)bhk);
-  if constexpr (std::is_same<C, attn_dev::BwdPipeCfg>::value ||
-                std::is_same<C, attn_dev::BwdBm128Cfg>::value) {
+  if constexpr (std::is_same<C, attn_dev::BwdBm128Cfg>::value) {
     // dK and dV leave by TMA stores of the same boxes as K and V
     CUtensorMap tdk, tdv;
     if (!attn_host::encode_tmap_3d_bf16(&tdk, a.dk, D, a.Tk, bhk, C::CHUNK, C::BN, 1, C::SPAN) ||

@@ -11,7 +11,9 @@
 //
 // Loop order: keys outer, as the page describes for FlashAttention-1's
 // backward, so a CTA finishes dK and dV of its key tile in tensor memory
-// and only dQ is accumulated across CTAs.  One CTA (320 threads, one per SM)
+// and only dQ is accumulated across CTAs.  The rest of this comment
+// describes attn_bwd_kernel<D> (d <= 64); d = 128 runs
+// attn_bwd_bm128_kernel, described at its definition.  One CTA (320 threads, one per SM)
 // owns 128 keys of one K/V head and walks every query tile of every query
 // head of that head's group (grouped-query attention); under causal masking
 // it starts at the first query tile that sees its keys.  Per step of 128
@@ -498,439 +500,6 @@ __global__ void __launch_bounds__(320, 1)
 }
 
 // ---------------------------------------------------------------------------
-// d = 128: steps of 64 queries with S^T and dP^T double-buffered in tensor
-// memory, so the tensor core computes the next step's S^T and dP^T while
-// the P/dS threads work on this step, and three stages of Q and dO.  dQ is
-// computed transposed, dQ^T = K^T dS^T (M = d = 128 lanes, one per head-dim
-// column), over the dP^T columns of its buffer once dK has read dS^T; the
-// thread of each head-dim column adds its 64 values straight into the fp32
-// accumulator (one coalesced 128-byte reduction per warp instruction).
-//
-// Tensor memory: buffer b in {0,1}: S^T_b [128b, 128b+64), dP^T_b [128b+64,
-// 128b+128) with dQ^T_b over all 64 columns; the bf16 P^T_b (dS^T_b) of queries
-// [32c, 32c+32) is packed into the 16 columns at 32c of S^T_b (dP^T_b), the
-// columns the fp32 values of those queries came from; dV [256,384); dK
-// [384,512).
-struct BwdPipeCfg {
-  static constexpr int D = 128;
-  static constexpr int BM = 64;                       // queries per step
-  static constexpr int BN = 128;                      // keys per CTA
-  static constexpr int SPAN = 128;
-  static constexpr int CHUNK = 64;
-  static constexpr int NCHUNK = 2;
-  static constexpr uint32_t KV_BYTES = BN * D * 2;    // 32 KB
-  static constexpr uint32_t QT_BYTES = BM * D * 2;    // 16 KB
-  static constexpr uint32_t AUX_BYTES = BM * 32;      // 2 KB: 16 bf16 per query
-  static constexpr uint32_t STAGE_BYTES = 2 * QT_BYTES + AUX_BYTES;  // Q | dO | aux
-  static constexpr int STAGES = 3;
-  static constexpr uint32_t OFF_K = 0;
-  static constexpr uint32_t OFF_V = OFF_K + KV_BYTES;
-  static constexpr uint32_t OFF_STAGE = OFF_V + KV_BYTES;
-  static constexpr uint32_t OFF_DS = OFF_STAGE + STAGES * STAGE_BYTES;  // 2 x [128 keys x 128 B]
-  static constexpr uint32_t DS_BYTES = BN * 128;
-  // constant key-side aux operands: [1, 1, 0, ...] (S^T) and [0, 0, 1, 1, 0, ...] (dP^T)
-  static constexpr uint32_t OFF_KAUX = OFF_DS + 2 * DS_BYTES;
-  static constexpr uint32_t OFF_VAUX = OFF_KAUX + BN * 32;
-  static constexpr uint32_t OFF_BAR = OFF_VAUX + BN * 32;
-  // kv_full, dkdv_full, drain, then per stage q_full, q_empty, then per
-  // buffer s_full, p_full, dq_full, dq_empty, ds_free
-  static constexpr int NBAR = 3 + 2 * STAGES + 5 * 2;
-  static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
-  static constexpr uint32_t TMEM_COLS = 512;
-  __host__ __device__ static constexpr uint32_t tm_s(int b) { return 128 * b; }
-  __host__ __device__ static constexpr uint32_t tm_dp(int b) { return 128 * b + 64; }
-  static constexpr uint32_t TM_DV = 256, TM_DK = 384;
-  // column of the packed bf16 queries [16kk, 16kk+16) within S^T_b / dP^T_b
-  __host__ __device__ static constexpr uint32_t packed_col(int kk) {
-    return (kk / 2) * 32 + (kk % 2) * 8;
-  }
-  static constexpr int THREADS = 448;
-  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-  static_assert(OFF_STAGE % 1024 == 0 && OFF_DS % 1024 == 0, "alignment");
-  static_assert(4 * BN * SPAN <= STAGES * STAGE_BYTES, "dK/dV staging fits the Q/dO stages");
-};
-
-__global__ void __launch_bounds__(448, 1)
-    attn_bwd_pipelined_kernel(const __grid_constant__ CUtensorMap tm_q,
-                              const __grid_constant__ CUtensorMap tm_k,
-                              const __grid_constant__ CUtensorMap tm_v,
-                              const __grid_constant__ CUtensorMap tm_do,
-                              const __grid_constant__ CUtensorMap tm_dk,
-                              const __grid_constant__ CUtensorMap tm_dv,
-                              const BwdParams p) {
-  using C = BwdPipeCfg;
-  constexpr int D = C::D;
-  constexpr int ST = C::STAGES;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t sbase = smem_u32(smem);
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
-  uint64_t *kv_full = bars + 0, *dkdv_full = bars + 1, *drain = bars + 2;
-  uint64_t *q_full = bars + 3, *q_empty = q_full + ST;
-  uint64_t *s_full = q_empty + ST, *p_full = s_full + 2, *dq_full = p_full + 2;
-  uint64_t *dq_empty = dq_full + 2, *ds_free = dq_empty + 2;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const uint64_t wait_ns = p.wait_ns;
-
-  const int kt = blockIdx.x;
-  const int bkv = blockIdx.y;
-  const int b = bkv / p.Hkv;
-  const int g = bkv - b * p.Hkv;
-  const int delta = p.Tk - p.Tq;
-  const int n_qt = p.Tq_pad / C::BM;  // 64-query tiles
-  const int qt_lo = p.causal ? max(0, kt * C::BN - delta) / C::BM : 0;
-  const int n_q = n_qt - qt_lo;
-  const int n_steps = n_q > 0 ? p.group * n_q : 0;
-
-  if (threadIdx.x == 0) {
-    mbar_init(kv_full, 1);
-    mbar_init(dkdv_full, 1);
-    mbar_init(drain, 1);
-    for (int s = 0; s < ST; ++s) {
-      mbar_init(&q_full[s], 1);
-      mbar_init(&q_empty[s], 1);
-    }
-    for (int x = 0; x < 2; ++x) {
-      mbar_init(&s_full[x], 1);
-      mbar_init(&p_full[x], 2 * C::BN);
-      mbar_init(&dq_full[x], 1);
-      mbar_init(&dq_empty[x], 128);
-      mbar_init(&ds_free[x], 1);
-    }
-    *abort_flag = 0;
-    fence_mbar_init();
-    prefetch_tmap(&tm_q);
-    prefetch_tmap(&tm_k);
-    prefetch_tmap(&tm_v);
-    prefetch_tmap(&tm_do);
-  }
-  if (threadIdx.x < C::BN) {
-    // row r of the key-side aux operands, in 8-row x 16-byte core matrices
-    // (core matrix (r / 8, k-half) at (r / 8) * 256 + k-half * 128, row r % 8
-    // at + (r % 8) * 16); bf16 1.0 is 0x3f80
-    const int r = threadIdx.x;
-    const uint32_t off = (r >> 3) * 256 + (r & 7) * 16;
-    *reinterpret_cast<uint4 *>(smem + C::OFF_KAUX + off) = make_uint4(0x3f803f80u, 0u, 0u, 0u);
-    *reinterpret_cast<uint4 *>(smem + C::OFF_KAUX + off + 128) = make_uint4(0u, 0u, 0u, 0u);
-    *reinterpret_cast<uint4 *>(smem + C::OFF_VAUX + off) = make_uint4(0u, 0x3f803f80u, 0u, 0u);
-    *reinterpret_cast<uint4 *>(smem + C::OFF_VAUX + off + 128) = make_uint4(0u, 0u, 0u, 0u);
-    fence_proxy_async_smem();
-  }
-  if (warp == 0) {
-    tmem_alloc(tmem_slot, C::TMEM_COLS);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-
-  auto fail = [&]() {
-    atomicExch(p.status, kBwdStatusTimeout);
-    *abort_flag = 1;
-  };
-  auto step_head = [&](int s) { return g * p.group + s / n_q; };
-  auto step_qt = [&](int s) { return qt_lo + s % n_q; };
-
-  if (warp == 12) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      bool ok = true;
-      int last[ST];
-      for (int s = 0; s < ST; ++s) last[s] = -1;
-      mbar_arrive_expect_tx(kv_full, 2 * C::KV_BYTES);
-      for (int c = 0; c < C::NCHUNK; ++c) {
-        tma_load_3d(smem + C::OFF_K + c * (C::BN * C::SPAN), &tm_k, kv_full, c * C::CHUNK,
-                    kt * C::BN, bkv);
-        tma_load_3d(smem + C::OFF_V + c * (C::BN * C::SPAN), &tm_v, kv_full, c * C::CHUNK,
-                    kt * C::BN, bkv);
-      }
-      for (int s = 0; s < n_steps && ok; ++s) {
-        const int st = s % ST, u = s / ST;
-        if (*abort_flag) { ok = false; break; }
-        if (s >= ST && !mbar_wait(&q_empty[st], (u - 1) & 1, wait_ns)) { ok = false; break; }
-        const int bh = b * p.Hq + step_head(s);
-        const int q0 = step_qt(s) * C::BM;
-        uint8_t *stage = smem + C::OFF_STAGE + st * C::STAGE_BYTES;
-        mbar_arrive_expect_tx(&q_full[st], 2 * C::QT_BYTES + C::AUX_BYTES);
-        for (int c = 0; c < C::NCHUNK; ++c) {
-          tma_load_3d(stage + c * (C::BM * C::SPAN), &tm_q, &q_full[st], c * C::CHUNK, q0, bh);
-          tma_load_3d(stage + C::QT_BYTES + c * (C::BM * C::SPAN), &tm_do, &q_full[st],
-                      c * C::CHUNK, q0, bh);
-        }
-        const size_t aoff = ((size_t)bh * (p.Tq_pad / C::BM) + q0 / C::BM) * C::AUX_BYTES;
-        bulk_load(stage + 2 * C::QT_BYTES, p.aux + aoff, C::AUX_BYTES, &q_full[st]);
-        last[st] = s;
-      }
-      if (!ok) fail();
-      mbar_wait(kv_full, 0, wait_ns);
-      for (int s = 0; s < ST; ++s)
-        if (last[s] >= 0) mbar_wait(&q_full[s], (last[s] / ST) & 1, wait_ns);
-    }
-    __syncwarp();
-  } else if (warp == 13) {
-    // ------------------------------------- MMA issuer (converged, elected lane)
-    {
-      auto wait_all = [&](uint64_t *bar, uint32_t parity) -> bool {
-        return __all_sync(0xffffffffu, mbar_wait(bar, parity, wait_ns));
-      };
-      constexpr uint32_t I_S = make_idesc_bf16(C::BN, C::BM, false);          // S^T, dP^T
-      constexpr uint32_t I_ACC = make_idesc_bf16(C::BN, D, true);             // dV, dK
-      constexpr uint32_t I_DQ = make_idesc_bf16_ab(D, C::BM, true, true);     // dQ^T
-      const uint64_t k_kd = make_smem_desc(sbase + C::OFF_K, 16, 8 * C::SPAN, kLayoutSW128);
-      const uint64_t v_kd = make_smem_desc(sbase + C::OFF_V, 16, 8 * C::SPAN, kLayoutSW128);
-      // K^T as the MN-major A of dQ^T: M = head dim (next 64 columns at +BN*SPAN)
-      const uint64_t k_md =
-          make_smem_desc(sbase + C::OFF_K, C::BN * C::SPAN, 8 * C::SPAN, kLayoutSW128);
-      auto adv = [](uint64_t desc, uint32_t bytes) { return desc + (uint64_t)(bytes >> 4); };
-      // aux K-step: S^T gains -L/scale per query column, dP^T gains -D
-      const uint64_t kaux_d = make_smem_desc(sbase + C::OFF_KAUX, 128, 256, kLayoutNone);
-      const uint64_t vaux_d = make_smem_desc(sbase + C::OFF_VAUX, 128, 256, kLayoutNone);
-      // S^T(s) and dP^T(s) into buffer s & 1
-      auto issue_sdp = [&](int s) {
-        const int x = s & 1;
-        const uint32_t stage = sbase + C::OFF_STAGE + (s % ST) * C::STAGE_BYTES;
-        const uint64_t q_kd = make_smem_desc(stage, 16, 8 * C::SPAN, kLayoutSW128);
-        const uint64_t do_kd = make_smem_desc(stage + C::QT_BYTES, 16, 8 * C::SPAN, kLayoutSW128);
-        const uint64_t qaux_d = make_smem_desc(stage + 2 * C::QT_BYTES, 128, 256, kLayoutNone);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t a_off = ((kk * 16) / C::CHUNK) * (C::BN * C::SPAN) + ((kk * 16) % C::CHUNK) * 2;
-          const uint32_t b_off = ((kk * 16) / C::CHUNK) * (C::BM * C::SPAN) + ((kk * 16) % C::CHUNK) * 2;
-          mma_bf16_ss_elect(tmem + C::tm_s(x), adv(k_kd, a_off), adv(q_kd, b_off), I_S,
-                            kk > 0 ? 1u : 0u);
-        }
-        mma_bf16_ss_elect(tmem + C::tm_s(x), kaux_d, qaux_d, I_S, 1u);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t a_off = ((kk * 16) / C::CHUNK) * (C::BN * C::SPAN) + ((kk * 16) % C::CHUNK) * 2;
-          const uint32_t b_off = ((kk * 16) / C::CHUNK) * (C::BM * C::SPAN) + ((kk * 16) % C::CHUNK) * 2;
-          mma_bf16_ss_elect(tmem + C::tm_dp(x), adv(v_kd, a_off), adv(do_kd, b_off), I_S,
-                            kk > 0 ? 1u : 0u);
-        }
-        mma_bf16_ss_elect(tmem + C::tm_dp(x), vaux_d, qaux_d, I_S, 1u);
-        mma_commit_elect(&s_full[x]);
-      };
-      bool ok = wait_all(kv_full, 0);
-      if (ok && n_steps > 0) {
-        ok = wait_all(&q_full[0], 0);
-        if (ok) issue_sdp(0);
-      }
-      for (int s = 0; s < n_steps && ok; ++s) {
-        const int x = s & 1;
-        const int st = s % ST;
-        if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
-        // the next step's S^T and dP^T into the other buffer, once its
-        // previous dQ^T (step s - 1) has been drained
-        if (s + 1 < n_steps) {
-          if (!wait_all(&q_full[(s + 1) % ST], ((s + 1) / ST) & 1)) { ok = false; break; }
-          if (s >= 1 && !wait_all(&dq_empty[x ^ 1], ((s - 1) >> 1) & 1)) { ok = false; break; }
-          issue_sdp(s + 1);
-        }
-        if (!wait_all(&p_full[x], (s >> 1) & 1)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t stage = sbase + C::OFF_STAGE + st * C::STAGE_BYTES;
-        const uint64_t q_md = make_smem_desc(stage, C::BM * C::SPAN, 8 * C::SPAN, kLayoutSW128);
-        const uint64_t do_md =
-            make_smem_desc(stage + C::QT_BYTES, C::BM * C::SPAN, 8 * C::SPAN, kLayoutSW128);
-        // dV += P^T dO, dK += dS^T Q   (16 queries = 8 columns of packed bf16)
-#pragma unroll
-        for (int kk = 0; kk < C::BM / 16; ++kk)
-          mma_bf16_ts_elect(tmem + C::TM_DV, tmem + C::tm_s(x) + C::packed_col(kk),
-                            adv(do_md, kk * 16 * C::SPAN), I_ACC, (s > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < C::BM / 16; ++kk)
-          mma_bf16_ts_elect(tmem + C::TM_DK, tmem + C::tm_dp(x) + C::packed_col(kk),
-                            adv(q_md, kk * 16 * C::SPAN), I_ACC, (s > 0 || kk > 0) ? 1u : 0u);
-        mma_commit_elect(&q_empty[st]);
-        // dQ^T = K^T dS^T   (16 keys per MMA; B = dS^T rows of 64 queries)
-        const uint64_t ds_md = make_smem_desc(sbase + C::OFF_DS + x * C::DS_BYTES, C::DS_BYTES,
-                                              8 * 128, kLayoutSW128);
-#pragma unroll
-        for (int kk = 0; kk < C::BN / 16; ++kk)
-          mma_bf16_ss_elect(tmem + C::tm_dp(x), adv(k_md, kk * 16 * C::SPAN),
-                            adv(ds_md, kk * 16 * 128), I_DQ, kk > 0 ? 1u : 0u);
-        mma_commit_elect(&dq_full[x]);
-        mma_commit_elect(&ds_free[x]);
-      }
-      if (!ok) fail();
-      mma_commit_elect(dkdv_full);
-      mma_commit_elect(drain);
-      wait_all(drain, 0);
-    }
-    __syncwarp();
-  } else if (warp < 8) {
-    // ------------------------------------------- P and dS, one key per thread
-    // Two warpgroups: warpgroup c takes queries [32c, 32c+32) of each step.
-    const int r = threadIdx.x & (C::BN - 1);
-    const int c = warp >> 2;
-    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const int key = kt * C::BN + r;
-    const bool key_ok = key < p.Tk;
-    const float sl2 = p.scale_log2;
-    bool ok = true;
-    for (int s = 0; s < n_steps; ++s) {
-      const int x = s & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[x], (s >> 1) & 1, wait_ns) && !*abort_flag);
-      if (!ok) break;
-      tc_fence_after();
-      const int q0 = step_qt(s) * C::BM;
-      const bool need_mask = p.causal && (kt * C::BN + C::BN - 1 > q0 + delta);
-      const int lim = key - delta - q0;  // query q (in tile) sees the key iff q >= lim
-      uint8_t *ds_row = smem + C::OFF_DS + x * C::DS_BYTES + r * 128;
-      {
-        float sv[32], dp[32];
-        tmem_ld32_wait(tmem + lane_base + C::tm_s(x) + c * 32, sv);
-        tmem_ld32_wait(tmem + lane_base + C::tm_dp(x) + c * 32, dp);
-        uint32_t pw[16], dw[16];
-        // S^T already holds S - L/scale and dP^T holds dP - D (the aux K-step)
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const int q = c * 32 + i;
-          const float2 x = __fmul2_rn(make_float2(sv[i], sv[i + 1]), make_float2(sl2, sl2));
-          float p0 = ex2_approx(x.x);
-          float p1 = ex2_approx(x.y);
-          if (need_mask) {
-            if (q < lim) p0 = 0.f;
-            if (q + 1 < lim) p1 = 0.f;
-          }
-          if (!key_ok) p0 = p1 = 0.f;
-          const float2 d = __fmul2_rn(make_float2(p0, p1), make_float2(dp[i], dp[i + 1]));
-          pw[i / 2] = pack_bf16x2(p0, p1);
-          dw[i / 2] = pack_bf16x2(d.x, d.y);
-        }
-        tmem_st16(tmem + lane_base + C::tm_s(x) + c * 32, pw);
-        tmem_st16(tmem + lane_base + C::tm_dp(x) + c * 32, dw);
-        // dS^T row: queries [32c, 32c+32) are 16-byte units 4c .. 4c+3 of the
-        // 128-byte row, swizzled by the row; the buffer is free once the dQ^T
-        // MMA of step s - 2 has read it.
-        if (s >= 2) {
-          ok = __all_sync(0xffffffffu, mbar_wait(&ds_free[x], ((s - 2) >> 1) & 1, wait_ns));
-          if (!ok) break;
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int unit = c * 4 + j;
-          *reinterpret_cast<uint4 *>(ds_row + ((unit ^ (r & 7)) << 4)) =
-              make_uint4(dw[4 * j], dw[4 * j + 1], dw[4 * j + 2], dw[4 * j + 3]);
-        }
-      }
-      if (!ok) break;
-      tmem_st_wait();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(&p_full[x]);
-    }
-    tmem_st_wait();
-    if (!ok) fail();
-    if (n_steps > 0 && ok) {
-      ok = __all_sync(0xffffffffu, mbar_wait(dkdv_full, 0, wait_ns));
-      if (!ok) fail();
-    }
-    if (ok) {
-      // All MMAs have completed (dkdv_full), so the Q/dO stages are free: dV
-      // and dK (times scale) go there as bf16 in the 128-byte-swizzled layout
-      // of the K/V tiles (per tile two 64-column chunks of 128 rows x 128 B),
-      // and leave by TMA stores, which also drop rows past the sequence end.
-      tc_fence_after();
-      uint8_t *out = smem + C::OFF_STAGE;  // dV chunk 0, 1, then dK chunk 0, 1
-      {
-        const int which = c;  // warpgroup 0 writes dV, warpgroup 1 dK
-        const uint32_t col = which == 0 ? C::TM_DV : C::TM_DK;
-        const float mul = which == 0 ? 1.f : p.scale;
-#pragma unroll 1
-        for (int cg = 0; cg < D / 32; ++cg) {
-          float v[32];
-          if (n_steps > 0) {
-            tmem_ld32_wait(tmem + lane_base + col + cg * 32, v);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = 0.f;
-          }
-          // columns [32cg, 32cg+32) are 16-byte units 4(cg%2) .. 4(cg%2)+3 of
-          // row r in chunk cg/2, swizzled by the row
-          uint8_t *row = out + (which * 2 + cg / 2) * (C::BN * C::SPAN) + r * C::SPAN;
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int unit = (cg & 1) * 4 + u;
-            *reinterpret_cast<uint4 *>(row + ((unit ^ (r & 7)) << 4)) =
-                make_uint4(pack_bf16x2(v[8 * u] * mul, v[8 * u + 1] * mul),
-                           pack_bf16x2(v[8 * u + 2] * mul, v[8 * u + 3] * mul),
-                           pack_bf16x2(v[8 * u + 4] * mul, v[8 * u + 5] * mul),
-                           pack_bf16x2(v[8 * u + 6] * mul, v[8 * u + 7] * mul));
-          }
-        }
-      }
-      fence_proxy_async_smem();
-      named_barrier_sync(1, 2 * C::BN);
-      if (threadIdx.x == 0) {
-        for (int c = 0; c < C::NCHUNK; ++c) {
-          tma_store_3d(&tm_dv, out + c * (C::BN * C::SPAN), c * C::CHUNK, kt * C::BN, bkv);
-          tma_store_3d(&tm_dk, out + (C::NCHUNK + c) * (C::BN * C::SPAN), c * C::CHUNK,
-                       kt * C::BN, bkv);
-        }
-        bulk_commit_group();
-        bulk_wait_group0();
-      }
-    }
-  } else {
-    // --------------------------- dQ^T of each step, one head-dim column per thread
-    // Thread cdim holds column cdim of the step's dQ (64 queries) and adds it
-    // into the fp32 accumulator with one reduction per query: a warp covers
-    // 32 consecutive head-dim columns, so each instruction is one coalesced
-    // 128-byte reduction, with no shared-memory staging.
-    const int cdim = threadIdx.x - 2 * C::BN;  // head-dim column == TMEM lane
-    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    bool ok = true;
-    for (int s = 0; s < n_steps; ++s) {
-      const int x = s & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(&dq_full[x], (s >> 1) & 1, wait_ns) && !*abort_flag);
-      if (!ok) break;
-      tc_fence_after();
-      float v[64];
-      {
-        float a0[32], a1[32];
-        tmem_ld32_wait(tmem + lane_base + C::tm_dp(x), a0);
-        tmem_ld32_wait(tmem + lane_base + C::tm_dp(x) + 32, a1);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          v[i] = a0[i];
-          v[32 + i] = a1[i];
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(&dq_empty[x]);  // the step's dQ^T has left tensor memory
-      const int bh = b * p.Hq + step_head(s);
-      const int q0 = step_qt(s) * C::BM;
-      const int nq = min(C::BM, p.Tq - q0);
-      float *dst = p.dq_acc + ((size_t)bh * p.Tq + q0) * D + cdim;
-      if (nq == C::BM) {
-#pragma unroll
-        for (int q = 0; q < C::BM; ++q) atomicAdd(dst + (size_t)q * D, v[q]);
-      } else {
-#pragma unroll
-        for (int q = 0; q < C::BM; ++q)
-          if (q < nq) atomicAdd(dst + (size_t)q * D, v[q]);
-      }
-    }
-    if (!ok) fail();
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 0) {
-    tc_fence_after();
-    tmem_dealloc(tmem, C::TMEM_COLS);
-  }
-}
-
-// ---------------------------------------------------------------------------
 // d = 128, 128-query steps: every product is an M = 128, N = 128 MMA (an
 // N = 64 product costs about 50 cycles of the tensor pipe for 32 cycles of
 // work, N = 128 costs its 64).  Tensor memory holds one step: region A
@@ -941,6 +510,11 @@ __global__ void __launch_bounds__(448, 1)
 // dP(s) goes first (once dQ^T(s-1) has left region B), so the P/dS threads
 // form dS(s) right after P(s); S(s+1) runs while they do.  Q (with its aux
 // rows) is double-buffered, dO single-buffered.
+//
+// The fp32 reductions of dQ bound this kernel: every (key tile, 128-query
+// step) pair adds 64 KB into the accumulator, and the GPU's L2 completes
+// fp32 reductions at about 3.3 TB/s whatever the instruction width, so the
+// additions alone take about as long as the whole step.
 //
 // Warps 0-7: P and dS, one key per thread, warpgroup c owning queries
 // [64c, 64c+64); warps 8-15: dQ^T drain, warp w owning TMEM lanes
