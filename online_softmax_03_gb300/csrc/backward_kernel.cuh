@@ -65,6 +65,11 @@
 
 namespace attn_dev {
 
+// The two bf16 halves of a pack_bf16x2 word as fp32 (exact).
+__device__ __forceinline__ float2 unpack_bf16x2(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
 constexpr unsigned int kBwdStatusTimeout = 6;     // ATTN_ERR_DEVICE_TIMEOUT
 constexpr unsigned int kBwdStatusMisaligned = 3;  // ATTN_ERR_MISALIGNED
 

@@ -383,11 +383,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
-// The two bf16 halves of a pack_bf16x2 word as fp32 (exact).
-__device__ __forceinline__ float2 unpack_bf16x2(uint32_t w) {
-  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-}
-
 // ------------------------------------------------- UMMA operand descriptors
 
 // Swizzle modes as encoded in the shared-memory matrix descriptor.  Without
