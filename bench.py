@@ -493,6 +493,14 @@ def run_ours(args, rank, world, local_rank):
                 PREFILL.B, PREFILL.Hq, PREFILL.Tq, PREFILL.Tk, PREFILL.d, True)
                 / (bwd_ms / 1e3) / 1e12 / peak_tf, 4),
             "launches": "prep + backward kernel + dQ conversion",
+            "dq_reduction": {
+                "bound": "fp32 reductions into the dQ accumulator (L2)",
+                "bytes_per_call": acct.backward_dq_reduction_bytes(
+                    PREFILL.B, PREFILL.Hq, PREFILL.Tq, PREFILL.Tk, PREFILL.d, True),
+                "achieved_tb_s_whole_call": round(acct.backward_dq_reduction_bytes(
+                    PREFILL.B, PREFILL.Hq, PREFILL.Tq, PREFILL.Tk, PREFILL.d, True)
+                    / (bwd_ms / 1e3) / 1e12, 3),
+            },
             "traffic_main_kernel": ncu_traffic("attn_bwd_bm128_kernel/" + PREFILL.name,
                                                source_sha(*BACKWARD_SOURCES)),
         },

@@ -37,6 +37,24 @@ def backward_flops(B: int, Hq: int, Tq: int, Tk: int, d: int, causal: bool) -> f
     return f / 2.0 if causal else f
 
 
+def backward_dq_reduction_bytes(B: int, Hq: int, Tq: int, Tk: int, d: int, causal: bool,
+                                key_tile: int = 128, query_tile: int = 128) -> int:
+    """Bytes of fp32 dQ the keys-outer backward adds into its global
+    accumulator: every (key tile, query tile) pair a CTA visits contributes a
+    partial for each query row of the tile that exists (rows past Tq are not
+    added), d fp32 values each.  Under causal masking key tile j visits the
+    query tiles from the first one that sees its first key."""
+    n_kt = -(-Tk // key_tile)
+    n_qt = -(-Tq // query_tile)
+    delta = Tk - Tq
+    rows = 0
+    for j in range(n_kt):
+        lo = max(0, j * key_tile - delta) // query_tile if causal else 0
+        for t in range(lo, n_qt):
+            rows += min(query_tile, Tq - t * query_tile)
+    return B * Hq * rows * d * 4
+
+
 def visible_pairs(Tq: int, Tk: int, causal: bool, window: int = 0) -> int:
     """(row, key) pairs inside the mask of one (batch, head): all Tq*Tk, the
     bottom-right causal triangle, or the causal band of `window` keys."""

@@ -76,3 +76,19 @@ def test_backward_flops_are_five_products():
     assert acc.backward_flops(4, 32, 4096, 4096, 128, True) == 2.5 * acc.attention_flops(
         4, 32, 4096, 4096, 128, True)
     assert acc.backward_flops(1, 1, 3, 5, 2, False) == 5 * 2 * 3 * 5 * 2
+
+
+def test_backward_dq_reduction_bytes():
+    # square causal case: key tile j visits the n - j query tiles from its own
+    # diagonal on, n (n + 1) / 2 pairs of 128 x 128 rows x columns; for the
+    # bench shape this is 4,429,185,024 bytes (ncu counted 138,412,032
+    # 32-byte reduction sectors per backward launch, the same bytes)
+    n = 4096 // 128
+    assert acc.backward_dq_reduction_bytes(4, 32, 4096, 4096, 128, True) == \
+        4 * 32 * (n * (n + 1) // 2) * 128 * 128 * 4 == 138412032 * 32
+    # non-causal: every key tile adds a partial for every query row
+    assert acc.backward_dq_reduction_bytes(2, 3, 200, 300, 64, False) == 2 * 3 * 3 * 200 * 64 * 4
+    # causal with more keys than queries: Tq = 130 (query tiles of 128 and 2
+    # rows), Tk = 300 (delta 170); the first query to see key tile 2 (keys
+    # 256..299) is row 86, in tile 0, so all three key tiles visit all 130 rows
+    assert acc.backward_dq_reduction_bytes(1, 1, 130, 300, 32, True) == 3 * 130 * 32 * 4
