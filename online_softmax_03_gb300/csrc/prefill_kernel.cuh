@@ -616,11 +616,14 @@ __global__ void __launch_bounds__(320, 1)
                                (p.causal && kbase + C::BN - 1 > row0 + delta) ||
                                (kWindow && kbase < tile_lo);
         if (need_mask) {
+          // the row sees the columns [lo, lo + cnt) of this tile: keys from
+          // max(lim_lo, 0) to min(lim, Tk - 1)
+          const int lo = max((kWindow ? max(lim_lo, 0) : 0) - kbase, 0);
+          const int hi = min(min(lim, Tk - 1) - kbase, C::BN - 1);
+          const unsigned cnt = (unsigned)max(hi - lo + 1, 0);
 #pragma unroll
-          for (int c = 0; c < C::BN; ++c) {
-            const int key = kbase + c;
-            if (key > lim || (kWindow && key < lim_lo) || key >= Tk) s[c] = -INFINITY;
-          }
+          for (int c = 0; c < C::BN; ++c)
+            if ((unsigned)(c - lo) >= cnt) s[c] = -INFINITY;
         }
         float mx[8];
 #pragma unroll
