@@ -290,9 +290,11 @@ size_t attn_bwd_workspace_bytes(int B, int Hq, int Tq, int d);
  *   workspace     device scratch of attn_bwd_workspace_bytes(B, Hq, Tq, d)
  *                 bytes, 16-byte aligned, caller-owned (contents ignored)
  *
- * dQ is accumulated in fp32 across key tiles by atomic tensor reductions,
- * so its last bits may differ from run to run (the page's note on the
- * nondeterminism of the atomic backward); dK and dV are deterministic.
+ * dQ is accumulated in fp32 across key tiles by atomic reductions into the
+ * workspace (coalesced global reductions at d = 128, TMA tensor reductions
+ * at d <= 64), so its last bits may differ from run to run (the page's note
+ * on the nondeterminism of the atomic backward); dK and dV are
+ * deterministic.
  * Errors are those of attn_fwd, plus ATTN_ERR_INVALID_ARG for a NULL
  * gradient pointer, ATTN_ERR_MISALIGNED for one not 16-byte aligned, and
  * ATTN_ERR_WORKSPACE.
