@@ -27,7 +27,7 @@ int launch_main(const attn_host::BwdArgs &a, Kern kern, const attn_dev::BwdParam
     return ATTN_ERR_CUDA;
   const int n_kt = (a.Tk + C::BN - 1) / C::BN;
   const dim3 grid(n_kt, (unsigned)bhk);
-  if constexpr (std::is_same<C, attn_dev::BwdBm128Cfg>::value) {
+  if constexpr (std::is_same<C, attn_dev::BwdBm128Cfg<D>>::value) {
     // dK and dV leave by TMA stores of the same boxes as K and V
     CUtensorMap tdk, tdv;
     if (!attn_host::encode_tmap_3d_bf16(&tdk, a.dk, D, a.Tk, bhk, C::CHUNK, C::BN, 1, C::SPAN) ||
@@ -79,9 +79,9 @@ int launch_bwd(const attn_host::BwdArgs &a, unsigned int *status) {
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.wait_ns = a.wait_ns;
   int rc;
-  if constexpr (D == 128)
-    rc = launch_main<D, attn_dev::BwdBm128Cfg>(a, attn_dev::attn_bwd_bm128_kernel, p, dq_acc,
-                                              bhq, bhk, false);
+  if constexpr (D >= 64)
+    rc = launch_main<D, attn_dev::BwdBm128Cfg<D>>(a, attn_dev::attn_bwd_bm128_kernel<D>, p,
+                                                 dq_acc, bhq, bhk, false);
   else
     rc = launch_main<D, attn_dev::BwdCfg<D>>(a, attn_dev::attn_bwd_kernel<D>, p, dq_acc, bhq,
                                              bhk, true);

@@ -525,19 +525,23 @@ __global__ void __launch_bounds__(320, 1)
 // [64c, 64c+64); warps 8-15: dQ^T drain, warp w owning TMEM lanes
 // 32(w%4).. (head-dim columns) for queries [64h, 64h+64), h = (w-8)/4;
 // warp 16: TMA producer; warp 17: MMA issuer (converged, elected lane).
+template <int D_>
 struct BwdBm128Cfg {
-  static constexpr int D = 128;
+  static constexpr int D = D_;
   static constexpr int BM = 128;                      // queries per step
   static constexpr int BN = 128;                      // keys per CTA
   static constexpr int SPAN = 128;
   static constexpr int CHUNK = 64;
-  static constexpr int NCHUNK = 2;
-  static constexpr uint32_t KV_BYTES = BN * D * 2;    // 32 KB
-  static constexpr uint32_t QT_BYTES = BM * D * 2;    // 32 KB
+  static constexpr int NCHUNK = D / CHUNK;
+  static constexpr uint32_t KV_BYTES = BN * D * 2;    // 32 KB at d = 128
+  static constexpr uint32_t QT_BYTES = BM * D * 2;    // 32 KB at d = 128
+  // K^T is the M = 128 A operand of dQ^T whatever d is: at d = 64 the K tile
+  // is followed by 16 KB of zeros standing for head-dim rows 64..127
+  static constexpr uint32_t KREG_BYTES = BN * 128 * 2;
   static constexpr uint32_t AUX_BYTES = BM * 32;      // 4 KB: 16 bf16 per query
   static constexpr uint32_t QBUF_BYTES = QT_BYTES + AUX_BYTES;  // Q | aux, 36 KB
   static constexpr uint32_t OFF_K = 0;
-  static constexpr uint32_t OFF_V = OFF_K + KV_BYTES;
+  static constexpr uint32_t OFF_V = OFF_K + KREG_BYTES;
   static constexpr uint32_t OFF_Q = OFF_V + KV_BYTES;               // 2 buffers
   static constexpr uint32_t OFF_DO = OFF_Q + 2 * QBUF_BYTES;        // 1 buffer
   static constexpr uint32_t OFF_DS = OFF_DO + QT_BYTES;             // dS^T, 2 x 16 KB
@@ -551,7 +555,7 @@ struct BwdBm128Cfg {
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t TM_A = 0, TM_B = 128, TM_DV = 256, TM_DK = 384;
+  static constexpr uint32_t TM_A = 0, TM_B = 128, TM_DV = 256, TM_DK = 256 + D;
   static constexpr int THREADS = 576;
   // column of the packed bf16 queries [16kk, 16kk+16) within region A / B
   __host__ __device__ static constexpr uint32_t packed_col(int kk) {
@@ -561,9 +565,11 @@ struct BwdBm128Cfg {
   static_assert(OFF_Q % 1024 == 0 && QBUF_BYTES % 1024 == 0 && OFF_DO % 1024 == 0 &&
                     OFF_DS % 1024 == 0,
                 "1 KiB aligned swizzled tiles");
-  static_assert(4 * BN * SPAN <= 2 * QBUF_BYTES, "dK/dV staging fits the Q buffers");
+  static_assert(2 * NCHUNK * BN * SPAN <= 2 * QBUF_BYTES, "dK/dV staging fits the Q buffers");
+  static_assert(D == 64 || D == 128, "head dim");
 };
 
+template <int D_>
 __global__ void __launch_bounds__(576, 1)
     attn_bwd_bm128_kernel(const __grid_constant__ CUtensorMap tm_q,
                           const __grid_constant__ CUtensorMap tm_k,
@@ -572,7 +578,7 @@ __global__ void __launch_bounds__(576, 1)
                           const __grid_constant__ CUtensorMap tm_dk,
                           const __grid_constant__ CUtensorMap tm_dv,
                           const BwdParams p) {
-  using C = BwdBm128Cfg;
+  using C = BwdBm128Cfg<D_>;
   constexpr int D = C::D;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -604,7 +610,7 @@ __global__ void __launch_bounds__(576, 1)
   if (threadIdx.x == 0) {
     // p_full and ds_full: all 256 P/dS threads; dq_empty: all 256 dQ threads
     for (int i = 0; i < C::NBAR; ++i)
-      mbar_init(&bars[i], (i == 4 || i == 6) ? 2 * C::BN : i == 8 ? 2 * C::D : 1);
+      mbar_init(&bars[i], (i == 4 || i == 6) ? 2 * C::BN : i == 8 ? 2 * D : 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&tm_q);
@@ -622,6 +628,12 @@ __global__ void __launch_bounds__(576, 1)
     *reinterpret_cast<uint4 *>(smem + C::OFF_KAUX + off + 128) = make_uint4(0u, 0u, 0u, 0u);
     *reinterpret_cast<uint4 *>(smem + C::OFF_VAUX + off) = make_uint4(0u, 0x3f803f80u, 0u, 0u);
     *reinterpret_cast<uint4 *>(smem + C::OFF_VAUX + off + 128) = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+  }
+  if constexpr (D < 128) {
+    // the zero head-dim rows 64..127 of K^T (read by the dQ^T products)
+    for (uint32_t o = threadIdx.x * 16; o < C::KREG_BYTES - C::KV_BYTES; o += C::THREADS * 16)
+      *reinterpret_cast<uint4 *>(smem + C::OFF_K + C::KV_BYTES + o) = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async_smem();
   }
   if (warp == 0) {
@@ -689,7 +701,8 @@ __global__ void __launch_bounds__(576, 1)
     };
     constexpr uint32_t I_S = make_idesc_bf16(C::BN, C::BM, false);       // S^T, dP^T
     constexpr uint32_t I_ACC = make_idesc_bf16(C::BN, D, true);          // dV, dK
-    constexpr uint32_t I_DQ = make_idesc_bf16_ab(D, C::BM, true, true);  // dQ^T
+    // dQ^T: M = 128 head-dim rows (zero rows past d)
+    constexpr uint32_t I_DQ = make_idesc_bf16_ab(128, C::BM, true, true);
     const uint64_t k_kd = make_smem_desc(sbase + C::OFF_K, 16, 8 * C::SPAN, kLayoutSW128);
     const uint64_t v_kd = make_smem_desc(sbase + C::OFF_V, 16, 8 * C::SPAN, kLayoutSW128);
     // K^T as the MN-major A of dQ^T: M = head dim (next 64 columns at +BN*SPAN)
@@ -877,7 +890,7 @@ __global__ void __launch_bounds__(576, 1)
       // chunks of 128 rows x 128 B) and leave by TMA stores, which also drop
       // rows past the sequence end.
       tc_fence_after();
-      uint8_t *out = smem + C::OFF_Q;  // dV chunk 0, 1, then dK chunk 0, 1
+      uint8_t *out = smem + C::OFF_Q;  // dV chunks, then dK chunks
       const uint32_t col = c == 0 ? C::TM_DV : C::TM_DK;
       const float mul = c == 0 ? 1.f : p.scale;
 #pragma unroll 1
@@ -891,7 +904,7 @@ __global__ void __launch_bounds__(576, 1)
         }
         // columns [32cg, 32cg+32) are 16-byte units 4(cg%2) .. 4(cg%2)+3 of
         // row r in chunk cg/2, swizzled by the row
-        uint8_t *row = out + (c * 2 + cg / 2) * (C::BN * C::SPAN) + r * C::SPAN;
+        uint8_t *row = out + (c * C::NCHUNK + cg / 2) * (C::BN * C::SPAN) + r * C::SPAN;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int unit = (cg & 1) * 4 + u;
@@ -923,7 +936,9 @@ __global__ void __launch_bounds__(576, 1)
     const int h = (warp - 8) >> 2;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     bool ok = true;
-    for (int s = 0; s < n_steps; ++s) {
+    // at d = 64 only the warps of TMEM lanes 0..63 have head-dim columns
+    const int my_steps = cdim < D ? n_steps : 0;
+    for (int s = 0; s < my_steps; ++s) {
       ok = __all_sync(0xffffffffu, mbar_wait(dq_full, s & 1, wait_ns) && !*abort_flag);
       if (!ok) break;
       tc_fence_after();
