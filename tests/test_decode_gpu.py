@@ -59,6 +59,17 @@ def test_decode_shapes(B, Hq, Hkv, Tk, d):
     assert_close(o, lse, *oracle_full(q, k, v, False, w.scale), w.name)
 
 
+def test_decode_128k_context():
+    """131,072 cached tokens per sequence (B=2, Hq=32, Hkv=8, d=128): only 16
+    (sequence, K/V head) pairs, so the plan cuts each into tens of splits of
+    a few thousand keys; every row, after the merge, against the oracle."""
+    w = _decode_case(2, 32, 8, 131072, 128, 77)
+    q, k, v = synth.make_inputs(w, DEV)
+    o, lse = binding.decode(q, k, v)
+    torch.cuda.synchronize()
+    assert_close(o, lse, *oracle_full(q, k, v, False, w.scale), w.name)
+
+
 def test_decode_matches_prefill_entry_point_with_one_query():
     w = _decode_case(2, 8, 2, 640, 128, 77)
     q, k, v = synth.make_inputs(w, DEV)

@@ -100,6 +100,19 @@ def test_prefill_4k_sampled_rows_and_finiteness():
     assert torch.equal(o[:, :, 0], v[:, :, 0])
 
 
+def test_prefill_32k_context_sampled_rows():
+    """A 32,768-token causal sequence (B=1, H=8, d=128): the last rows visit
+    256 key tiles and the 1024 items range from 2 to 512 tile products;
+    sampled rows against the oracle and every output finite."""
+    w = synth.Workload("prefill_b1_h8_t32768_d128_causal", 1, 8, 8, 32768, 32768, 128, True,
+                       "normal", 21)
+    q, k, v, o, lse = _run(w)
+    rb, rh, ri = synth.sample_rows(w, 28)
+    o_ref, lse_ref = oracle_rows(q, k, v, w.causal, w.scale, rb, rh, ri)
+    assert_close(o[rb, rh, ri], lse[rb, rh, ri], o_ref, lse_ref, w.name)
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+
+
 def test_outputs_stay_inside_their_buffers():
     """Guard canaries around O and LSE are left untouched."""
     w = synth.Workload("canary", 2, 3, 3, 200, 200, 128, True, "normal", 10)
