@@ -291,8 +291,8 @@ size_t attn_bwd_workspace_bytes(int B, int Hq, int Tq, int d);
  *                 bytes, 16-byte aligned, caller-owned (contents ignored)
  *
  * dQ is accumulated in fp32 across key tiles by atomic reductions into the
- * workspace (coalesced global reductions at d = 128, TMA tensor reductions
- * at d <= 64), so its last bits may differ from run to run (the page's note
+ * workspace (coalesced global reductions at d >= 64, TMA tensor reductions
+ * at d = 32), so its last bits may differ from run to run (the page's note
  * on the nondeterminism of the atomic backward); dK and dV are
  * deterministic.
  * Errors are those of attn_fwd, plus ATTN_ERR_INVALID_ARG for a NULL

@@ -12,7 +12,7 @@
 // Loop order: keys outer, as the page describes for FlashAttention-1's
 // backward, so a CTA finishes dK and dV of its key tile in tensor memory
 // and only dQ is accumulated across CTAs.  The rest of this comment
-// describes attn_bwd_kernel<D> (d <= 64); d = 128 runs
+// describes attn_bwd_kernel<D> (d = 32); d = 64 and d = 128 run
 // attn_bwd_bm128_kernel, described at its definition.  One CTA (320 threads, one per SM)
 // owns 128 keys of one K/V head and walks every query tile of every query
 // head of that head's group (grouped-query attention); under causal masking
