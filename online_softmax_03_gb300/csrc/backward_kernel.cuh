@@ -505,11 +505,13 @@ __global__ void __launch_bounds__(320, 1)
 }
 
 // ---------------------------------------------------------------------------
-// d = 128, 128-query steps: every product is an M = 128, N = 128 MMA (an
-// N = 64 product costs about 50 cycles of the tensor pipe for 32 cycles of
-// work, N = 128 costs its 64).  Tensor memory holds one step: region A
-// [0,128) S^T, then the bf16 P^T packed in place; region B [128,256) dP^T,
-// then the packed dS^T, then dQ^T; dV [256,384); dK [384,512).  Per step the
+// d = 64 and 128, 128-query steps: S^T, dP^T and dQ^T are M = 128, N = 128
+// MMAs (an N = 64 product costs about 50 cycles of the tensor pipe for 32
+// cycles of work, N = 128 costs its 64), dV and dK have N = d.  Tensor memory
+// holds one step: region A [0,128) S^T, then the bf16 P^T packed in place;
+// region B [128,256) dP^T, then the packed dS^T, then dQ^T (128 head-dim
+// rows; at d = 64 rows 64..127 come from zero rows of K^T and are never
+// read); dV [256, 256+d); dK [256+d, 256+2d).  Per step the
 // tensor pipe runs, in issue order,
 //     dP(s)  dV(s)  S(s+1)  dK(s)  dQ^T(s)
 // dP(s) goes first (once dQ^T(s-1) has left region B), so the P/dS threads
@@ -523,8 +525,9 @@ __global__ void __launch_bounds__(320, 1)
 //
 // Warps 0-7: P and dS, one key per thread, warpgroup c owning queries
 // [64c, 64c+64); warps 8-15: dQ^T drain, warp w owning TMEM lanes
-// 32(w%4).. (head-dim columns) for queries [64h, 64h+64), h = (w-8)/4;
-// warp 16: TMA producer; warp 17: MMA issuer (converged, elected lane).
+// 32(w%4).. (head-dim columns; at d = 64 only lanes below 64 have any) for
+// queries [64h, 64h+64), h = (w-8)/4; warp 16: TMA producer; warp 17: MMA
+// issuer (converged, elected lane).
 template <int D_>
 struct BwdBm128Cfg {
   static constexpr int D = D_;
