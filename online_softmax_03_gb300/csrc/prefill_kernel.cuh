@@ -22,8 +22,10 @@
 //              of group t owns row r of tile t = TMEM lane r.  It reads its
 //              row of S_t from tensor memory, masks, updates (m, l), rescales
 //              its row of O_t when needed, and writes P as bf16 back into the
-//              first 64 columns of S_t.  At the end of an item it reads O_t, normalises
-//              and stores its row of O straight to global memory, and LSE.
+//              first 64 columns of S_t.  At the end of an item it reads O_t,
+//              normalises it and passes its row of O through a per-warp
+//              shared-memory staging area, so that the warp's global stores
+//              write whole 128-byte lines; LSE is stored directly.
 //   warp 8     TMA producer: Q tiles (as soon as the previous item's last
 //              S_t no longer needs them) and K and V tiles into a ring of
 //              STAGES shared-memory slots (swizzled boxes), across items.
@@ -125,7 +127,14 @@ struct PrefillCfg {
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_K = OFF_Q + NQ * Q_BYTES;
   static constexpr uint32_t OFF_V = OFF_K + STAGES * KV_BYTES;
-  static constexpr uint32_t OFF_BAR = OFF_V + STAGES * KV_BYTES;
+  // Epilogue staging: each softmax warp turns its 32 rows of O around in its
+  // own area, EPI_ROW bytes of every row per pass (EPI_UNITS 16-byte units).
+  static constexpr int EPI_ROW = (2 * D < 128) ? 2 * D : 128;
+  static constexpr int EPI_UNITS = EPI_ROW / 16;
+  static constexpr int EPI_PASSES = 2 * D / EPI_ROW;
+  static constexpr uint32_t EPI_WARP_BYTES = 32 * EPI_ROW;
+  static constexpr uint32_t OFF_EPI = OFF_V + STAGES * KV_BYTES;
+  static constexpr uint32_t OFF_BAR = OFF_EPI + 8 * EPI_WARP_BYTES;
   // drain, q_full[2], q_empty[2], s_full[2], p_full[2], o_done[2],
   // item_full[2], item_empty[2], then per stage k_full, v_full, k_empty, v_empty
   static constexpr int NBAR = 15 + 4 * STAGES;
@@ -144,6 +153,15 @@ struct PrefillCfg {
   static_assert(D % CHUNK == 0, "head dim must be a whole number of boxes");
   static_assert(Q_BYTES % 1024 == 0 && KV_BYTES % 1024 == 0, "1 KiB regions");
   static_assert(256 + 2 * D <= 512, "tensor memory budget");
+  static_assert(SMEM_BYTES <= 232448u, "shared memory budget");
+  static_assert(EPI_UNITS == 8 || EPI_UNITS == 4, "epilogue swizzle");
+  // The 16-byte unit u of staged row r sits at unit epi_swz(u, r) of the row,
+  // so the eight lanes of a shared-memory phase hit eight different banks
+  // both when a lane writes its own row and when eight lanes read one row
+  // (four and two rows at EPI_UNITS = 4).
+  __device__ __forceinline__ static int epi_swz(int u, int r) {
+    return EPI_UNITS == 8 ? (u ^ (r & 7)) : (u ^ ((r >> 1) & 3));
+  }
 };
 
 // Geometry of one work item, computed identically by every role: query tile
@@ -700,33 +718,63 @@ __global__ void __launch_bounds__(320, 1)
       ++o_cnt;
       tc_fence_after();
       const float inv_l = (l_sum > 0.f) ? 1.f / l_sum : 0.f;
-      uint4 packed[D / 8];
+      // O leaves through this warp's staging area: each thread writes its
+      // own row there, then each global store instruction writes whole
+      // 128-byte lines of 32 / EPI_UNITS rows (a thread storing its own row
+      // touches 32 lines per instruction, and those partial-line stores held
+      // up the next item's TMA loads).  The lane index is read here, not
+      // hoisted out of the item loop, so the staging addresses derived from
+      // it do not stay live across the loop.
+      uint32_t el;
+      asm volatile("mov.u32 %0, %%laneid;" : "=r"(el));
+      const int elane = (int)el;
+      uint8_t *stage = smem + C::OFF_EPI + warp * C::EPI_WARP_BYTES;
+      constexpr int EPI_COLS = C::EPI_ROW / 2;   // bf16 columns per pass
+      constexpr int ROWS_PER_ST = 32 / C::EPI_UNITS;
+      const int un = elane % C::EPI_UNITS;        // 16-byte unit this lane stores
+      // the first row this lane stores, and the rows after it ROWS_PER_ST apart:
+      // [B, Hq, Tq, D] rows, or token-major [total_q, Hq, D] rows when packed
+      const int g0 = row0 + (warp & 3) * 32 + elane / C::EPI_UNITS;
+      const size_t row_step = kVarlen ? (size_t)p.Hq * D : (size_t)D;
+      __nv_bfloat16 *optr = p.o + (kVarlen ? (size_t)(vi.q_base + g0) * p.Hq + it.bh
+                                           : (size_t)it.bh * Tq + g0) * D + un * 8;
+      // the whole row of O_t in one tensor-memory load (one wait)
+      float o[D];
+      if constexpr (D == 128)
+        tmem_ld128_wait(t_o, o);
+      else if constexpr (D == 64)
+        tmem_ld64_wait(t_o, o);
+      else
+        tmem_ld32_wait(t_o, o);
 #pragma unroll
-      for (int cb = 0; cb < D / 32; ++cb) {
-        float o[32];
-        tmem_ld32_wait(t_o + cb * 32, o);
+      for (int ps = 0; ps < C::EPI_PASSES; ++ps) {
 #pragma unroll
-        for (int u4 = 0; u4 < 4; ++u4) {
+        for (int u = 0; u < C::EPI_UNITS; ++u) {
+          const float *x = o + ps * EPI_COLS + u * 8;
           uint4 w;
-          w.x = pack_bf16x2(o[u4 * 8 + 0] * inv_l, o[u4 * 8 + 1] * inv_l);
-          w.y = pack_bf16x2(o[u4 * 8 + 2] * inv_l, o[u4 * 8 + 3] * inv_l);
-          w.z = pack_bf16x2(o[u4 * 8 + 4] * inv_l, o[u4 * 8 + 5] * inv_l);
-          w.w = pack_bf16x2(o[u4 * 8 + 6] * inv_l, o[u4 * 8 + 7] * inv_l);
-          packed[cb * 4 + u4] = w;
+          w.x = pack_bf16x2(x[0] * inv_l, x[1] * inv_l);
+          w.y = pack_bf16x2(x[2] * inv_l, x[3] * inv_l);
+          w.z = pack_bf16x2(x[4] * inv_l, x[5] * inv_l);
+          w.w = pack_bf16x2(x[6] * inv_l, x[7] * inv_l);
+          *reinterpret_cast<uint4 *>(stage + elane * C::EPI_ROW + (C::epi_swz(u, elane) << 4)) = w;
         }
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < C::EPI_UNITS; ++i) {
+          const int rr = i * ROWS_PER_ST + elane / C::EPI_UNITS;  // row in this warp
+          const uint4 w = *reinterpret_cast<const uint4 *>(stage + rr * C::EPI_ROW +
+                                                           (C::epi_swz(un, rr) << 4));
+          if (g0 + i * ROWS_PER_ST < Tq)
+            *reinterpret_cast<uint4 *>(optr + i * ROWS_PER_ST * row_step + ps * EPI_COLS) = w;
+        }
+        __syncwarp();
       }
       // O_t has been read: the next item's first PV_t may overwrite it (it
       // waits for this group's next P_t, published after this fence).
       tc_fence_before();
       if (row_g < Tq) {
-        // [B, Hq, Tq, D] rows, or token-major [total_q, Hq, D] rows when packed
-        const size_t orow_idx = kVarlen ? (size_t)(vi.q_base + row_g) * p.Hq + it.bh
-                                        : (size_t)it.bh * Tq + row_g;
         const size_t lse_idx = kVarlen ? (size_t)it.bh * p.total_q + vi.q_base + row_g
                                        : (size_t)it.bh * Tq + row_g;
-        uint4 *orow = reinterpret_cast<uint4 *>(p.o + orow_idx * D);
-#pragma unroll
-        for (int i = 0; i < D / 8; ++i) orow[i] = packed[i];
         float lse;
         if (l_sum > 0.f)
           lse = (m_used + log2f(l_sum)) * kLn2;

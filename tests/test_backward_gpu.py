@@ -134,3 +134,38 @@ def test_backward_rejects_bad_arguments():
                                                                              device=DEV))
     with pytest.raises(ValueError):
         binding.bwd(q, k, v, o, lse[:, :, :10], do)
+
+
+@pytest.mark.parametrize("d,scale", [(32, 0.05), (64, 0.3), (128, 0.02), (128, 0.25)])
+def test_backward_explicit_scale(d, scale):
+    """A scale other than 1/sqrt(d): the kernels fold -LSE/scale into the
+    score product and multiply dK by the scale, so a slip between the two
+    conventions shows here and not at the default."""
+    w, q, k, v, do = _case(1, 4, 2, 300, 300, d, True, seed=int(scale * 1000) + d)
+    o, lse = binding.fwd(q, k, v, causal=True, scale=scale)
+    dq, dk, dv = binding.bwd(q, k, v, o, lse, do, causal=True, scale=scale)
+    torch.cuda.synchronize()
+    rq, rk, rv, _, _ = ora.attention_backward(synth.bf16_bits(q), synth.bf16_bits(k),
+                                              synth.bf16_bits(v), synth.bf16_bits(do),
+                                              causal=True, scale=scale)
+    for name, a, r in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+        _check(f"{w.name} scale {scale} {name}", a, r)
+
+
+def test_backward_d64_long_sequence_sampled_group():
+    """The 128-query-step kernel at d = 64 over a long causal sequence with
+    GQA: one K/V head's group (its four query heads) against the oracle,
+    since dK and dV of a K/V head sum over exactly those query heads."""
+    w, q, k, v, do = _case(2, 8, 2, 2048, 2048, 64, True, seed=53)
+    o, lse = binding.fwd(q, k, v, causal=True)
+    dq, dk, dv = binding.bwd(q, k, v, o, lse, do, causal=True)
+    torch.cuda.synchronize()
+    b, g = 1, 1
+    qs = lambda x: x[b:b + 1, 4 * g:4 * g + 4]
+    ks = lambda x: x[b:b + 1, g:g + 1]
+    rq, rk, rv, _, _ = ora.attention_backward(
+        synth.bf16_bits(qs(q)), synth.bf16_bits(ks(k)), synth.bf16_bits(ks(v)),
+        synth.bf16_bits(qs(do)), causal=True)
+    _check("d64 long dq", qs(dq), rq)
+    _check("d64 long dk", ks(dk), rk)
+    _check("d64 long dv", ks(dv), rv)
