@@ -179,9 +179,14 @@ struct PrefillItem {
   __device__ __forceinline__ int jend() const { return max(hi0, hi1); }
 };
 
-// Ints per item-ring entry: the item index, then (packed batches) the
-// item's head, pair, query offset and length, key offset and length.
-constexpr int kRingInts = 8;
+// Ints per item-ring entry: the item index, its geometry (bh, bh_kv, q0,
+// lo0, hi0, lo1, hi1), then (packed batches) the sequence's query offset and
+// length and key offset and length.  The producer computes the geometry once
+// (integer divisions by launch parameters) so that the MMA and softmax roles
+// start the next item without that latency on their critical path.
+constexpr int kRingInts = 12;
+// the ring sits at byte 16 of the 128-byte misc area
+static_assert(16 + 2 * kRingInts * 4 <= 128, "item ring size");
 
 // Tile ranges of the two query tiles of the pair starting at row q0 of a
 // sequence with Tq queries and Tk keys.
@@ -351,18 +356,23 @@ __global__ void __launch_bounds__(320, 1)
   // Consumers read the next work item index from the producer's ring
   // (-1 ends the walk).  Returns false if the wait expired.
   // Packed batches: the geometry published with the item.
-  auto take_item = [&](int &fetch, int &idx, VarlenItem &vi) -> bool {
+  auto take_item = [&](int &fetch, int &idx, PrefillItem &it, VarlenItem &vi) -> bool {
     const int k = fetch & 1;
     if (!mbar_wait(&item_full[k], (fetch >> 1) & 1, wait_ns)) return false;
     const volatile int *e = item_ring + k * kRingInts;
     idx = e[0];
+    it.bh = e[1];
+    it.bh_kv = e[2];
+    it.q0 = e[3];
+    it.lo0 = e[4];
+    it.hi0 = e[5];
+    it.lo1 = e[6];
+    it.hi1 = e[7];
     if constexpr (kVarlen) {
-      vi.h = e[1];
-      vi.pair = e[2];
-      vi.q_base = e[3];
-      vi.Tq = e[4];
-      vi.k_base = e[5];
-      vi.Tk = e[6];
+      vi.q_base = e[8];
+      vi.Tq = e[9];
+      vi.k_base = e[10];
+      vi.Tk = e[11];
     }
     ++fetch;
     return true;
@@ -392,20 +402,28 @@ __global__ void __launch_bounds__(320, 1)
         volatile int *ring = item_ring + k * kRingInts;
         ring[0] = idx;
         VarlenItem vi{};
-        if constexpr (kVarlen) {
-          if (idx >= 0) {
+        PrefillItem it{};
+        if (idx >= 0) {
+          if constexpr (kVarlen) {
             vi = varlen_item(p, idx, n_items / p.Hq);
-            ring[1] = vi.h;
-            ring[2] = vi.pair;
-            ring[3] = vi.q_base;
-            ring[4] = vi.Tq;
-            ring[5] = vi.k_base;
-            ring[6] = vi.Tk;
+            it = varlen_prefill_item(p, vi);
+            ring[8] = vi.q_base;
+            ring[9] = vi.Tq;
+            ring[10] = vi.k_base;
+            ring[11] = vi.Tk;
+          } else {
+            it = prefill_item<kWindow>(p, idx);
           }
+          ring[1] = it.bh;
+          ring[2] = it.bh_kv;
+          ring[3] = it.q0;
+          ring[4] = it.lo0;
+          ring[5] = it.hi0;
+          ring[6] = it.lo1;
+          ring[7] = it.hi1;
         }
         mbar_arrive(&item_full[k]);
         if (idx < 0) break;
-        const PrefillItem it = kVarlen ? varlen_prefill_item(p, vi) : prefill_item<kWindow>(p, idx);
         for (int t = 0; t < C::NQ && ok; ++t) {
           if (!it.has(t)) continue;
           // Q_t is free once the previous item's last S_t has completed.
@@ -508,10 +526,10 @@ __global__ void __launch_bounds__(320, 1)
       for (int fetch = 0; ok;) {
         int idx = -1;
         VarlenItem vi;
-        if (!__all_sync(0xffffffffu, take_item(fetch, idx, vi))) { ok = false; break; }
+        PrefillItem it;
+        if (!__all_sync(0xffffffffu, take_item(fetch, idx, it, vi))) { ok = false; break; }
         if (lane == 0) mbar_arrive(&item_empty[(fetch - 1) & 1]);
         if (idx < 0) break;
-        const PrefillItem it = kVarlen ? varlen_prefill_item(p, vi) : prefill_item<kWindow>(p, idx);
         const int jb = kWindow ? it.jbeg() : 0, je = it.jend();
         // S_t of K/V tile jj in stage sj, the first S of tile t's range.
         auto start_tile = [&](const int t, int &q_cnt, const int sj, const int jj) -> bool {
@@ -601,12 +619,12 @@ __global__ void __launch_bounds__(320, 1)
     for (int fetch = 0; ok;) {
       int idx = -1;
       VarlenItem vi;
-      ok = __all_sync(0xffffffffu, take_item(fetch, idx, vi));
+      PrefillItem it;
+      ok = __all_sync(0xffffffffu, take_item(fetch, idx, it, vi));
       if (!ok) break;
       __syncwarp();
       if (lane == 0) mbar_arrive(&item_empty[(fetch - 1) & 1]);
       if (idx < 0) break;
-      const PrefillItem it = kVarlen ? varlen_prefill_item(p, vi) : prefill_item<kWindow>(p, idx);
       if (!it.has(t)) continue;
       const int Tq = kVarlen ? vi.Tq : p.Tq;
       const int Tk = kVarlen ? vi.Tk : p.Tk;
