@@ -17,8 +17,10 @@
  *
  * Conventions shared by every entry point
  * --------------------------------------
- *  - All tensor pointers are DEVICE pointers owned by the caller.  The
- *    library never allocates, frees or retains them.
+ *  - All tensor pointers are DEVICE pointers owned by the caller, except the
+ *    host buffers of attn_fwd_host / attn_decode_host.  The library never
+ *    allocates, frees or retains memory (those two create and release
+ *    their own streams and events).
  *  - bf16 tensors are dense and row-major:
  *        q [B, Hq, Tq, d]      k, v [B, Hkv, Tk, d]      o [B, Hq, Tq, d]
  *    lse is fp32 [B, Hq, Tq] and holds the natural-log log-sum-exp of the
@@ -303,6 +305,49 @@ int attn_bwd(const void *q, const void *k, const void *v, const void *o, const f
              const void *dout, void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int Tq,
              int Tk, int d, int causal, float scale, void *workspace, size_t workspace_bytes,
              void *stream);
+
+/*
+ * attn_fwd_host / attn_decode_host -- the same operations on HOST buffers.
+ *
+ * The exception to the device-pointer rule above: q, k, v (k_cache,
+ * v_cache) are read from, and o, lse written to, HOST memory in the layouts
+ * given above.  The buffers should be page-locked (cudaHostAlloc or
+ * cudaHostRegister); pageable memory works but its copies do not overlap.
+ * They must stay valid and unmodified until `stream` has completed the call.
+ *
+ *   workspace        DEVICE scratch of attn_fwd_host_workspace_bytes(...)
+ *                    (attn_decode_host_workspace_bytes(...)) bytes,
+ *                    256-byte aligned, caller-owned; it receives the device
+ *                    copies of every input and output (and, for decode, the
+ *                    split partials of attn_decode)
+ *   other arguments  as for attn_fwd (attn_decode)
+ *
+ * The call splits the problem into up to 16 chunks of whole (batch, K/V
+ * head) slices and overlaps, through two auxiliary streams and events that
+ * it creates and releases itself, the host-to-device copies of one chunk,
+ * the kernels of the previous one (attn_fwd / attn_decode on the chunk's
+ * part of the workspace) and the device-to-host copies of the one before.
+ * attn_fwd_host's results are bit-identical to copying the whole problem in
+ * and calling attn_fwd once (every query row is computed the same way
+ * whatever else the launch holds); attn_decode_host's agree with
+ * attn_decode to rounding, since attn_decode chooses its number of key
+ * splits from the number of sequences in a launch.  `stream` waits for its earlier work before
+ * the first copy and completes only after the last copy out, so
+ * synchronising `stream` makes o and lse valid in host memory.
+ *
+ * Errors: those of attn_fwd (attn_decode) checked on the host before any
+ * CUDA call, ATTN_ERR_WORKSPACE for a missing, misaligned or short
+ * workspace, ATTN_ERR_CUDA if a copy, a stream or an event cannot be set
+ * up.  A failure part-way leaves o and lse partly written.
+ */
+size_t attn_fwd_host_workspace_bytes(int B, int Hq, int Hkv, int Tq, int Tk, int d);
+int attn_fwd_host(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                  int Hq, int Hkv, int Tq, int Tk, int d, int causal, float scale,
+                  void *workspace, size_t workspace_bytes, void *stream);
+size_t attn_decode_host_workspace_bytes(int B, int Hq, int Hkv, int Tk, int d);
+int attn_decode_host(const void *q, const void *k_cache, const void *v_cache, void *o,
+                     float *lse, int B, int Hq, int Hkv, int Tk, int d, float scale,
+                     void *workspace, size_t workspace_bytes, void *stream);
 
 /* Human-readable name of a status code (never NULL). */
 const char *attn_status_string(int status);

@@ -70,6 +70,16 @@ def load_library():
             lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f,
                                      vp, ctypes.c_size_t, vp]
             lib.attn_bwd.restype = i
+            lib.attn_fwd_host_workspace_bytes.argtypes = [i, i, i, i, i, i]
+            lib.attn_fwd_host_workspace_bytes.restype = ctypes.c_size_t
+            lib.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp,
+                                          ctypes.c_size_t, vp]
+            lib.attn_fwd_host.restype = i
+            lib.attn_decode_host_workspace_bytes.argtypes = [i, i, i, i, i]
+            lib.attn_decode_host_workspace_bytes.restype = ctypes.c_size_t
+            lib.attn_decode_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp,
+                                             ctypes.c_size_t, vp]
+            lib.attn_decode_host.restype = i
             lib.attn_status_string.argtypes = [i]
             lib.attn_status_string.restype = ctypes.c_char_p
             lib.attn_device_status.argtypes = [vp, ctypes.POINTER(i)]
@@ -133,6 +143,26 @@ def attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Tq, Tk, d, causal, s
                                    causal, scale, workspace, workspace_bytes, stream)
 
 
+def attn_fwd_host_workspace_bytes(B, Hq, Hkv, Tq, Tk, d) -> int:
+    return load_library().attn_fwd_host_workspace_bytes(B, Hq, Hkv, Tq, Tk, d)
+
+
+def attn_fwd_host(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, causal, scale, workspace,
+                  workspace_bytes, stream) -> int:
+    return load_library().attn_fwd_host(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, causal, scale,
+                                        workspace, workspace_bytes, stream)
+
+
+def attn_decode_host_workspace_bytes(B, Hq, Hkv, Tk, d) -> int:
+    return load_library().attn_decode_host_workspace_bytes(B, Hq, Hkv, Tk, d)
+
+
+def attn_decode_host(q, k_cache, v_cache, o, lse, B, Hq, Hkv, Tk, d, scale, workspace,
+                     workspace_bytes, stream) -> int:
+    return load_library().attn_decode_host(q, k_cache, v_cache, o, lse, B, Hq, Hkv, Tk, d,
+                                           scale, workspace, workspace_bytes, stream)
+
+
 def attn_status_string(status: int) -> str:
     return load_library().attn_status_string(status).decode()
 
@@ -162,6 +192,30 @@ def _check_tensor(t, name, ndim):
         raise TypeError(f"{name} must be bfloat16")
     if t.dim() != ndim or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous {ndim}-d tensor")
+
+
+def _check_host_tensor(t, name, ndim):
+    import torch
+
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cpu" or not t.is_pinned():
+        raise ValueError(f"{name} must be a page-locked (pinned) CPU tensor")
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16")
+    if t.dim() != ndim or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {ndim}-d tensor")
+
+
+def _host_workspace(n, workspace, device):
+    import torch
+
+    if n == 0:
+        raise ValueError("invalid sizes")
+    if workspace is None:
+        # torch's caching allocator returns 512-byte aligned blocks
+        workspace = torch.empty(n, dtype=torch.uint8, device=device)
+    return workspace
 
 
 def _stream_handle(stream):
@@ -200,6 +254,61 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None,
         where = "attn_fwd_window"
     if rc != ATTN_OK:
         raise AttnError(rc, where)
+    return out, lse
+
+
+def fwd_host(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+             workspace=None, stream=None, device="cuda"):
+    """O, LSE from pinned host tensors through attn_fwd_host: q [B,Hq,Tq,d],
+    k/v [B,Hkv,Tk,d] in page-locked CPU memory; O and LSE come back in pinned
+    CPU tensors, valid once `stream` has been synchronised."""
+    import torch
+
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check_host_tensor(t, n, 4)
+    B, Hq, Tq, d = q.shape
+    Bk, Hkv, Tk, dk = k.shape
+    if (Bk, dk) != (B, d) or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("inconsistent q/k/v shapes")
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+    if lse is None:
+        lse = torch.empty((B, Hq, Tq), dtype=torch.float32).pin_memory()
+    workspace = _host_workspace(attn_fwd_host_workspace_bytes(B, Hq, Hkv, Tq, Tk, d),
+                                workspace, device)
+    rc = attn_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                       B, Hq, Hkv, Tq, Tk, d, int(bool(causal)),
+                       0.0 if scale is None else float(scale), workspace.data_ptr(),
+                       workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_host")
+    return out, lse
+
+
+def decode_host(q, k_cache, v_cache, scale: float | None = None, out=None, lse=None,
+                workspace=None, stream=None, device="cuda"):
+    """O, LSE for one query token per sequence from pinned host tensors
+    through attn_decode_host (q [B,Hq,1,d], caches [B,Hkv,Tk,d])."""
+    import torch
+
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _check_host_tensor(t, n, 4)
+    B, Hq, Tq, d = q.shape
+    Bk, Hkv, Tk, dk = k_cache.shape
+    if Tq != 1 or (Bk, dk) != (B, d) or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("decode expects q [B,Hq,1,d] and caches [B,Hkv,Tk,d]")
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+    if lse is None:
+        lse = torch.empty((B, Hq, 1), dtype=torch.float32).pin_memory()
+    workspace = _host_workspace(attn_decode_host_workspace_bytes(B, Hq, Hkv, Tk, d),
+                                workspace, device)
+    rc = attn_decode_host(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), out.data_ptr(),
+                          lse.data_ptr(), B, Hq, Hkv, Tk, d,
+                          0.0 if scale is None else float(scale), workspace.data_ptr(),
+                          workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_decode_host")
     return out, lse
 
 

@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libattn.so")
-SOURCES = ("api.cu", "prefill.cu", "decode.cu", "decode_noalloc.cu", "backward.cu")
+SOURCES = ("api.cu", "prefill.cu", "decode.cu", "decode_noalloc.cu", "backward.cu", "host_stream.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

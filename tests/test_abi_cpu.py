@@ -222,3 +222,95 @@ def test_library_has_no_oracle_dependency():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 with open(os.path.join(dirpath, f)) as fh:
                     assert not pat.search(fh.read()), f
+
+
+# ---------------------------------------------------- host-buffer entry points
+
+def test_host_workspace_bytes(lib):
+    # device copies of q, k, v, o (bf16) and lse (fp32), each region rounded
+    # up to 256 bytes
+    qb, kb, lb = 4 * 32 * 4096 * 128 * 2, 4 * 32 * 4096 * 128 * 2, 4 * 32 * 4096 * 4
+    assert binding.attn_fwd_host_workspace_bytes(4, 32, 32, 4096, 4096, 128) == 2 * qb + 2 * kb + lb
+    r = lambda x: (x + 255) // 256 * 256
+    assert binding.attn_fwd_host_workspace_bytes(1, 2, 1, 3, 5, 32) == \
+        2 * r(2 * 3 * 32 * 2) + 2 * r(5 * 32 * 2) + r(2 * 3 * 4)
+    assert binding.attn_fwd_host_workspace_bytes(1, 6, 4, 8, 8, 64) == 0
+    assert binding.attn_fwd_host_workspace_bytes(1, 4, 4, 8, 8, 48) == 0
+    # decode: the same device copies plus attn_decode's split partials
+    part = binding.attn_decode_workspace_bytes(64, 32, 8, 8192, 128)
+    assert binding.attn_decode_host_workspace_bytes(64, 32, 8, 8192, 128) == \
+        2 * r(64 * 32 * 128 * 2) + 2 * r(64 * 8 * 8192 * 128 * 2) + r(64 * 32 * 4) + r(part)
+    assert binding.attn_decode_host_workspace_bytes(0, 32, 8, 8192, 128) == 0
+
+
+HW = 0x100000  # fake 256-byte aligned device workspace
+
+
+def _fwd_host(**kw):
+    a = dict(q=Q, k=K, v=V, o=O, lse=L, B=1, Hq=4, Hkv=2, Tq=8, Tk=16, d=64, causal=1,
+             scale=0.0, ws=HW, ws_bytes=1 << 30)
+    a.update(kw)
+    return binding.attn_fwd_host(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["Hq"],
+                                 a["Hkv"], a["Tq"], a["Tk"], a["d"], a["causal"], a["scale"],
+                                 a["ws"], a["ws_bytes"], None)
+
+
+def _decode_host(**kw):
+    a = dict(q=Q, k=K, v=V, o=O, lse=L, B=2, Hq=8, Hkv=2, Tk=100, d=128, scale=0.0,
+             ws=HW, ws_bytes=1 << 30)
+    a.update(kw)
+    return binding.attn_decode_host(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"],
+                                    a["Hq"], a["Hkv"], a["Tk"], a["d"], a["scale"], a["ws"],
+                                    a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), binding.ATTN_ERR_INVALID_ARG),
+    (dict(lse=None), binding.ATTN_ERR_INVALID_ARG),
+    (dict(B=0), binding.ATTN_ERR_INVALID_ARG),
+    (dict(Hq=6, Hkv=4), binding.ATTN_ERR_INVALID_ARG),
+    (dict(Tq=17, Tk=16), binding.ATTN_ERR_INVALID_ARG),
+    (dict(causal=2), binding.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), binding.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), binding.ATTN_ERR_INVALID_ARG),
+    (dict(scale=-0.5), binding.ATTN_ERR_INVALID_ARG),
+    (dict(d=96), binding.ATTN_ERR_UNSUPPORTED),
+    (dict(ws=None), binding.ATTN_ERR_WORKSPACE),
+    (dict(ws=HW + 16), binding.ATTN_ERR_WORKSPACE),
+    (dict(ws_bytes=1024), binding.ATTN_ERR_WORKSPACE),
+])
+def test_fwd_host_rejects_bad_arguments_on_the_host(lib, kw, code):
+    assert _fwd_host(**kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(k=None), binding.ATTN_ERR_INVALID_ARG),
+    (dict(Tk=0), binding.ATTN_ERR_INVALID_ARG),
+    (dict(Hq=8, Hkv=3), binding.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), binding.ATTN_ERR_INVALID_ARG),
+    (dict(d=16), binding.ATTN_ERR_UNSUPPORTED),
+    (dict(ws=None), binding.ATTN_ERR_WORKSPACE),
+    (dict(ws_bytes=4096), binding.ATTN_ERR_WORKSPACE),
+])
+def test_decode_host_rejects_bad_arguments_on_the_host(lib, kw, code):
+    assert _decode_host(**kw) == code
+
+
+def test_host_entry_points_with_valid_arguments_reach_cuda(lib):
+    # Past validation the first CUDA call (a stream) fails without a GPU.
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("fake pointers must never reach a real device")
+    assert _fwd_host() == binding.ATTN_ERR_CUDA
+    assert _decode_host() == binding.ATTN_ERR_CUDA
+
+
+def test_host_wrappers_require_pinned_cpu_tensors():
+    import torch
+
+    x = torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16)  # pageable
+    with pytest.raises(ValueError):
+        binding.fwd_host(x, x, x)
+    with pytest.raises(ValueError):
+        binding.decode_host(x[:, :, :1], x, x)
