@@ -624,6 +624,9 @@ int oracle_attn_varlen(const void *q, const void *k, const void *v, int in_type,
  *   dS    = P o (dP - D)        (o: elementwise; D broadcast along rows)
  *   dQ    = scale dS K,   dK = scale dS^T Q
  *
+ * The mask is the forward's: causal, and with window > 0 also the sliding
+ * window of "4.2 FlashAttention I", Exercise 4 (masked entries have P = 0,
+ * so they carry no gradient).
  * For every (b, h) the full Tq x Tk matrices S, P, dP, dS are materialised.
  * Under grouped-query attention K/V head g serves query heads
  * g*group .. g*group+group-1, so dK_g and dV_g sum their contributions.
@@ -633,9 +636,9 @@ int oracle_attn_varlen(const void *q, const void *k, const void *v, int in_type,
  */
 int oracle_attn_bwd_dense(const void *q, const void *k, const void *v, const void *dout,
                           int in_type, int B, int Hq, int Hkv, int Tq, int Tk, int d,
-                          int causal, double scale, double *dq, double *dk, double *dv,
-                          double *o_out, double *lse_out) {
-  int rc = check_shape(B, Hq, Hkv, Tq, Tk, d, causal, 0);
+                          int causal, int window, double scale, double *dq, double *dk,
+                          double *dv, double *o_out, double *lse_out) {
+  int rc = check_shape(B, Hq, Hkv, Tq, Tk, d, causal, window);
   if (rc) return rc;
   const int group = Hq / Hkv;
   int status = ORACLE_OK;
@@ -671,7 +674,7 @@ int oracle_attn_bwd_dense(const void *q, const void *k, const void *v, const voi
           double *Pi = &P[(size_t)i * Tk];
           double m = -INFINITY;
           for (int j = 0; j < Tk; ++j) {
-            if (!visible(i, j, Tq, Tk, causal, 0)) {
+            if (!visible(i, j, Tq, Tk, causal, window)) {
               Pi[j] = -INFINITY;
               continue;
             }

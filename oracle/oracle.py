@@ -72,7 +72,7 @@ def _load():
             lib.oracle_attn_varlen.argtypes = [vp, vp, vp, ip, vp, vp, ip, ip, ip, ip,
                                                ip, ip, ip, dp, vp, vp]
             lib.oracle_attn_bwd_dense.argtypes = [vp, vp, vp, vp, ip, ip, ip, ip, ip, ip, ip,
-                                                  ip, dp, vp, vp, vp, vp, vp]
+                                                  ip, ip, dp, vp, vp, vp, vp, vp]
             lib.oracle_attn_bwd_blocked.argtypes = [vp, vp, vp, vp, ip, vp, vp, ip, ip, ip,
                                                     ip, ip, ip, ip, dp, ip, ip, vp, vp, vp]
             for f in (lib.oracle_attn_dense, lib.oracle_attn_rows,
@@ -259,10 +259,11 @@ def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, causal=False, scale=No
     return o, lse
 
 
-def attention_backward(q, k, v, dout, causal=False, scale=None):
+def attention_backward(q, k, v, dout, causal=False, scale=None, window=0):
     """Gradients of attention from the plain definition (S, P, dP, dS
     materialised).  q, dout [B,Hq,Tq,d]; k, v [B,Hkv,Tk,d]; float64 or bf16
-    bits, all of one type.  Returns (dq, dk, dv, o, lse) in float64."""
+    bits, all of one type.  window > 0 (causal only) applies the forward's
+    sliding-window mask.  Returns (dq, dk, dv, o, lse) in float64."""
     B, Hq, Hkv, Tq, Tk, d = _shapes(q, k, v)
     q, k, v, t = _inputs(q, k, v)
     do, td = _as_input(dout)
@@ -275,8 +276,8 @@ def attention_backward(q, k, v, dout, causal=False, scale=None):
     o = np.empty((B, Hq, Tq, d), np.float64)
     lse = np.empty((B, Hq, Tq), np.float64)
     rc = _load().oracle_attn_bwd_dense(_ptr(q), _ptr(k), _ptr(v), _ptr(do), t, B, Hq, Hkv, Tq,
-                                       Tk, d, int(bool(causal)), scale, _ptr(dq), _ptr(dk),
-                                       _ptr(dv), _ptr(o), _ptr(lse))
+                                       Tk, d, int(bool(causal)), int(window), scale, _ptr(dq),
+                                       _ptr(dk), _ptr(dv), _ptr(o), _ptr(lse))
     _check(rc)
     return dq, dk, dv, o, lse
 

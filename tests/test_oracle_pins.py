@@ -652,3 +652,56 @@ def test_backward_bf16_inputs_match_the_upcast_f64_inputs():
     b = ora.attention_backward(up(q), up(k), up(v), up(do), causal=True)
     for x, y in zip(a, b):
         np.testing.assert_array_equal(x, y)
+
+
+# --- backward under the sliding window ("4.2 FlashAttention I", Exercise 4:
+# query i sees keys i - W < j <= i; the backward inherits the forward's mask)
+
+@pytest.mark.parametrize("Tq,Tk,Hq,Hkv,window", [(9, 9, 2, 2, 3), (7, 12, 4, 2, 4), (6, 6, 1, 1, 1)])
+def test_window_backward_matches_finite_differences(Tq, Tk, Hq, Hkv, window):
+    """Central differences of sum(dO * O) through the windowed forward
+    definition, every coordinate of a small problem (GQA and Tq < Tk
+    included)."""
+    B, d = 1, 4
+    q, k, v = _rand((B, Hq, Tq, d), 180), _rand((B, Hkv, Tk, d), 181), _rand((B, Hkv, Tk, d), 182)
+    do = _rand((B, Hq, Tq, d), 183)
+    dq, dk, dv, o, lse = ora.attention_backward(q, k, v, do, causal=True, window=window)
+    o_fwd, lse_fwd, _ = ora.attention_dense(q, k, v, causal=True, window=window)
+    np.testing.assert_allclose(o, o_fwd, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lse, lse_fwd, rtol=0, atol=1e-14)
+    loss = lambda qq, kk, vv: float(
+        (do * ora.attention_dense(qq, kk, vv, causal=True, window=window)[0]).sum())
+    for idx in np.ndindex(q.shape):
+        assert abs(_fd_grad(lambda x: loss(x, k, v), q, idx) - dq[idx]) < 1e-7
+    for idx in np.ndindex(k.shape):
+        assert abs(_fd_grad(lambda x: loss(q, x, v), k, idx) - dk[idx]) < 1e-7
+        assert abs(_fd_grad(lambda x: loss(q, k, x), v, idx) - dv[idx]) < 1e-7
+
+
+def test_window_backward_reduces_to_causal_and_to_the_diagonal():
+    """A window of at least Tk keys is the causal mask (identical results);
+    a window of one key leaves each query only the key at its own position,
+    so O_i = V_{i+Tk-Tq}, P is that one-hot row, dS = P (dO.V - dO.O) = 0
+    (dQ = dK = 0) and dV_j sums dO over the query rows (and query heads) at
+    position j."""
+    B, Hq, Hkv, Tq, Tk, d = 2, 4, 2, 7, 11, 8
+    q, k, v = _rand((B, Hq, Tq, d), 184), _rand((B, Hkv, Tk, d), 185), _rand((B, Hkv, Tk, d), 186)
+    do = _rand((B, Hq, Tq, d), 187)
+    full = ora.attention_backward(q, k, v, do, causal=True)
+    wide = ora.attention_backward(q, k, v, do, causal=True, window=Tk)
+    for a, b in zip(full, wide):
+        np.testing.assert_array_equal(a, b)
+    dq, dk, dv, o, _ = ora.attention_backward(q, k, v, do, causal=True, window=1)
+    delta, G = Tk - Tq, Hq // Hkv
+    np.testing.assert_allclose(o, np.repeat(v, G, axis=1)[:, :, delta:], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(dq, 0.0, atol=1e-15)
+    np.testing.assert_allclose(dk, 0.0, atol=1e-15)
+    want = np.zeros_like(dv)
+    want[:, :, delta:] = do.reshape(B, Hkv, G, Tq, d).sum(axis=2)
+    np.testing.assert_allclose(dv, want, rtol=0, atol=1e-15)
+
+
+def test_window_backward_rejects_a_window_without_causal():
+    q = _rand((1, 1, 4, 4), 188)
+    with pytest.raises(ValueError):
+        ora.attention_backward(q, q, q, q, causal=False, window=2)
