@@ -307,6 +307,24 @@ int attn_bwd(const void *q, const void *k, const void *v, const void *o, const f
              void *stream);
 
 /*
+ * attn_bwd_window -- gradients of attn_fwd_window.
+ *
+ * As attn_bwd with the causal mask, and each query's probabilities confined
+ * to its `window` most recent keys (p - window < j <= p, p = i + Tk - Tq;
+ * "4.2 FlashAttention I", Exercise 4): masked entries have P = 0 and carry
+ * no gradient, so every K/V tile only visits the query tiles whose window
+ * reaches it.  o and lse must be attn_fwd_window's outputs for the same
+ * window.  Keys that no query sees get zero dk and dv.
+ *   window    number of keys each query sees (>= 1)
+ * Other arguments, layouts, workspace and errors are those of attn_bwd;
+ * window < 1 or Tq > Tk return ATTN_ERR_INVALID_ARG.
+ */
+int attn_bwd_window(const void *q, const void *k, const void *v, const void *o,
+                    const float *lse, const void *dout, void *dq, void *dk, void *dv, int B,
+                    int Hq, int Hkv, int Tq, int Tk, int d, int window, float scale,
+                    void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * attn_fwd_host / attn_decode_host -- the same operations on HOST buffers.
  *
  * The exception to the device-pointer rule above: q, k, v (k_cache,

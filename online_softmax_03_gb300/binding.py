@@ -70,6 +70,8 @@ def load_library():
             lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f,
                                      vp, ctypes.c_size_t, vp]
             lib.attn_bwd.restype = i
+            lib.attn_bwd_window.argtypes = lib.attn_bwd.argtypes
+            lib.attn_bwd_window.restype = i
             lib.attn_fwd_host_workspace_bytes.argtypes = [i, i, i, i, i, i]
             lib.attn_fwd_host_workspace_bytes.restype = ctypes.c_size_t
             lib.attn_fwd_host.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp,
@@ -161,6 +163,12 @@ def attn_decode_host(q, k_cache, v_cache, o, lse, B, Hq, Hkv, Tk, d, scale, work
                      workspace_bytes, stream) -> int:
     return load_library().attn_decode_host(q, k_cache, v_cache, o, lse, B, Hq, Hkv, Tk, d,
                                            scale, workspace, workspace_bytes, stream)
+
+
+def attn_bwd_window(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Tq, Tk, d, window, scale,
+                    workspace, workspace_bytes, stream) -> int:
+    return load_library().attn_bwd_window(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Tq, Tk,
+                                          d, window, scale, workspace, workspace_bytes, stream)
 
 
 def attn_status_string(status: int) -> str:
@@ -437,9 +445,10 @@ def fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqle
 
 
 def bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None,
-        workspace=None, dq=None, dk=None, dv=None, stream=None):
+        workspace=None, dq=None, dk=None, dv=None, stream=None, window: int | None = None):
     """dq, dk, dv of attention through attn_bwd: q/k/v/causal/scale as given
-    to `fwd`, (o, lse) what `fwd` returned, dout = dL/dO."""
+    to `fwd`, (o, lse) what `fwd` returned, dout = dL/dO.  With `window`
+    (the same as given to `fwd`) through attn_bwd_window."""
     import torch
 
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
@@ -459,11 +468,15 @@ def bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None,
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    rc = attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                  dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, Tq,
-                  Tk, d, int(bool(causal)), 0.0 if scale is None else float(scale),
-                  workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-                  _stream_handle(stream))
+    sc = 0.0 if scale is None else float(scale)
+    ptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+            dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, Hq, Hkv, Tq, Tk, d)
+    ws = (workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+          _stream_handle(stream))
+    if window is None:
+        rc, where = attn_bwd(*ptrs, int(bool(causal)), sc, *ws), "attn_bwd"
+    else:
+        rc, where = attn_bwd_window(*ptrs, int(window), sc, *ws), "attn_bwd_window"
     if rc != ATTN_OK:
-        raise AttnError(rc, "attn_bwd")
+        raise AttnError(rc, where)
     return dq, dk, dv

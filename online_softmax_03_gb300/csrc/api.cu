@@ -292,10 +292,11 @@ ATTN_API size_t attn_bwd_workspace_bytes(int B, int Hq, int Tq, int d) {
   return attn_host::bwd_workspace_bytes_for(B, Hq, Tq, d);
 }
 
-ATTN_API int attn_bwd(const void *q, const void *k, const void *v, const void *o,
-                      const float *lse, const void *dout, void *dq, void *dk, void *dv, int B,
-                      int Hq, int Hkv, int Tq, int Tk, int d, int causal, float scale,
-                      void *workspace, size_t workspace_bytes, void *stream) {
+namespace {
+int bwd_common(const void *q, const void *k, const void *v, const void *o, const float *lse,
+               const void *dout, void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int Tq,
+               int Tk, int d, int causal, int window, float scale, void *workspace,
+               size_t workspace_bytes, void *stream) {
   float sc = 0.f;
   // q/k/v/o/lse as for attn_fwd, then the gradient tensors
   int rc = validate(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, causal, scale, &sc);
@@ -323,12 +324,32 @@ ATTN_API int attn_bwd(const void *q, const void *k, const void *v, const void *o
   a.Tk = Tk;
   a.d = d;
   a.causal = causal;
+  a.window = window;
   a.scale = sc;
   a.workspace = workspace;
   a.workspace_bytes = workspace_bytes;
   a.stream = static_cast<cudaStream_t>(stream);
   a.wait_ns = g_wait_ns.load();
   return attn_host::bwd_launch(a);
+}
+}  // namespace
+
+ATTN_API int attn_bwd(const void *q, const void *k, const void *v, const void *o,
+                      const float *lse, const void *dout, void *dq, void *dk, void *dv, int B,
+                      int Hq, int Hkv, int Tq, int Tk, int d, int causal, float scale,
+                      void *workspace, size_t workspace_bytes, void *stream) {
+  return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Tq, Tk, d, causal, 0, scale,
+                    workspace, workspace_bytes, stream);
+}
+
+ATTN_API int attn_bwd_window(const void *q, const void *k, const void *v, const void *o,
+                             const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                             int B, int Hq, int Hkv, int Tq, int Tk, int d, int window,
+                             float scale, void *workspace, size_t workspace_bytes,
+                             void *stream) {
+  if (window < 1) return ATTN_ERR_INVALID_ARG;
+  return bwd_common(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Tq, Tk, d, 1, window, scale,
+                    workspace, workspace_bytes, stream);
 }
 
 ATTN_API const char *attn_status_string(int status) {

@@ -75,6 +75,7 @@ int launch_bwd(const attn_host::BwdArgs &a, unsigned int *status) {
   p.Tq_pad = Tq_pad;
   p.n_qt = Tq_pad / 128;
   p.causal = a.causal;
+  p.window = a.window;
   p.scale = a.scale;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.wait_ns = a.wait_ns;

@@ -85,6 +85,7 @@ struct BwdParams {
   int Tq, Tk, Tq_pad;
   int n_qt;                // ceil(Tq / 128)
   int causal;
+  int window;              // > 0: causal sliding window of this many keys
   float scale, scale_log2;
   unsigned long long wait_ns;
 };
@@ -172,7 +173,11 @@ __global__ void __launch_bounds__(320, 1)
   // Query tiles that see any key of this tile: under causal masking query i
   // sees key j iff j <= i + delta.
   const int qt_lo = p.causal ? max(0, kt * C::BN - delta) / C::BM : 0;
-  const int n_q = p.n_qt - qt_lo;
+  // Under a sliding window query i also needs j > i + delta - window: the
+  // tile's last key is seen by queries up to kt*BN + BN - 2 - delta + window.
+  const int q_last = kt * C::BN + C::BN - 2 - delta + p.window;
+  const int qt_end = p.window > 0 ? (q_last < 0 ? 0 : min(p.n_qt, q_last / C::BM + 1)) : p.n_qt;
+  const int n_q = qt_end - qt_lo;
   const int n_steps = n_q > 0 ? p.group * n_q : 0;
 
   if (threadIdx.x == 0) {
@@ -347,6 +352,8 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const int key = kt * C::BN + r;
     const bool key_ok = key < p.Tk;
+    // keys a query sees after its first one (the whole rest without a window)
+    const unsigned span = p.window > 0 ? (unsigned)p.window : 0x7fffffffu;
     const float sl2 = p.scale_log2;
     uint8_t *ds_row = smem + C::OFF_DS + r * 128;
     bool ok = true;
@@ -355,9 +362,13 @@ __global__ void __launch_bounds__(320, 1)
       if (!ok) break;
       tc_fence_after();
       const int q0 = step_qt(s) * C::BM;
-      // keys above the diagonal of some query of the tile need the mask
-      const bool need_mask = p.causal && (kt * C::BN + C::BN - 1 > q0 + delta);
-      const int lim = key - delta - q0;  // query q (in tile) sees the key iff q >= lim
+      // keys above the diagonal of some query of the tile, or (window)
+      // left of some query's window, need the mask
+      const bool need_mask =
+          (p.causal && (kt * C::BN + C::BN - 1 > q0 + delta)) ||
+          (p.window > 0 && q0 + C::BM - 1 >= kt * C::BN - delta + p.window);
+      // query q (in tile) sees the key iff lim <= q < lim + span
+      const int lim = key - delta - q0;
 #pragma unroll 1
       for (int c = 0; c < C::BM / 32; ++c) {
         float sv[32], dp[32];
@@ -372,8 +383,8 @@ __global__ void __launch_bounds__(320, 1)
           float p0 = ex2_approx(x.x);
           float p1 = ex2_approx(x.y);
           if (need_mask) {
-            if (q < lim) p0 = 0.f;
-            if (q + 1 < lim) p1 = 0.f;
+            if ((unsigned)(q - lim) >= span) p0 = 0.f;
+            if ((unsigned)(q + 1 - lim) >= span) p1 = 0.f;
           }
           if (!key_ok) p0 = p1 = 0.f;
           const float2 d = __fmul2_rn(make_float2(p0, p1), make_float2(dp[i], dp[i + 1]));
@@ -607,7 +618,11 @@ __global__ void __launch_bounds__(576, 1)
   const int delta = p.Tk - p.Tq;
   const int n_qt = p.Tq_pad / C::BM;  // 128-query tiles
   const int qt_lo = p.causal ? max(0, kt * C::BN - delta) / C::BM : 0;
-  const int n_q = n_qt - qt_lo;
+  // Under a sliding window query i also needs j > i + delta - window: the
+  // tile's last key is seen by queries up to kt*BN + BN - 2 - delta + window.
+  const int q_last = kt * C::BN + C::BN - 2 - delta + p.window;
+  const int qt_end = p.window > 0 ? (q_last < 0 ? 0 : min(n_qt, q_last / C::BM + 1)) : n_qt;
+  const int n_q = qt_end - qt_lo;
   const int n_steps = n_q > 0 ? p.group * n_q : 0;
 
   if (threadIdx.x == 0) {
@@ -807,6 +822,8 @@ __global__ void __launch_bounds__(576, 1)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const int key = kt * C::BN + r;
     const bool key_ok = key < p.Tk;
+    // keys a query sees after its first one (the whole rest without a window)
+    const unsigned span = p.window > 0 ? (unsigned)p.window : 0x7fffffffu;
     const float sl2 = p.scale_log2;
     // dS^T row r of this warpgroup's 64 queries: 128 bytes in chunk c
     uint8_t *ds_row = smem + C::OFF_DS + c * C::DS_CHUNK + r * 128;
@@ -816,8 +833,11 @@ __global__ void __launch_bounds__(576, 1)
       if (!ok) break;
       tc_fence_after();
       const int q0 = step_qt(s) * C::BM;
-      const bool need_mask = p.causal && (kt * C::BN + C::BN - 1 > q0 + delta);
-      const int lim = key - delta - q0;  // query q (in tile) sees the key iff q >= lim
+      const bool need_mask =
+          (p.causal && (kt * C::BN + C::BN - 1 > q0 + delta)) ||
+          (p.window > 0 && q0 + C::BM - 1 >= kt * C::BN - delta + p.window);
+      // query q (in tile) sees the key iff lim <= q < lim + span
+      const int lim = key - delta - q0;
       uint32_t pk[32];                   // P of the 64 queries, bf16 pairs
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -831,8 +851,8 @@ __global__ void __launch_bounds__(576, 1)
           float p0 = ex2_approx(x.x);
           float p1 = ex2_approx(x.y);
           if (need_mask) {
-            if (q < lim) p0 = 0.f;
-            if (q + 1 < lim) p1 = 0.f;
+            if ((unsigned)(q - lim) >= span) p0 = 0.f;
+            if ((unsigned)(q + 1 - lim) >= span) p1 = 0.f;
           }
           if (!key_ok) p0 = p1 = 0.f;
           pk[16 * h + i / 2] = pack_bf16x2(p0, p1);

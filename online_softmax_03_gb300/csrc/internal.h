@@ -50,6 +50,7 @@ struct BwdArgs {
   const float *lse;
   void *dq, *dk, *dv;
   int B, Hq, Hkv, Tq, Tk, d, causal;
+  int window = 0;  // > 0: causal sliding window of this many keys
   float scale;
   void *workspace;
   size_t workspace_bytes;

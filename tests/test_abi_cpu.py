@@ -314,3 +314,14 @@ def test_host_wrappers_require_pinned_cpu_tensors():
         binding.fwd_host(x, x, x)
     with pytest.raises(ValueError):
         binding.decode_host(x[:, :, :1], x, x)
+
+
+def test_bwd_window_rejects_bad_windows_on_the_host(lib):
+    for bad in (0, -1):
+        rc = binding.attn_bwd_window(Q, K, V, O, L, Q, K, V, O, 1, 2, 2, 16, 16, 64, bad, 0.0,
+                                     W, 1 << 20, None)
+        assert rc == binding.ATTN_ERR_INVALID_ARG
+    # causal is implied: more queries than keys is rejected like attn_bwd's causal case
+    rc = binding.attn_bwd_window(Q, K, V, O, L, Q, K, V, O, 1, 2, 2, 17, 16, 64, 4, 0.0,
+                                 W, 1 << 20, None)
+    assert rc == binding.ATTN_ERR_INVALID_ARG

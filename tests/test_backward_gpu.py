@@ -169,3 +169,63 @@ def test_backward_d64_long_sequence_sampled_group():
     _check("d64 long dq", qs(dq), rq)
     _check("d64 long dk", ks(dk), rk)
     _check("d64 long dv", ks(dv), rv)
+
+
+# --- sliding window ("4.2 FlashAttention I", Exercise 4): attn_bwd_window
+
+@pytest.mark.parametrize("B,Hq,Hkv,Tq,Tk,d,window", [
+    (1, 2, 2, 300, 300, 128, 100),
+    (1, 4, 2, 200, 333, 64, 129),     # GQA, Tq < Tk, ragged tiles
+    (2, 2, 1, 257, 257, 32, 1),       # one key per query: dQ = dK = 0
+    (1, 3, 3, 700, 700, 128, 256),
+    (2, 4, 1, 333, 333, 64, 2000),    # window past Tk: plain causal
+    (1, 2, 2, 1000, 1000, 128, 300),  # key tiles with no query in reach of some tiles
+])
+def test_window_backward_against_oracle(B, Hq, Hkv, Tq, Tk, d, window):
+    w, q, k, v, do = _case(B, Hq, Hkv, Tq, Tk, d, True, seed=Tq + window)
+    o, lse = binding.fwd(q, k, v, window=window)
+    dq, dk, dv = binding.bwd(q, k, v, o, lse, do, window=window)
+    torch.cuda.synchronize()
+    rq, rk, rv, _, _ = ora.attention_backward(synth.bf16_bits(q), synth.bf16_bits(k),
+                                              synth.bf16_bits(v), synth.bf16_bits(do),
+                                              causal=True, window=window)
+    for name, a, r in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+        _check(f"{w.name} w{window} {name}", a, r)
+
+
+def test_window_backward_long_sequence_sampled_heads():
+    """B=1, H=4, T=4096, d=128, W=1024 (the window row's window over 32 key
+    tiles): two heads against the oracle (each head's gradients depend only
+    on it)."""
+    w, q, k, v, do = _case(1, 4, 4, 4096, 4096, 128, True, seed=57)
+    o, lse = binding.fwd(q, k, v, window=1024)
+    dq, dk, dv = binding.bwd(q, k, v, o, lse, do, window=1024)
+    torch.cuda.synchronize()
+    for h in (0, 3):
+        sl = lambda x: x[:, h:h + 1]
+        rq, rk, rv, _, _ = ora.attention_backward(
+            synth.bf16_bits(sl(q)), synth.bf16_bits(sl(k)), synth.bf16_bits(sl(v)),
+            synth.bf16_bits(sl(do)), causal=True, window=1024)
+        for name, a, r in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+            _check(f"window long h{h} {name}", sl(a), r)
+
+
+def test_window_backward_at_least_tk_is_the_causal_backward():
+    """With window >= Tk every key tile visits the same query tiles with the
+    same masks as the causal backward: dK and dV repeat bit for bit, dQ to
+    the rounding of its reduction order."""
+    w, q, k, v, do = _case(1, 4, 2, 640, 640, 128, True, seed=58)
+    o, lse = binding.fwd(q, k, v, causal=True)
+    a = binding.bwd(q, k, v, o, lse, do, causal=True)
+    b = binding.bwd(q, k, v, o, lse, do, window=640)
+    torch.cuda.synchronize()
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+    assert (a[0].float() - b[0].float()).abs().max().item() <= 1e-2 * a[0].float().abs().max().item()
+
+
+def test_window_backward_rejects_bad_windows():
+    w, q, k, v, do = _case(1, 2, 2, 64, 64, 64, True, seed=59)
+    o, lse = binding.fwd(q, k, v, causal=True)
+    for bad in (0, -3):
+        with pytest.raises(binding.AttnError):
+            binding.bwd(q, k, v, o, lse, do, window=bad)
