@@ -312,16 +312,25 @@ def run_ours(args, rank, world, local_rank):
         return e0.elapsed_time(e1) / n
 
     # ---- rows beyond the specified step, each timed alone after it
-    win_ms = paged_ms = varlen_ms = bwd_ms = None
+    win_ms = paged_ms = varlen_ms = bwd_ms = bwd_win_ms = None
     varlen_flops = varlen_docs = 0
     if not args.no_extra_rows:
-        # sliding-window prefill
-        qw, kw, vw = synth.make_inputs(synth.WINDOW_8K, dev)
+        # sliding-window prefill, then its backward (dO drawn like the inputs)
+        WW = synth.WINDOW_8K
+        qw, kw, vw = synth.make_inputs(WW, dev)
         ow = torch.empty_like(qw)
         lw = torch.empty(qw.shape[:3], dtype=torch.float32, device=dev)
         win_ms = time_alone(
             lambda: binding.fwd(qw, kw, vw, window=synth.WINDOW_KEYS, out=ow, lse=lw), 30)
-        del qw, kw, vw, ow, lw
+        wdo = torch.randn(qw.shape, generator=torch.Generator(device=dev).manual_seed(1003),
+                          device=dev, dtype=torch.float32).to(torch.bfloat16)
+        wws = torch.empty(binding.attn_bwd_workspace_bytes(WW.B, WW.Hq, WW.Tq, WW.d),
+                          dtype=torch.uint8, device=dev)
+        wdq, wdk, wdv = torch.empty_like(qw), torch.empty_like(kw), torch.empty_like(vw)
+        bwd_win_ms = time_alone(
+            lambda: binding.bwd(qw, kw, vw, ow, lw, wdo, window=synth.WINDOW_KEYS, workspace=wws,
+                                dq=wdq, dk=wdk, dv=wdv), 20)
+        del qw, kw, vw, ow, lw, wdo, wws, wdq, wdk, wdv
         # decode against a paged cache (16-token pages, shuffled pool)
         pw = synth.PAGED_DECODE
         pq, pk, pv, ptab, plen = synth.make_paged_inputs(
@@ -505,6 +514,19 @@ def run_ours(args, rank, world, local_rank):
             },
             "traffic_main_kernel": ncu_traffic("attn_bwd_bm128_kernel/" + PREFILL.name,
                                                source_sha(*BACKWARD_SOURCES)),
+        },
+        "backward_window": None if bwd_win_ms is None else {
+            "workload": synth.WINDOW_8K.name,
+            "window_keys": synth.WINDOW_KEYS,
+            "value": round(2.5 * acct.window_flops(
+                synth.WINDOW_8K.B, synth.WINDOW_8K.Hq, synth.WINDOW_8K.Tq, synth.WINDOW_8K.Tk,
+                synth.WINDOW_8K.d, synth.WINDOW_KEYS) / (bwd_win_ms / 1e3) / 1e12, 2),
+            "unit": "TFLOP/s (5 products over the visible pairs, 2.5 x the window forward count)",
+            "ms": round(bwd_win_ms, 4),
+            "launches": "prep + backward kernel + dQ conversion",
+            "dq_reduction_bytes_per_call": acct.backward_dq_reduction_bytes(
+                synth.WINDOW_8K.B, synth.WINDOW_8K.Hq, synth.WINDOW_8K.Tq, synth.WINDOW_8K.Tk,
+                synth.WINDOW_8K.d, True, window=synth.WINDOW_KEYS),
         },
         "gpu_launches": K * 3,
         "clocks": clk,

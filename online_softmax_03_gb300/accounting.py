@@ -38,19 +38,26 @@ def backward_flops(B: int, Hq: int, Tq: int, Tk: int, d: int, causal: bool) -> f
 
 
 def backward_dq_reduction_bytes(B: int, Hq: int, Tq: int, Tk: int, d: int, causal: bool,
-                                key_tile: int = 128, query_tile: int = 128) -> int:
+                                key_tile: int = 128, query_tile: int = 128,
+                                window: int = 0) -> int:
     """Bytes of fp32 dQ the keys-outer backward adds into its global
     accumulator: every (key tile, query tile) pair a CTA visits contributes a
     partial for each query row of the tile that exists (rows past Tq are not
     added), d fp32 values each.  Under causal masking key tile j visits the
-    query tiles from the first one that sees its first key."""
+    query tiles from the first one that sees its first key; under a sliding
+    window of W keys only up to the last one whose window reaches its last
+    key (query j*key_tile + key_tile - 2 - (Tk - Tq) + W)."""
     n_kt = -(-Tk // key_tile)
     n_qt = -(-Tq // query_tile)
     delta = Tk - Tq
     rows = 0
     for j in range(n_kt):
-        lo = max(0, j * key_tile - delta) // query_tile if causal else 0
-        for t in range(lo, n_qt):
+        lo = max(0, j * key_tile - delta) // query_tile if causal or window else 0
+        hi = n_qt
+        if window:
+            last = j * key_tile + key_tile - 2 - delta + window
+            hi = 0 if last < 0 else min(n_qt, last // query_tile + 1)
+        for t in range(lo, hi):
             rows += min(query_tile, Tq - t * query_tile)
     return B * Hq * rows * d * 4
 

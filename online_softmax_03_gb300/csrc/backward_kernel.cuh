@@ -16,8 +16,10 @@
 // attn_bwd_bm128_kernel, described at its definition.  One CTA (320 threads, one per SM)
 // owns 128 keys of one K/V head and walks every query tile of every query
 // head of that head's group (grouped-query attention); under causal masking
-// it starts at the first query tile that sees its keys.  Per step of 128
-// queries:
+// it starts at the first query tile that sees its keys, and under a sliding
+// window of W keys ("4.2 FlashAttention I", Exercise 4) it also stops after
+// the last query tile whose window reaches them, masking the steps that
+// cross either edge.  Per step of 128 queries:
 //
 //   warp 8     producer: K and V of the key tile once, then per step the Q
 //              and dO tiles (TMA) and the step's aux rows (bulk copy).

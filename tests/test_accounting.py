@@ -92,3 +92,18 @@ def test_backward_dq_reduction_bytes():
     # rows), Tk = 300 (delta 170); the first query to see key tile 2 (keys
     # 256..299) is row 86, in tile 0, so all three key tiles visit all 130 rows
     assert acc.backward_dq_reduction_bytes(1, 1, 130, 300, 32, True) == 3 * 130 * 32 * 4
+
+
+def test_backward_dq_reduction_bytes_under_a_window():
+    # a window of at least Tk keys is the causal count
+    assert acc.backward_dq_reduction_bytes(2, 4, 1000, 1000, 64, True, window=1000) == \
+        acc.backward_dq_reduction_bytes(2, 4, 1000, 1000, 64, True)
+    # T = 8192, W = 1024: key tile j (keys 128j .. 128j+127) is seen by queries
+    # 128j .. 128j+126+1024, i.e. query tiles j .. j+8 (9 tiles), clipped at the
+    # last of the 64 tiles; every tile is a full 128 rows
+    steps = sum(min(64, j + 9) - j for j in range(64))
+    assert steps == 64 * 9 - 36
+    assert acc.backward_dq_reduction_bytes(4, 32, 8192, 8192, 128, True, window=1024) == \
+        4 * 32 * steps * 128 * 128 * 4
+    # W = 1: each key tile reaches only its own query tile
+    assert acc.backward_dq_reduction_bytes(1, 1, 256, 256, 32, True, window=1) == 2 * 128 * 32 * 4
