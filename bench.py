@@ -527,6 +527,8 @@ def run_ours(args, rank, world, local_rank):
             "dq_reduction_bytes_per_call": acct.backward_dq_reduction_bytes(
                 synth.WINDOW_8K.B, synth.WINDOW_8K.Hq, synth.WINDOW_8K.Tq, synth.WINDOW_8K.Tk,
                 synth.WINDOW_8K.d, True, window=synth.WINDOW_KEYS),
+            "traffic_main_kernel": ncu_traffic("attn_bwd_bm128_kernel/" + synth.WINDOW_8K.name,
+                                               source_sha(*BACKWARD_SOURCES)),
         },
         "gpu_launches": K * 3,
         "clocks": clk,
