@@ -480,3 +480,47 @@ def bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None,
     if rc != ATTN_OK:
         raise AttnError(rc, where)
     return dq, dk, dv
+
+
+# ------------------------------------------------------------- autograd
+
+def _autograd_function():
+    import torch
+
+    class _Attention(torch.autograd.Function):
+        """O = attention(q, k, v) through attn_fwd / attn_fwd_window, with the
+        gradients of attn_bwd / attn_bwd_window; saves (q, k, v, O, LSE), so
+        the backward recomputes the probabilities from the row log-sum-exp
+        instead of storing them ("4.2 FlashAttention I", section "The
+        backward pass: recomputation instead of storage")."""
+
+        @staticmethod
+        def forward(ctx, q, k, v, causal, scale, window):
+            o, lse = fwd(q, k, v, causal=causal, scale=scale, window=window)
+            ctx.save_for_backward(q, k, v, o, lse)
+            ctx.causal, ctx.scale, ctx.window = causal, scale, window
+            return o
+
+        @staticmethod
+        def backward(ctx, do):
+            q, k, v, o, lse = ctx.saved_tensors
+            dq, dk, dv = bwd(q, k, v, o, lse, do.contiguous(), causal=ctx.causal,
+                             scale=ctx.scale, window=ctx.window)
+            return dq, dk, dv, None, None, None
+
+    return _Attention
+
+
+_ATTENTION = None
+
+
+def attention(q, k, v, causal: bool = False, scale: float | None = None,
+              window: int | None = None):
+    """Differentiable attention for bf16 CUDA tensors q [B,Hq,Tq,d] and
+    k, v [B,Hkv,Tk,d]: the forward through `fwd`, the backward through `bwd`
+    (GQA gradients of a K/V head sum over its query heads).  `window`
+    selects the causal sliding window."""
+    global _ATTENTION
+    if _ATTENTION is None:
+        _ATTENTION = _autograd_function()
+    return _ATTENTION.apply(q, k, v, bool(causal) or window is not None, scale, window)

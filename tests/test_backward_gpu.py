@@ -229,3 +229,20 @@ def test_window_backward_rejects_bad_windows():
     for bad in (0, -3):
         with pytest.raises(binding.AttnError):
             binding.bwd(q, k, v, o, lse, do, window=bad)
+
+
+@pytest.mark.parametrize("causal,window", [(False, None), (True, None), (True, 100)])
+def test_autograd_attention_matches_the_oracle(causal, window):
+    """binding.attention as a torch autograd op: a loss's gradients through
+    it equal the oracle's backward for dO = dLoss/dO."""
+    w, q, k, v, do = _case(1, 4, 2, 300, 300, 64, causal, seed=60 + (window or 0))
+    qg, kg, vg = (x.clone().requires_grad_(True) for x in (q, k, v))
+    o = binding.attention(qg, kg, vg, causal=causal, window=window)
+    (o.float() * do.float()).sum().backward()
+    torch.cuda.synchronize()
+    rq, rk, rv, ro, _ = ora.attention_backward(synth.bf16_bits(q), synth.bf16_bits(k),
+                                               synth.bf16_bits(v), synth.bf16_bits(do),
+                                               causal=causal, window=window or 0)
+    assert np.abs(o.detach().float().cpu().numpy() - ro).max() <= 2e-2
+    for name, a, r in (("dq", qg.grad, rq), ("dk", kg.grad, rk), ("dv", vg.grad, rv)):
+        _check(f"autograd {name}", a, r)
