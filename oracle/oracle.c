@@ -532,7 +532,8 @@ int oracle_attn_paged_decode(const void *q, const void *k_pages,
  * flash_attn_varlen_func call: cumulative int32 offsets of length B+1, and
  * no score between two documents is ever formed).  Each sequence is an
  * independent attention problem with the definition at the top of this
- * file (causal: bottom-right aligned inside the sequence).
+ * file (causal: bottom-right aligned inside the sequence; window > 0: also
+ * the sliding window of "4.2 FlashAttention I", Exercise 4, inside it).
  *
  * Layout (token-major, as packed activations come):
  *   q, o  [total_q, Hq, d]      k, v  [total_k, Hkv, d]     lse  [Hq, total_q]
@@ -543,10 +544,10 @@ int oracle_attn_paged_decode(const void *q, const void *k_pages,
  */
 int oracle_attn_varlen(const void *q, const void *k, const void *v, int in_type,
                        const int *cu_q, const int *cu_k, int B, int Hq, int Hkv,
-                       int total_q, int total_k, int d, int causal, double scale,
-                       double *o, double *lse) {
+                       int total_q, int total_k, int d, int causal, int window,
+                       double scale, double *o, double *lse) {
   if (B < 1 || Hq < 1 || Hkv < 1 || d < 1 || total_q < 0 || total_k < 0 ||
-      Hq % Hkv != 0 || cu_q[0] != 0 || cu_k[0] != 0)
+      Hq % Hkv != 0 || cu_q[0] != 0 || cu_k[0] != 0 || window < 0 || (window > 0 && !causal))
     return ORACLE_ERR_ARG;
   for (int b = 0; b < B; ++b) {
     const int nq = cu_q[b + 1] - cu_q[b], nk = cu_k[b + 1] - cu_k[b];
@@ -578,7 +579,7 @@ int oracle_attn_varlen(const void *q, const void *k, const void *v, int in_type,
         load_rows(q, in_type, (qrow * Hq + h) * (size_t)d, 0, 1, d, qi);
         double m = -INFINITY;
         for (int j = 0; j < nk; ++j) {
-          if (!visible(i, j, nq, nk, causal, 0)) {
+          if (!visible(i, j, nq, nk, causal, window)) {
             s[j] = -INFINITY;
             continue;
           }

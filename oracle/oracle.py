@@ -70,7 +70,7 @@ def _load():
             lib.oracle_attn_paged_decode.argtypes = [vp, vp, vp, ip, vp, vp, ip, ip,
                                                      ip, ip, ip, ip, ip, dp, vp, vp]
             lib.oracle_attn_varlen.argtypes = [vp, vp, vp, ip, vp, vp, ip, ip, ip, ip,
-                                               ip, ip, ip, dp, vp, vp]
+                                               ip, ip, ip, ip, dp, vp, vp]
             lib.oracle_attn_bwd_dense.argtypes = [vp, vp, vp, vp, ip, ip, ip, ip, ip, ip, ip,
                                                   ip, ip, dp, vp, vp, vp, vp, vp]
             lib.oracle_attn_bwd_blocked.argtypes = [vp, vp, vp, vp, ip, vp, vp, ip, ip, ip,
@@ -231,10 +231,11 @@ def attention_paged_decode(q, k_pages, v_pages, block_table, seq_lens, scale=Non
     return o, lse
 
 
-def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, causal=False, scale=None):
+def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, causal=False, scale=None, window=0):
     """Packed variable-length attention.
 
-    q [total_q, Hq, d]; k, v [total_k, Hkv, d]; cu_seqlens_q / _k int [B+1].
+    q [total_q, Hq, d]; k, v [total_k, Hkv, d]; cu_seqlens_q / _k int [B+1];
+    window > 0 (causal only) applies the sliding window inside each sequence.
     Returns (o [total_q, Hq, d], lse [Hq, total_q]) in float64; rows outside
     every sequence are NaN.
     """
@@ -254,7 +255,7 @@ def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, causal=False, scale=No
     lse = np.full((Hq, total_q), np.nan)
     rc = _load().oracle_attn_varlen(_ptr(qa), _ptr(ka), _ptr(va), tq, _ptr(cq), _ptr(ck),
                                     cq.size - 1, Hq, Hkv, total_q, total_k, d,
-                                    int(bool(causal)), scale, _ptr(o), _ptr(lse))
+                                    int(bool(causal)), int(window), scale, _ptr(o), _ptr(lse))
     _check(rc)
     return o, lse
 

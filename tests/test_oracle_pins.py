@@ -705,3 +705,47 @@ def test_window_backward_rejects_a_window_without_causal():
     q = _rand((1, 1, 4, 4), 188)
     with pytest.raises(ValueError):
         ora.attention_backward(q, q, q, q, causal=False, window=2)
+
+
+@pytest.mark.parametrize("window", [1, 3, 6, 40])
+def test_varlen_window_is_the_dense_window_per_sequence(window):
+    """With a sliding window each sequence of the pack equals the dense
+    windowed definition on that sequence alone (the window counted inside
+    the sequence, bottom-right aligned; W past every length is causal)."""
+    Hq, Hkv, d = 4, 2, 8
+    lq, lk = [5, 0, 17, 1, 9], [9, 4, 17, 3, 9]
+    qs = [_rand((Hq, n, d), 200 + i) for i, n in enumerate(lq)]
+    ks = [_rand((Hkv, n, d), 210 + i) for i, n in enumerate(lk)]
+    vs = [_rand((Hkv, n, d), 220 + i) for i, n in enumerate(lk)]
+    (q, cq), (k, ck), (v, _) = _pack(qs), _pack(ks), _pack(vs)
+    o, lse = ora.attention_varlen(q, k, v, cq, ck, causal=True, window=window)
+    for b in range(len(lq)):
+        if lq[b] == 0:
+            continue
+        od, ld, _ = ora.attention_dense(qs[b][None], ks[b][None], vs[b][None], causal=True,
+                                        window=window)
+        np.testing.assert_allclose(o[cq[b]:cq[b + 1]], od[0].transpose(1, 0, 2), rtol=0, atol=1e-14)
+        np.testing.assert_allclose(lse[:, cq[b]:cq[b + 1]], ld[0], rtol=0, atol=1e-14)
+    if window == 40:
+        oc, lc = ora.attention_varlen(q, k, v, cq, ck, causal=True)
+        rows = ~np.isnan(oc[:, 0, 0])
+        np.testing.assert_array_equal(o[rows], oc[rows])
+
+
+def test_varlen_window_one_key_copies_the_value_at_each_position():
+    """W = 1: every query sees only the key at its own position, so O is that
+    value row and LSE the single scaled score (closed form)."""
+    H, d = 2, 4
+    lens = [3, 7]
+    q, cu = _pack([_rand((H, n, d), 230 + i) for i, n in enumerate(lens)])
+    k, _ = _pack([_rand((H, n, d), 232 + i) for i, n in enumerate(lens)])
+    v, _ = _pack([_rand((H, n, d), 234 + i) for i, n in enumerate(lens)])
+    o, lse = ora.attention_varlen(q, k, v, cu, cu, causal=True, window=1, scale=0.5)
+    np.testing.assert_allclose(o, v, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(lse, 0.5 * (q * k).sum(axis=2).T, rtol=0, atol=1e-14)
+
+
+def test_varlen_window_requires_causal():
+    q, cu = _pack([_rand((1, 4, 4), 236)])
+    with pytest.raises(ValueError):
+        ora.attention_varlen(q, q, q, cu, cu, causal=False, window=2)
