@@ -151,6 +151,24 @@ int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float 
                     void *stream);
 
 /*
+ * attn_fwd_varlen_window -- packed variable-length forward with a causal
+ * sliding window inside each sequence.
+ *
+ * As attn_fwd_varlen with the causal mask, and each query of a sequence sees
+ * only that sequence's `window` most recent keys (p - window < j <= p with
+ * p = i + nk - nq inside the sequence; "4.2 FlashAttention I", Exercise 4).
+ * K/V tiles wholly outside every row's window are never loaded.
+ *   window    number of keys each query sees (>= 1)
+ * Other arguments, layouts, workspace and errors are those of
+ * attn_fwd_varlen; window < 1 returns ATTN_ERR_INVALID_ARG.
+ */
+int attn_fwd_varlen_window(const void *q, const void *k, const void *v, void *o, float *lse,
+                           const int *cu_seqlens_q, const int *cu_seqlens_k, int B, int Hq,
+                           int Hkv, int total_q, int total_k, int max_seqlen_q,
+                           int max_seqlen_k, int d, int window, float scale, void *workspace,
+                           size_t workspace_bytes, void *stream);
+
+/*
  * attn_decode_workspace_bytes -- scratch needed by attn_decode.
  *
  * Depends only on the sizes (not on the GPU), so it may be called before any

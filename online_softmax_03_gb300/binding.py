@@ -57,6 +57,8 @@ def load_library():
             lib.attn_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i,
                                             i, i, f, vp, ctypes.c_size_t, vp]
             lib.attn_fwd_varlen.restype = i
+            lib.attn_fwd_varlen_window.argtypes = lib.attn_fwd_varlen.argtypes
+            lib.attn_fwd_varlen_window.restype = i
             lib.attn_decode_workspace_bytes.argtypes = [i, i, i, i, i]
             lib.attn_decode_workspace_bytes.restype = ctypes.c_size_t
             lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp,
@@ -114,6 +116,15 @@ def attn_fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, B, Hq, Hkv, tot
     return load_library().attn_fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, B, Hq,
                                           Hkv, total_q, total_k, max_seqlen_q, max_seqlen_k, d,
                                           causal, scale, workspace, workspace_bytes, stream)
+
+
+def attn_fwd_varlen_window(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, B, Hq, Hkv, total_q,
+                           total_k, max_seqlen_q, max_seqlen_k, d, window, scale, workspace,
+                           workspace_bytes, stream) -> int:
+    return load_library().attn_fwd_varlen_window(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k,
+                                                 B, Hq, Hkv, total_q, total_k, max_seqlen_q,
+                                                 max_seqlen_k, d, window, scale, workspace,
+                                                 workspace_bytes, stream)
 
 
 def attn_decode_workspace_bytes(B, Hq, Hkv, Tk, d) -> int:
@@ -405,10 +416,11 @@ def decode_paged(q, k_pages, v_pages, block_table, seq_lens, max_seq_len: int | 
 
 def fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,
                causal: bool = False, scale: float | None = None, workspace=None, out=None,
-               lse=None, stream=None):
+               lse=None, stream=None, window: int | None = None):
     """O [total_q,Hq,d], LSE [Hq,total_q] for a packed batch: q [total_q,Hq,d],
     k/v [total_k,Hkv,d] (bf16, token-major), cu_seqlens_q/_k int32 [B+1] on
-    the GPU, max_seqlen_q/_k host-side bounds of the lengths."""
+    the GPU, max_seqlen_q/_k host-side bounds of the lengths.  With `window`
+    through attn_fwd_varlen_window (causal, the window inside each sequence)."""
     import torch
 
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
@@ -433,14 +445,16 @@ def fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqle
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((Hq, total_q), dtype=torch.float32, device=q.device)
-    rc = attn_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                         lse.data_ptr(), cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), B,
-                         Hq, Hkv, total_q, total_k, int(max_seqlen_q), int(max_seqlen_k), d,
-                         int(bool(causal)), 0.0 if scale is None else float(scale),
-                         workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-                         _stream_handle(stream))
+    fn, where = (attn_fwd_varlen, "attn_fwd_varlen") if window is None else \
+        (attn_fwd_varlen_window, "attn_fwd_varlen_window")
+    rc = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+            cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), B, Hq, Hkv, total_q, total_k,
+            int(max_seqlen_q), int(max_seqlen_k), d,
+            int(bool(causal)) if window is None else int(window),
+            0.0 if scale is None else float(scale), workspace.data_ptr(),
+            workspace.numel() * workspace.element_size(), _stream_handle(stream))
     if rc != ATTN_OK:
-        raise AttnError(rc, "attn_fwd_varlen")
+        raise AttnError(rc, where)
     return out, lse
 
 

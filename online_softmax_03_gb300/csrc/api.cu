@@ -161,11 +161,12 @@ ATTN_API size_t attn_fwd_varlen_workspace_bytes(int B, int total_q, int max_seql
   return attn_host::varlen_workspace_bytes_for(B, total_q, max_seqlen_q);
 }
 
-ATTN_API int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
-                             const int *cu_seqlens_q, const int *cu_seqlens_k, int B, int Hq,
-                             int Hkv, int total_q, int total_k, int max_seqlen_q,
-                             int max_seqlen_k, int d, int causal, float scale, void *workspace,
-                             size_t workspace_bytes, void *stream) {
+namespace {
+int varlen_common(const void *q, const void *k, const void *v, void *o, float *lse,
+                  const int *cu_seqlens_q, const int *cu_seqlens_k, int B, int Hq, int Hkv,
+                  int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int d,
+                  int causal, int window, float scale, void *workspace,
+                  size_t workspace_bytes, void *stream) {
   float sc = 0.f;
   // the shared checks, with the longest sequences standing in for Tq and Tk
   int rc = validate(q, k, v, o, lse, B, Hq, Hkv, max_seqlen_q, max_seqlen_k, d, 0, scale, &sc);
@@ -194,7 +195,7 @@ ATTN_API int attn_fwd_varlen(const void *q, const void *k, const void *v, void *
   a.Tk = max_seqlen_k;
   a.d = d;
   a.causal = causal;
-  a.window = 0;
+  a.window = window;
   a.scale = sc;
   a.stream = static_cast<cudaStream_t>(stream);
   a.wait_ns = g_wait_ns.load();
@@ -207,6 +208,29 @@ ATTN_API int attn_fwd_varlen(const void *q, const void *k, const void *v, void *
   a.workspace = workspace;
   a.workspace_bytes = workspace_bytes;
   return attn_host::prefill_launch(a);
+}
+}  // namespace
+
+ATTN_API int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                             const int *cu_seqlens_q, const int *cu_seqlens_k, int B, int Hq,
+                             int Hkv, int total_q, int total_k, int max_seqlen_q,
+                             int max_seqlen_k, int d, int causal, float scale, void *workspace,
+                             size_t workspace_bytes, void *stream) {
+  return varlen_common(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, B, Hq, Hkv, total_q,
+                       total_k, max_seqlen_q, max_seqlen_k, d, causal, 0, scale, workspace,
+                       workspace_bytes, stream);
+}
+
+ATTN_API int attn_fwd_varlen_window(const void *q, const void *k, const void *v, void *o,
+                                    float *lse, const int *cu_seqlens_q,
+                                    const int *cu_seqlens_k, int B, int Hq, int Hkv,
+                                    int total_q, int total_k, int max_seqlen_q,
+                                    int max_seqlen_k, int d, int window, float scale,
+                                    void *workspace, size_t workspace_bytes, void *stream) {
+  if (window < 1) return ATTN_ERR_INVALID_ARG;
+  return varlen_common(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, B, Hq, Hkv, total_q,
+                       total_k, max_seqlen_q, max_seqlen_k, d, 1, window, scale, workspace,
+                       workspace_bytes, stream);
 }
 
 ATTN_API size_t attn_decode_workspace_bytes(int B, int Hq, int Hkv, int Tk, int d) {

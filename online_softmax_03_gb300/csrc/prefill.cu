@@ -80,17 +80,20 @@ constexpr int kPlanThreads = 1024;
 constexpr int kPlanBins = 8192;
 constexpr int kBinsPerThread = kPlanBins / kPlanThreads;
 
-__device__ __forceinline__ int pair_weight(int nq, int nk, int pair, int causal) {
+__device__ __forceinline__ int pair_weight(int nq, int nk, int pair, int causal, int window) {
   const int n_kt = (nk + 127) / 128;
   if (!causal) return n_kt;
   const int last = min(pair * 256 + 255, nq - 1);
-  return min(n_kt, (last + nk - nq) / 128 + 1);
+  const int hi = min(n_kt, (last + nk - nq) / 128 + 1);
+  if (window <= 0) return hi;
+  // under a window the pair's first row starts the tiles it visits
+  return hi - max(0, pair * 256 + nk - nq - window + 1) / 128;
 }
 
 __global__ void __launch_bounds__(kPlanThreads)
     varlen_plan_kernel(const int *__restrict__ cu_q, const int *__restrict__ cu_k, int B,
                        int total_q, int total_k, int max_q, int max_k, int causal,
-                       int *__restrict__ list, long long capacity,
+                       int window, int *__restrict__ list, long long capacity,
                        unsigned int *__restrict__ status) {
   __shared__ int hist[kPlanBins];
   __shared__ int part[kPlanThreads];
@@ -119,7 +122,7 @@ __global__ void __launch_bounds__(kPlanThreads)
   for (int b = tid; b < B; b += kPlanThreads) {
     const int nq = cu_q[b + 1] - cu_q[b], nk = cu_k[b + 1] - cu_k[b];
     for (int pr = 0; (long long)pr * 256 < nq; ++pr) {
-      const int w = min(pair_weight(nq, nk, pr, causal), kPlanBins - 1);
+      const int w = min(pair_weight(nq, nk, pr, causal, window), kPlanBins - 1);
       atomicAdd(&hist[kPlanBins - 1 - w], 1);  // heaviest class first
     }
   }
@@ -149,7 +152,7 @@ __global__ void __launch_bounds__(kPlanThreads)
   for (int b = tid; b < B; b += kPlanThreads) {
     const int nq = cu_q[b + 1] - cu_q[b], nk = cu_k[b + 1] - cu_k[b];
     for (int pr = 0; (long long)pr * 256 < nq; ++pr) {
-      const int w = min(pair_weight(nq, nk, pr, causal), kPlanBins - 1);
+      const int w = min(pair_weight(nq, nk, pr, causal, window), kPlanBins - 1);
       const int pos = atomicAdd(&hist[kPlanBins - 1 - w], 1);
       if (pos < capacity) {
         list[2 + 2 * pos] = b;
@@ -204,7 +207,7 @@ int launch_varlen(const attn_host::PrefillArgs &a, unsigned int *status, unsigne
     p.head_group = (int)g;
   }
   p.causal = a.causal;
-  p.window = 0;
+  p.window = a.window;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.wait_ns = a.wait_ns;
   p.inject = a.inject;
@@ -214,12 +217,14 @@ int launch_varlen(const attn_host::PrefillArgs &a, unsigned int *status, unsigne
   p.total_q = a.total_q;
   p.work = work + 2 * (g_launch_seq.fetch_add(1) % kWorkSlots);
   varlen_plan_kernel<<<1, kPlanThreads, 0, a.stream>>>(
-      a.cu_q, a.cu_k, a.B, a.total_q, a.total_k, a.Tq, a.Tk, a.causal,
+      a.cu_q, a.cu_k, a.B, a.total_q, a.total_k, a.Tq, a.Tk, a.causal, a.window,
       static_cast<int *>(a.workspace), capacity, status);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   const long long items = capacity * a.Hq;  // upper bound; the list holds the count
   const long long grid = items < sms ? items : sms;
-  auto kern = attn_dev::prefill_fwd_kernel<D, false, true>;
+  // the sliding window inside each sequence compiles a variant of its own
+  auto kern = a.window > 0 ? attn_dev::prefill_fwd_kernel<D, true, true>
+                           : attn_dev::prefill_fwd_kernel<D, false, true>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)C::SMEM_BYTES) != cudaSuccess)
     return ATTN_ERR_CUDA;

@@ -249,13 +249,14 @@ __device__ __forceinline__ VarlenItem varlen_item(const PrefillParams &p, int id
   return v;
 }
 
+template <bool kWindow>
 __device__ __forceinline__ PrefillItem varlen_prefill_item(const PrefillParams &p,
                                                            const VarlenItem &v) {
   PrefillItem it;
   it.bh = v.h;
   it.bh_kv = v.h / p.group;
   it.q0 = v.pair * 256;
-  prefill_ranges<false>(it, v.Tq, v.Tk, p.causal, 0);
+  prefill_ranges<kWindow>(it, v.Tq, v.Tk, p.causal, p.window);
   return it;
 }
 
@@ -406,7 +407,7 @@ __global__ void __launch_bounds__(320, 1)
         if (idx >= 0) {
           if constexpr (kVarlen) {
             vi = varlen_item(p, idx, n_items / p.Hq);
-            it = varlen_prefill_item(p, vi);
+            it = varlen_prefill_item<kWindow>(p, vi);
             ring[8] = vi.q_base;
             ring[9] = vi.Tq;
             ring[10] = vi.k_base;

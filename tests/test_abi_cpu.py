@@ -325,3 +325,10 @@ def test_bwd_window_rejects_bad_windows_on_the_host(lib):
     rc = binding.attn_bwd_window(Q, K, V, O, L, Q, K, V, O, 1, 2, 2, 17, 16, 64, 4, 0.0,
                                  W, 1 << 20, None)
     assert rc == binding.ATTN_ERR_INVALID_ARG
+
+
+def test_varlen_window_rejects_bad_windows_on_the_host(lib):
+    for bad in (0, -2):
+        rc = binding.attn_fwd_varlen_window(Q, K, V, O, L, T_, S_, 2, 4, 2, 64, 64, 32, 32, 64,
+                                            bad, 0.0, W, 1 << 20, None)
+        assert rc == binding.ATTN_ERR_INVALID_ARG

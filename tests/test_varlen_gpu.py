@@ -142,3 +142,60 @@ def test_varlen_bad_device_offsets_are_reported_and_nothing_is_written(cq_list, 
     torch.cuda.synchronize()
     assert binding.attn_device_status() == binding.ATTN_ERR_INVALID_ARG
     assert (o == 3.0).all() and (lse == 3.0).all()
+
+
+# --- sliding window inside each sequence (attn_fwd_varlen_window)
+
+@pytest.mark.parametrize("lens_q,lens_k,Hq,Hkv,d,window", [
+    ((100, 1, 300, 257), (100, 1, 300, 257), 4, 4, 128, 64),
+    ((5, 0, 700), (9, 4, 700), 8, 2, 64, 129),          # Tq < Tk, an empty sequence
+    ((128, 256, 384), (128, 256, 384), 2, 1, 32, 1),    # one key per query
+    ((513, 255, 2), (513, 255, 2), 3, 3, 64, 300),
+    ((1000, 37, 1), (1000, 50, 3000), 6, 2, 128, 5000),  # window past every length: causal
+])
+def test_varlen_window_against_oracle(lens_q, lens_k, Hq, Hkv, d, window):
+    q, k, v, cq, ck = synth.make_varlen_inputs(lens_q, lens_k, Hq, Hkv, d,
+                                               seed=sum(lens_q) + window, device=DEV)
+    o, lse = binding.fwd_varlen(q, k, v, cq, ck, max(lens_q), max(lens_k), window=window)
+    torch.cuda.synchronize()
+    ref = ora.attention_varlen(synth.bf16_bits(q), synth.bf16_bits(k), synth.bf16_bits(v),
+                               cq.cpu().numpy(), ck.cpu().numpy(), causal=True, window=window)
+    r = _rows(cq)
+    assert_close(o[r], lse[:, r], ref[0][r], ref[1][:, r], f"varlen w{window} {lens_q}/{lens_k}")
+
+
+def test_varlen_window_single_sequence_matches_attn_fwd_window_bit_for_bit():
+    w = synth.Workload("vl_win_single", 1, 8, 2, 1500, 2000, 128, True, "normal", 43)
+    q4, k4, v4 = synth.make_inputs(w, DEV)
+    o4, l4 = binding.fwd(q4, k4, v4, window=300)
+    tok = lambda x: x[0].transpose(0, 1).contiguous()
+    cq = torch.tensor([0, w.Tq], dtype=torch.int32, device=DEV)
+    ck = torch.tensor([0, w.Tk], dtype=torch.int32, device=DEV)
+    o, lse = binding.fwd_varlen(tok(q4), tok(k4), tok(v4), cq, ck, w.Tq, w.Tk, window=300)
+    torch.cuda.synchronize()
+    assert torch.equal(o, tok(o4)) and torch.equal(lse, l4[0])
+
+
+def test_varlen_window_packed_documents_sampled_rows():
+    """The bench pack (27 documents, 65,536 tokens, H=32, d=128) with a
+    1024-key window: sampled rows of every document, on sampled heads,
+    against the oracle's windowed definition on that document alone."""
+    lens = synth.packed_lengths(synth.VARLEN_TOKENS, synth.VARLEN.seed)
+    q, k, v, cq, ck = synth.make_varlen_inputs(lens, lens, 32, 32, 128, seed=44, device=DEV)
+    o, lse = binding.fwd_varlen(q, k, v, cq, ck, max(lens), max(lens), window=1024)
+    torch.cuda.synchronize()
+    c = cq.cpu().numpy()
+    rng = np.random.default_rng(45)
+    head_major = lambda x: x.transpose(0, 1).unsqueeze(0).contiguous()  # [1, H, n, d]
+    for b in range(len(lens)):
+        n = int(c[b + 1] - c[b])
+        sl = slice(int(c[b]), int(c[b + 1]))
+        ri = np.concatenate([[0, n - 1], rng.integers(0, n, size=4)]).astype(np.int32)
+        rh = rng.integers(0, 32, size=ri.size).astype(np.int32)
+        ref_o, ref_l = ora.attention_rows(synth.bf16_bits(head_major(q[sl])),
+                                          synth.bf16_bits(head_major(k[sl])),
+                                          synth.bf16_bits(head_major(v[sl])),
+                                          np.zeros_like(ri), rh, ri, causal=True, window=1024)
+        got_o = o[sl][torch.as_tensor(ri, device=DEV).long(), torch.as_tensor(rh, device=DEV).long()]
+        got_l = lse[:, sl][torch.as_tensor(rh, device=DEV).long(), torch.as_tensor(ri, device=DEV).long()]
+        assert_close(got_o, got_l, ref_o, ref_l, f"window pack doc {b}")
