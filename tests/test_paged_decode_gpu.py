@@ -151,3 +151,23 @@ def test_paged_decode_rejects_bad_host_arguments():
         binding.decode_paged(q, kp, vp, table, sl, max_seq_len=33)  # > 2 pages of 16
     with pytest.raises(ValueError):
         binding.decode_paged(q, kp, vp, table.long(), sl)
+
+
+def test_dense_cache_with_per_sequence_lengths_as_one_page_per_sequence():
+    """A dense cache [B, Hkv, T, d] whose T is a power of two <= 4096 is a
+    page pool with page_size = T and the table b -> b, so decode over
+    sequences of different lengths in a dense cache is attn_decode_paged with
+    one page per sequence: it must equal the dense definition on each
+    sequence's first seq_lens[b] keys."""
+    B, Hq, Hkv, T, d = 5, 16, 4, 2048, 128
+    w = synth.Workload("dense_lens", B, Hq, Hkv, 1, T, d, False, "normal", 70)
+    q, k, v = synth.make_inputs(w, DEV)
+    lens = torch.tensor([2048, 1, 777, 1500, 64], dtype=torch.int32, device=DEV)
+    table = torch.arange(B, dtype=torch.int32, device=DEV).reshape(B, 1)
+    o, lse = binding.decode_paged(q, k, v, table, lens, max_seq_len=T)
+    torch.cuda.synchronize()
+    for b, n in enumerate(lens.tolist()):
+        ref_o, ref_l, _ = ora.attention_dense(synth.bf16_bits(q[b:b + 1]),
+                                              synth.bf16_bits(k[b:b + 1, :, :n]),
+                                              synth.bf16_bits(v[b:b + 1, :, :n]), causal=False)
+        assert_close(o[b:b + 1], lse[b:b + 1], ref_o, ref_l, f"dense lens b{b} n{n}")
