@@ -199,6 +199,88 @@ def whole_job_rate(units_per_rank: float, seconds_max: float, world: int) -> flo
 
 # ------------------------------------------------------------------ GPU arm
 
+CONFIG_ROWS = (
+    ("config1_tiny_causal", synth.TINY),
+    ("config1_tiny_full", synth.TINY_NONCAUSAL),
+    ("config2_prefill_1k_causal", synth.PREFILL_1K),
+    ("config4_t8192_causal", synth.LONG_8K_CAUSAL),
+    ("config4_t8192_full", synth.LONG_8K_FULL),
+    ("config4_t8000_causal", synth.LONG_8000_CAUSAL),
+    ("config4_t8000_full", synth.LONG_8000_FULL),
+)
+FLUSH_BYTES = 256 << 20  # twice the L2
+
+
+def time_cold(fn, n, flush, stream):
+    """Device time (ms) of each of n launches of fn, every launch preceded by
+    an L2 flush that is not timed; the flush also covers the host's work of
+    the next call, so the events bracket the kernels alone."""
+    import torch
+
+    for _ in range(3):
+        flush()
+        fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    for a, b in ev:
+        flush()
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def time_config_rows(dev, stream, peak_burst):
+    """Configurations 1, 2 and 4 of the specification: per-launch device time
+    (p10/p50/p90 over 50 launches, each after an L2 flush), TFLOP/s with the
+    causal half, and the fraction of the measured burst bf16 peak."""
+    import torch
+
+    from online_softmax_03_gb300 import binding
+
+    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    rows = {}
+    for key, w in CONFIG_ROWS:
+        q, k, v = synth.make_inputs(w, dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.Hq, w.Tq), dtype=torch.float32, device=dev)
+        ms = time_cold(lambda: binding.fwd(q, k, v, causal=w.causal, scale=w.scale, out=o,
+                                           lse=lse),
+                       50, flush_buf.zero_, stream)
+        flops = acct.attention_flops(w.B, w.Hq, w.Tq, w.Tk, w.d, w.causal)
+        p10, p50, p90 = percentiles(ms)
+        rows[key] = {
+            "workload": w.name,
+            "ms_p10_p50_p90": [p10, p50, p90],
+            "tflops": round(flops / (p50 / 1e3) / 1e12, 2),
+            "frac_of_burst_peak": round(flops / (p50 / 1e3) / 1e12 / peak_burst, 4),
+            "flops_per_launch": flops,
+        }
+        del q, k, v, o, lse
+    del flush_buf
+    return {"rows": rows,
+            "timing": ("50 launches each, every launch after an untimed 256 MB write that "
+                       "flushes L2; CUDA events around each launch; median reported"),
+            "kernel": "prefill_fwd_kernel<d> (d = 32, 128, 64)"}
+
+
+def pick_peak(peaks, timed_s, clk):
+    """The bf16 denominator for a kernel timed in this run: the burst figure
+    when the timed region is short (< 1 s) or the SM clock stayed at its
+    maximum, else the sustained one (measured over seconds under the power
+    cap)."""
+    at_max = (clk.get("sm_mhz") is not None and clk.get("sm_max_mhz")
+              and clk["sm_mhz"] >= 0.97 * clk["sm_max_mhz"])
+    if timed_s < 1.0 or at_max:
+        why = (f"timed region {timed_s:.3f} s" + (", median SM clock at its maximum"
+                                                  if at_max else ""))
+        return peaks["bf16_tflops"], "bf16_tflops (burst)", why
+    return (peaks["bf16_tflops_sustained"], "bf16_tflops_sustained",
+            f"timed region {timed_s:.3f} s with the SM clock below its maximum")
+
+
 def percentiles(ms):
     """10th, 50th and 90th percentile of this rank's per-launch times (ms)."""
     xs = sorted(ms)
@@ -311,6 +393,12 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / n
 
+    # ---- the other specified configurations, each timed per launch after an
+    # L2 flush (their inputs, 0.1-100 MB, would otherwise stay in the 129 MB L2)
+    config_rows = None
+    if not args.no_extra_rows:
+        config_rows = time_config_rows(dev, stream, peaks["bf16_tflops"])
+
     # ---- rows beyond the specified step, each timed alone after it
     win_ms = paged_ms = varlen_ms = bwd_ms = bwd_win_ms = None
     varlen_flops = varlen_docs = 0
@@ -384,7 +472,7 @@ def run_ours(args, rank, world, local_rank):
     dec_gbs = whole_job_rate(K * dec_bytes, dec_s, world) / 1e9
     per_launch_tflops = pre_flops / (pre_s / K) / 1e12
     per_launch_gbs = dec_bytes / (dec_s / K) / 1e9
-    peak_tf = peaks["bf16_tflops_sustained"]
+    peak_tf, peak_key, peak_why = pick_peak(peaks, total_ms / 1e3, clk)
     peak_bw = peaks["hbm_gbs"]
     h2d_pre = sum(t.numel() * t.element_size() for t in (qp, kp, vp))
     d2h_pre = op.numel() * 2 + lp.numel() * 4
@@ -421,8 +509,9 @@ def run_ours(args, rank, world, local_rank):
             "peak": peak_tf,
             "unit": "TFLOP/s",
             "frac": round(per_launch_tflops / peak_tf, 4),
-            "peak_source": f"{peak_src} bf16_tflops_sustained (the loop runs for seconds)",
-            "frac_of_burst_peak": round(per_launch_tflops / peaks["bf16_tflops"], 4),
+            "peak_source": f"{peak_src} {peak_key}: {peak_why}",
+            "frac_of_sustained_peak": round(per_launch_tflops / peaks["bf16_tflops_sustained"],
+                                            4),
             "traffic": ncu_traffic("prefill_fwd_kernel<128>/" + PREFILL.name,
                                    source_sha(*PREFILL_SOURCES)),
             "algorithmic_flops_per_launch": pre_flops,
@@ -468,9 +557,10 @@ def run_ours(args, rank, world, local_rank):
             "ms": round(win_ms, 4),
             "traffic": ncu_traffic("prefill_fwd_kernel<128,window>/" + synth.WINDOW_8K.name,
                                    source_sha(*PREFILL_SOURCES)),
-            "frac_of_sustained_peak": round(acct.window_flops(
+            "frac_of_burst_peak": round(acct.window_flops(
                 synth.WINDOW_8K.B, synth.WINDOW_8K.Hq, synth.WINDOW_8K.Tq, synth.WINDOW_8K.Tk,
-                synth.WINDOW_8K.d, synth.WINDOW_KEYS) / (win_ms / 1e3) / 1e12 / peak_tf, 4),
+                synth.WINDOW_8K.d, synth.WINDOW_KEYS) / (win_ms / 1e3) / 1e12
+                / peaks["bf16_tflops"], 4),
         },
         "paged_decode": None if paged_ms is None else {
             "workload": synth.PAGED_DECODE.name,
@@ -489,7 +579,8 @@ def run_ours(args, rank, world, local_rank):
             "value": round(varlen_flops / (varlen_ms / 1e3) / 1e12, 2),
             "unit": "TFLOP/s (4*d per visible pair)",
             "ms": round(varlen_ms, 4),
-            "frac_of_sustained_peak": round(varlen_flops / (varlen_ms / 1e3) / 1e12 / peak_tf, 4),
+            "frac_of_burst_peak": round(varlen_flops / (varlen_ms / 1e3) / 1e12
+                                        / peaks["bf16_tflops"], 4),
             "launches": "planning kernel + prefill kernel",
             "traffic": ncu_traffic("prefill_fwd_kernel<128,varlen>/" + synth.VARLEN.name,
                                    source_sha(*PREFILL_SOURCES)),
@@ -500,9 +591,9 @@ def run_ours(args, rank, world, local_rank):
                                                PREFILL.d, True) / (bwd_ms / 1e3) / 1e12, 2),
             "unit": "TFLOP/s (5 products, causal half)",
             "ms": round(bwd_ms, 4),
-            "frac_of_sustained_peak": round(acct.backward_flops(
+            "frac_of_burst_peak": round(acct.backward_flops(
                 PREFILL.B, PREFILL.Hq, PREFILL.Tq, PREFILL.Tk, PREFILL.d, True)
-                / (bwd_ms / 1e3) / 1e12 / peak_tf, 4),
+                / (bwd_ms / 1e3) / 1e12 / peaks["bf16_tflops"], 4),
             "launches": "prep + backward kernel + dQ conversion",
             "dq_reduction": {
                 "bound": "fp32 reductions into the dQ accumulator (L2)",
@@ -530,6 +621,7 @@ def run_ours(args, rank, world, local_rank):
             "traffic_main_kernel": ncu_traffic("attn_bwd_bm128_kernel/" + synth.WINDOW_8K.name,
                                                source_sha(*BACKWARD_SOURCES)),
         },
+        "configs": config_rows,
         "gpu_launches": K * 3,
         "clocks": clk,
     }
@@ -620,6 +712,51 @@ def run_reference(args, rank, world):
     print(json.dumps(result), flush=True)
 
 
+PROFILE_WORKLOADS = {w.name: w for w in synth.ALL + (synth.WINDOW_8K,)}
+
+
+def run_profile(args):
+    """Profiling case: `--launches` launches of one workload's kernels and
+    nothing else, so that an ncu capture (-k, -s, -c) runs in a process that
+    holds only that workload's tensors.  Prints one line naming what ran; it
+    is not a bench line."""
+    import torch
+
+    from online_softmax_03_gb300 import binding
+    from online_softmax_03_gb300 import build as cuda_build
+
+    cuda_build.build()
+    binding.load_library()
+    name = args.profile
+    backward = name.endswith(":bwd")
+    w = PROFILE_WORKLOADS[name[:-4] if backward else name]
+    dev = torch.device("cuda", 0)
+    q, k, v = synth.make_inputs(w, dev)
+    if w.decode:
+        ws = binding.decode_workspace(k, w.Hq)
+        o, lse = torch.empty_like(q), torch.empty((w.B, w.Hq, 1), dtype=torch.float32, device=dev)
+        fn = lambda: binding.decode(q, k, v, workspace=ws, out=o, lse=lse)  # noqa: E731
+    else:
+        window = synth.WINDOW_KEYS if w is synth.WINDOW_8K else None
+        o, lse = binding.fwd(q, k, v, causal=w.causal, scale=w.scale, window=window)
+        fn = lambda: binding.fwd(q, k, v, causal=w.causal, scale=w.scale, window=window,  # noqa
+                                 out=o, lse=lse)
+        if backward:
+            do = torch.randn(q.shape, generator=torch.Generator(device=dev).manual_seed(1002),
+                             device=dev, dtype=torch.float32).to(torch.bfloat16)
+            bws = torch.empty(binding.attn_bwd_workspace_bytes(w.B, w.Hq, w.Tq, w.d),
+                              dtype=torch.uint8, device=dev)
+            dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+            fn = lambda: binding.bwd(q, k, v, o, lse, do, causal=w.causal, scale=w.scale,  # noqa
+                                     window=window, workspace=bws, dq=dq, dk=dk, dv=dv)
+    for _ in range(args.launches):
+        fn()
+    torch.cuda.synchronize()
+    assert binding.attn_device_status() == binding.ATTN_OK
+    print(json.dumps({"profile": name, "launches": args.launches,
+                      "device_bytes": torch.cuda.max_memory_allocated()}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -630,7 +767,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra-rows", action="store_true",
                     help="skip the separately timed rows beyond the specified step")
+    ap.add_argument("--profile", choices=sorted(PROFILE_WORKLOADS) +
+                    sorted(n + ":bwd" for n in PROFILE_WORKLOADS if "decode" not in n),
+                    help="run only this workload's kernels (for ncu captures); "
+                         "NAME:bwd runs the backward")
+    ap.add_argument("--launches", type=int, default=3)
     args = ap.parse_args()
+    if args.profile:
+        run_profile(args)
+        return
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
     rank = int(os.environ.get("RANK", "0"))

@@ -42,12 +42,28 @@
  *    gives up on a bounded wait records ATTN_ERR_DEVICE_TIMEOUT in a device
  *    status word read by attn_device_status().
  *  - The entry points keep no per-call state and may be called from several
- *    host threads.
+ *    host threads.  The first call on a device looks up, once, the device's
+ *    SM count and the addresses of the library's device words, and raises
+ *    each kernel's shared-memory limit; make that first call before any
+ *    stream capture begins.
+ *  - The forward kernels (attn_fwd, attn_fwd_window, attn_fwd_varlen,
+ *    attn_fwd_varlen_window) take their work items from ATTN_FWD_MAX_IN_FLIGHT
+ *    work counters per device, used in turn, and from as many more for
+ *    launches captured into CUDA graphs.  At most that many forward launches
+ *    (of each kind) may be in flight on one device at once, across all
+ *    streams and threads.  If a launch's counter is taken over by a newer
+ *    launch before it finishes, the older launch stops (its outputs are then
+ *    incomplete) and attn_device_status reports ATTN_ERR_IN_FLIGHT_LIMIT;
+ *    counts are never shared silently.  A captured launch may be replayed
+ *    any number of times, one replay at a time.
  */
 #ifndef ATTN_GB300_H
 #define ATTN_GB300_H
 
 #include <stddef.h>
+
+/* Forward launches that may be in flight at once on one device. */
+#define ATTN_FWD_MAX_IN_FLIGHT 64
 
 #ifdef __cplusplus
 extern "C" {
@@ -60,7 +76,8 @@ typedef enum {
   ATTN_ERR_MISALIGNED = 3,     /* a pointer breaks the alignment rule         */
   ATTN_ERR_WORKSPACE = 4,      /* decode workspace missing or too small       */
   ATTN_ERR_CUDA = 5,           /* a CUDA runtime/driver call failed           */
-  ATTN_ERR_DEVICE_TIMEOUT = 6  /* a kernel gave up waiting (see below)        */
+  ATTN_ERR_DEVICE_TIMEOUT = 6, /* a kernel gave up waiting (see below)        */
+  ATTN_ERR_IN_FLIGHT_LIMIT = 7 /* more forward launches in flight than slots  */
 } attn_status;
 
 /*
@@ -227,7 +244,10 @@ int attn_decode(const void *q, const void *k_cache, const void *v_cache,
  *  - Every call uses the same array.  Calls that overlap on the GPU (other
  *    streams, other host threads) race on it and must be ordered by the
  *    caller.  The array keeps the last call's contents; no call depends on
- *    them, since every partial is written before it is read.
+ *    them, since every partial is written before it is read, including the
+ *    empty partial a split writes when it gives up on a bounded wait.
+ *  - The wait limit and test hooks of attn_debug_set apply as for
+ *    attn_decode; after ATTN_ERR_DEVICE_TIMEOUT, o and lse are unspecified.
  */
 #define ATTN_DECODE_NOALLOC_MAX_BYTES ((size_t)16 << 20)
 int attn_decode_noalloc(const void *q, const void *k_cache, const void *v_cache,
@@ -408,9 +428,16 @@ int attn_device_status(void *stream, int *status);
  *
  *   wait_limit_ns  time a kernel waits on one barrier before giving up
  *                  (0 restores the default of 1 s)
- *   inject         0 = none; 1 = the prefill kernel withholds the first V
- *                  tile load, so a bounded wait must expire and report
- *                  ATTN_ERR_DEVICE_TIMEOUT
+ *   inject         0 = none; otherwise one load is withheld so that a
+ *                  bounded wait must expire and report
+ *                  ATTN_ERR_DEVICE_TIMEOUT:
+ *                    1 = the forward kernel's first V tile,
+ *                    2 = the first K/V tile of the decode kernels' first
+ *                        CTA (attn_decode, attn_decode_paged,
+ *                        attn_decode_noalloc),
+ *                    3 = the first dO tile of the backward kernel's first
+ *                        CTA (attn_bwd, attn_bwd_window)
+ *                  The outputs of a call that timed out are unspecified.
  */
 void attn_debug_set(unsigned long long wait_limit_ns, int inject);
 

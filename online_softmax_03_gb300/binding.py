@@ -24,8 +24,10 @@ ATTN_ERR_MISALIGNED = 3
 ATTN_ERR_WORKSPACE = 4
 ATTN_ERR_CUDA = 5
 ATTN_ERR_DEVICE_TIMEOUT = 6
+ATTN_ERR_IN_FLIGHT_LIMIT = 7
 STATUS_CODES = (ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_MISALIGNED,
-                ATTN_ERR_WORKSPACE, ATTN_ERR_CUDA, ATTN_ERR_DEVICE_TIMEOUT)
+                ATTN_ERR_WORKSPACE, ATTN_ERR_CUDA, ATTN_ERR_DEVICE_TIMEOUT,
+                ATTN_ERR_IN_FLIGHT_LIMIT)
 
 _lock = threading.Lock()
 _lib = None

@@ -60,17 +60,93 @@ int validate(const void *q, const void *k, const void *v, const void *o,
 
 namespace attn_host {
 
-int check_device_sm103(int *num_sms) {
-  int dev = 0, major = 0, minor = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
-  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return ATTN_ERR_CUDA;
-  if (major != 10 || minor != 3) return ATTN_ERR_UNSUPPORTED;
-  if (num_sms) *num_sms = sms;
+// Per-device facts and lookups made once, on the first call that runs on a
+// device, so that a call's host work is validation, tensor-map encoding and
+// the launch.
+namespace {
+constexpr int kMaxDevices = 64;
+constexpr int kMaxCached = 64;  // symbols or kernels remembered per device
+
+struct DeviceFacts {
+  int state = 0;  // 0 = not queried, 1 = sm_103, 2 = another GPU
+  int sms = 0;
+};
+
+std::mutex g_cache_mu;
+DeviceFacts g_facts[kMaxDevices];
+struct CachedPtr {
+  const void *key;
+  void *value;
+};
+CachedPtr g_symbols[kMaxDevices][kMaxCached];
+int g_n_symbols[kMaxDevices];
+const void *g_smem_set[kMaxDevices][kMaxCached];
+int g_smem_bytes[kMaxDevices][kMaxCached];
+int g_n_smem[kMaxDevices];
+
+int current_device(int *dev) {
+  if (cudaGetDevice(dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (*dev < 0 || *dev >= kMaxDevices) return ATTN_ERR_UNSUPPORTED;
   return ATTN_OK;
 }
+}  // namespace
+
+int check_device_sm103(int *num_sms) {
+  int dev = 0;
+  int rc = current_device(&dev);
+  if (rc != ATTN_OK) return rc;
+  std::lock_guard<std::mutex> lock(g_cache_mu);
+  DeviceFacts &f = g_facts[dev];
+  if (f.state == 0) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    f.state = (major == 10 && minor == 3) ? 1 : 2;
+    f.sms = sms;
+  }
+  if (f.state != 1) return ATTN_ERR_UNSUPPORTED;
+  if (num_sms) *num_sms = f.sms;
+  return ATTN_OK;
+}
+
+int symbol_address(const void *symbol, void **out) {
+  int dev = 0;
+  int rc = current_device(&dev);
+  if (rc != ATTN_OK) return rc;
+  std::lock_guard<std::mutex> lock(g_cache_mu);
+  for (int i = 0; i < g_n_symbols[dev]; ++i)
+    if (g_symbols[dev][i].key == symbol) {
+      *out = g_symbols[dev][i].value;
+      return ATTN_OK;
+    }
+  void *ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, symbol) != cudaSuccess || !ptr) return ATTN_ERR_CUDA;
+  if (g_n_symbols[dev] < kMaxCached) g_symbols[dev][g_n_symbols[dev]++] = {symbol, ptr};
+  *out = ptr;
+  return ATTN_OK;
+}
+
+int ensure_smem_limit(const void *kern, int bytes) {
+  int dev = 0;
+  int rc = current_device(&dev);
+  if (rc != ATTN_OK) return rc;
+  std::lock_guard<std::mutex> lock(g_cache_mu);
+  for (int i = 0; i < g_n_smem[dev]; ++i)
+    if (g_smem_set[dev][i] == kern && g_smem_bytes[dev][i] >= bytes) return ATTN_OK;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+      cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (g_n_smem[dev] < kMaxCached) {
+    g_smem_set[dev][g_n_smem[dev]] = kern;
+    g_smem_bytes[dev][g_n_smem[dev]++] = bytes;
+  }
+  return ATTN_OK;
+}
+
+unsigned long long wait_limit_ns() { return g_wait_ns.load(); }
+int inject_hook() { return g_inject.load(); }
 
 bool encode_tmap_3d_bf16(CUtensorMap *map, const void *base, uint64_t inner,
                          uint64_t rows, uint64_t planes, uint32_t box_inner,
@@ -154,7 +230,10 @@ ATTN_API int attn_fwd_window(const void *q, const void *k, const void *v, void *
                              float *lse, int B, int Hq, int Hkv, int Tq, int Tk, int d,
                              int window, float scale, void *stream) {
   if (window < 1) return ATTN_ERR_INVALID_ARG;
-  return fwd_common(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, 1, window, scale, stream);
+  // a window of Tk keys or more leaves every key at or before a query's
+  // position visible: plain causal attention, computed by that path
+  return fwd_common(q, k, v, o, lse, B, Hq, Hkv, Tq, Tk, d, 1, window >= Tk ? 0 : window, scale,
+                    stream);
 }
 
 ATTN_API size_t attn_fwd_varlen_workspace_bytes(int B, int total_q, int max_seqlen_q) {
@@ -264,6 +343,7 @@ ATTN_API int attn_decode(const void *q, const void *k_cache, const void *v_cache
   a.workspace_bytes = workspace_bytes;
   a.stream = static_cast<cudaStream_t>(stream);
   a.wait_ns = g_wait_ns.load();
+  a.inject = g_inject.load();
   return attn_host::decode_launch(a);
 }
 
@@ -302,6 +382,7 @@ ATTN_API int attn_decode_paged(const void *q, const void *k_pages, const void *v
   a.workspace_bytes = workspace_bytes;
   a.stream = static_cast<cudaStream_t>(stream);
   a.wait_ns = g_wait_ns.load();
+  a.inject = g_inject.load();
   a.paged = true;
   a.block_table = block_table;
   a.seq_lens = seq_lens;
@@ -354,6 +435,7 @@ int bwd_common(const void *q, const void *k, const void *v, const void *o, const
   a.workspace_bytes = workspace_bytes;
   a.stream = static_cast<cudaStream_t>(stream);
   a.wait_ns = g_wait_ns.load();
+  a.inject = g_inject.load();
   return attn_host::bwd_launch(a);
 }
 }  // namespace
@@ -385,6 +467,8 @@ ATTN_API const char *attn_status_string(int status) {
     case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE: workspace missing or too small";
     case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA: CUDA call failed";
     case ATTN_ERR_DEVICE_TIMEOUT: return "ATTN_ERR_DEVICE_TIMEOUT: kernel wait expired";
+    case ATTN_ERR_IN_FLIGHT_LIMIT:
+      return "ATTN_ERR_IN_FLIGHT_LIMIT: too many forward launches in flight";
     default: return "ATTN_ERR_UNKNOWN";
   }
 }

@@ -22,8 +22,7 @@ int launch_main(const attn_host::BwdArgs &a, Kern kern, const attn_dev::BwdParam
       !attn_host::encode_tmap_3d_bf16(&tv, a.v, D, a.Tk, bhk, C::CHUNK, C::BN, 1, C::SPAN) ||
       (dq_map && !attn_host::encode_tmap_3d_f32(&tdq, dq_acc, D, a.Tq, bhq, 32, C::BM, 1)))
     return ATTN_ERR_CUDA;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)C::SMEM_BYTES) != cudaSuccess)
+  if (attn_host::ensure_smem_limit((const void *)kern, (int)C::SMEM_BYTES) != ATTN_OK)
     return ATTN_ERR_CUDA;
   const int n_kt = (a.Tk + C::BN - 1) / C::BN;
   const dim3 grid(n_kt, (unsigned)bhk);
@@ -79,6 +78,7 @@ int launch_bwd(const attn_host::BwdArgs &a, unsigned int *status) {
   p.scale = a.scale;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.wait_ns = a.wait_ns;
+  p.inject = a.inject;
   int rc;
   if constexpr (D >= 64)
     rc = launch_main<D, attn_dev::BwdBm128Cfg<D>>(a, attn_dev::attn_bwd_bm128_kernel<D>, p,
@@ -111,7 +111,8 @@ int bwd_launch(const BwdArgs &a) {
   int rc = check_device_sm103(nullptr);
   if (rc != ATTN_OK) return rc;
   unsigned int *status = nullptr;
-  if (cudaGetSymbolAddress(reinterpret_cast<void **>(&status), g_bwd_status) != cudaSuccess)
+  if (symbol_address((const void *)&g_bwd_status, reinterpret_cast<void **>(&status)) !=
+      ATTN_OK)
     return ATTN_ERR_CUDA;
   switch (a.d) {
     case 32: return launch_bwd<32>(a, status);

@@ -90,6 +90,7 @@ struct BwdParams {
   int window;              // > 0: causal sliding window of this many keys
   float scale, scale_log2;
   unsigned long long wait_ns;
+  int inject;              // test hook: 3 = CTA (0, 0) withholds its first dO tile
 };
 
 template <int D>
@@ -252,10 +253,14 @@ __global__ void __launch_bounds__(320, 1)
         const int q0 = step_qt(s) * C::BM;
         uint8_t *stage = smem + C::OFF_STAGE + st * C::STAGE_BYTES;
         mbar_arrive_expect_tx(&q_full[st], 2 * C::QT_BYTES + C::AUX_BYTES);
+        // test hook: the first dO tile of CTA (0, 0) is never loaded, so the
+        // wait for it must expire
+        const bool withhold = p.inject == 3 && s == 0 && blockIdx.x == 0 && blockIdx.y == 0;
         for (int c = 0; c < C::NCHUNK; ++c) {
           tma_load_3d(stage + c * (C::BM * C::SPAN), &tm_q, &q_full[st], c * C::CHUNK, q0, bh);
-          tma_load_3d(stage + C::QT_BYTES + c * (C::BM * C::SPAN), &tm_do, &q_full[st],
-                      c * C::CHUNK, q0, bh);
+          if (!withhold)
+            tma_load_3d(stage + C::QT_BYTES + c * (C::BM * C::SPAN), &tm_do, &q_full[st],
+                        c * C::CHUNK, q0, bh);
         }
         // the aux rows of the step's 128 queries: two consecutive 64-row blocks
         const size_t aoff = ((size_t)bh * (p.Tq_pad / 64) + q0 / 64) * 2048;
@@ -463,7 +468,11 @@ __global__ void __launch_bounds__(320, 1)
     bool ok = true;
     int n = 0;  // dQ chunks staged so far
     for (int s = 0; s < n_steps; ++s) {
-      ok = __all_sync(0xffffffffu, mbar_wait(dq_full, s & 1, wait_ns) && !*abort_flag);
+      // The four warps meet at named barriers below, so they take one
+      // decision on whether to go on.
+      const bool w_ok =
+          __all_sync(0xffffffffu, mbar_wait(dq_full, s & 1, wait_ns) && !*abort_flag);
+      ok = named_barrier_and(1, 128, w_ok);
       if (!ok) break;
       tc_fence_after();
       const int bh = b * p.Hq + step_head(s);
@@ -702,9 +711,12 @@ __global__ void __launch_bounds__(576, 1)
         last_q[qb] = s;
         if (s >= 1 && !mbar_wait(do_empty, (s - 1) & 1, wait_ns)) { ok = false; break; }
         mbar_arrive_expect_tx(do_full, C::QT_BYTES);
-        for (int c = 0; c < C::NCHUNK; ++c)
-          tma_load_3d(smem + C::OFF_DO + c * (C::BM * C::SPAN), &tm_do, do_full, c * C::CHUNK,
-                      q0, bh);
+        // test hook: the first dO tile of CTA (0, 0) is never loaded, so the
+        // wait for it must expire
+        if (!(p.inject == 3 && s == 0 && blockIdx.x == 0 && blockIdx.y == 0))
+          for (int c = 0; c < C::NCHUNK; ++c)
+            tma_load_3d(smem + C::OFF_DO + c * (C::BM * C::SPAN), &tm_do, do_full,
+                        c * C::CHUNK, q0, bh);
       }
       if (!ok) fail();
       // Drain: every copy issued has landed before shared memory is released.
@@ -908,6 +920,9 @@ __global__ void __launch_bounds__(576, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(dkdv_full, 0, wait_ns));
       if (!ok) fail();
     }
+    // Both warpgroups meet at a named barrier before the stores below, so
+    // they take one decision: a group that gave up on a wait stops both.
+    ok = named_barrier_and(1, 2 * C::BN, ok);
     if (ok) {
       // All MMAs have completed (dkdv_full), so the Q buffers are free: dV
       // (warpgroup 0) and dK times scale (warpgroup 1) go there as bf16 in the

@@ -1,5 +1,6 @@
 // decode.cu -- launchers for the split-KV decode kernels.
 #include <algorithm>
+#include <atomic>
 #include <climits>
 
 #include "../../include/attn.h"
@@ -13,22 +14,32 @@ template <int D, int GP, bool kPaged>
 int launch_split(const attn_dev::DecodeParams &p, dim3 grid, cudaStream_t st) {
   using C = attn_dev::DecodeCfg<D, GP>;
   auto kern = attn_dev::decode_split_kernel<D, GP, kPaged>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)C::SMEM_BYTES) != cudaSuccess)
+  if (attn_host::ensure_smem_limit((const void *)kern, (int)C::SMEM_BYTES) != ATTN_OK)
     return ATTN_ERR_CUDA;
   kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+// Resident split CTAs per SM, queried once per device.
 template <int D, int GP>
 int resident_ctas(int *out) {
   using C = attn_dev::DecodeCfg<D, GP>;
-  auto kern = attn_dev::decode_split_kernel<D, GP, false>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)C::SMEM_BYTES) != cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(out, kern, C::THREADS,
-                                                    C::SMEM_BYTES) != cudaSuccess)
+  constexpr int kMaxDevices = 64;
+  static std::atomic<int> cached[kMaxDevices];  // 0 = not queried yet
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
     return ATTN_ERR_CUDA;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    auto kern = attn_dev::decode_split_kernel<D, GP, false>;
+    if (attn_host::ensure_smem_limit((const void *)kern, (int)C::SMEM_BYTES) != ATTN_OK ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, C::THREADS, C::SMEM_BYTES) !=
+            cudaSuccess)
+      return ATTN_ERR_CUDA;
+    if (n < 1) n = 1;
+    cached[dev].store(n, std::memory_order_relaxed);
+  }
+  *out = n;
   return ATTN_OK;
 }
 
@@ -81,7 +92,8 @@ int decode_launch(const DecodeArgs &a) {
   int rc = check_device_sm103(&sms);
   if (rc != ATTN_OK) return rc;
   unsigned int *status = nullptr;
-  if (cudaGetSymbolAddress(reinterpret_cast<void **>(&status), g_decode_status) != cudaSuccess)
+  if (symbol_address((const void *)&g_decode_status, reinterpret_cast<void **>(&status)) !=
+      ATTN_OK)
     return ATTN_ERR_CUDA;
   const int group = a.Hq / a.Hkv;
   const int gp = group <= 4 ? 4 : 8;
@@ -119,6 +131,7 @@ int decode_launch(const DecodeArgs &a) {
   p.n_hc = n_hc;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.wait_ns = a.wait_ns;
+  p.inject = a.inject;
   p.block_table = a.block_table;
   p.seq_lens = a.seq_lens;
   p.page_shift = 0;

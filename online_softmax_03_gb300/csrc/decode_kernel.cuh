@@ -58,6 +58,7 @@ struct DecodeParams {
   int n_hc;                 // head chunks of GP per K/V head
   float scale_log2;
   unsigned long long wait_ns;
+  int inject;               // test hook: 2 = CTA (0, 0, 0) withholds its first tile
   // paged cache only (Tk is then the longest allowed sequence)
   const int *block_table;   // [B, max_pages]
   const int *seq_lens;      // [B]
@@ -81,6 +82,7 @@ struct DecodeCfg {
   static constexpr uint32_t OFF_P = OFF_V + STAGES * TILE_BYTES;   // [CW][32] float2
   static constexpr uint32_t OFF_A = OFF_P + CW * 32 * 8;           // [CW][GP]
   static constexpr uint32_t OFF_BAR = OFF_A + CW * GP * 4;
+  static constexpr uint32_t OFF_FAIL = OFF_BAR + 2 * STAGES * 8;   // int: a warp gave up
   static constexpr uint32_t SMEM_BYTES = OFF_BAR + 2 * STAGES * 8 + 128;
   // merge scratch, aliased on the (drained) K/V ring after the main loop
   static constexpr uint32_t OFF_MM = 0;                            // [CW][GP]
@@ -159,11 +161,13 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS)
   const uint8_t *kg = reinterpret_cast<const uint8_t *>(p.k + kv_off);
   const uint8_t *vg = reinterpret_cast<const uint8_t *>(p.v + kv_off);
 
+  volatile int *failed = reinterpret_cast<volatile int *>(smem + C::OFF_FAIL);
   if (threadIdx.x == 0) {
     for (int s = 0; s < ST; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], C::CW);
     }
+    *failed = 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -184,7 +188,12 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS)
         mbar_arrive_expect_tx(&full[s], 2 * bytes);
         uint8_t *dk = smem + C::OFF_K + s * C::TILE_BYTES;
         uint8_t *dv = smem + C::OFF_V + s * C::TILE_BYTES;
-        if constexpr (kPaged) {
+        // test hook: the first tile of CTA (0, 0, 0) is never loaded, so the
+        // consumers' wait for it must expire
+        const bool withhold =
+            p.inject == 2 && t == 0 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0;
+        if (withhold) {
+        } else if constexpr (kPaged) {
           // The tile's keys k0 + t*TILE + [0, rows) may span several pages:
           // one copy per piece that lies within one page.
           const int page = 1 << p.page_shift;
@@ -352,7 +361,10 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS)
     }
     if (lane == 0) mbar_arrive(&empty[s]);
   }
-  if (!ok) atomicMax(p.status, kDecodeStatusTimeout);
+  if (!ok) {
+    atomicMax(p.status, kDecodeStatusTimeout);
+    if (lane == 0) *failed = 1;
+  }
   float acc[GP][VEC];
 #pragma unroll
   for (int hh = 0; hh < GP; ++hh) {
@@ -382,13 +394,17 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS)
 #pragma unroll
     for (int e = 0; e < VEC; ++e) aa[(warp * GP + hh) * D + lane * VEC + e] = acc[hh][e];
   named_barrier_sync(1, C::CW * 32);
-  if (ok) {
-    for (int idx = threadIdx.x; idx < nh * D; idx += C::CW * 32) {
-      const int hh = idx / D, col = idx - hh * D;
-      float ms = -INFINITY;
+  // A split whose consumers gave up writes an empty partial (m = -inf, l = 0,
+  // acc = 0), which the merge weighs with 0, so no call ever mixes in what an
+  // earlier call left in the workspace; the status word reports the timeout.
+  const bool merged_ok = *failed == 0;
+  for (int idx = threadIdx.x; idx < nh * D; idx += C::CW * 32) {
+    const int hh = idx / D, col = idx - hh * D;
+    float ms = -INFINITY;
+    float a = 0.f, ls = 0.f;
+    if (merged_ok) {
 #pragma unroll
       for (int w = 0; w < C::CW; ++w) ms = fmaxf(ms, mm[w * GP + hh]);
-      float a = 0.f, ls = 0.f;
 #pragma unroll
       for (int w = 0; w < C::CW; ++w) {
         const float mw = mm[w * GP + hh];
@@ -396,12 +412,12 @@ __global__ void __launch_bounds__(DecodeCfg<D, GP>::THREADS)
         a = fmaf(wt, aa[(w * GP + hh) * D + col], a);
         ls = fmaf(wt, ll[w * GP + hh], ls);
       }
-      const size_t row = (size_t)b * p.Hq + h0 + hh;
-      p.part_acc[(row * p.nsplit + sidx) * D + col] = a;
-      if (col == 0) {
-        p.part_ml[(row * p.nsplit + sidx) * 2 + 0] = ms;
-        p.part_ml[(row * p.nsplit + sidx) * 2 + 1] = ls;
-      }
+    }
+    const size_t row = (size_t)b * p.Hq + h0 + hh;
+    p.part_acc[(row * p.nsplit + sidx) * D + col] = a;
+    if (col == 0) {
+      p.part_ml[(row * p.nsplit + sidx) * 2 + 0] = ms;
+      p.part_ml[(row * p.nsplit + sidx) * 2 + 1] = ls;
     }
   }
 }

@@ -84,6 +84,7 @@ ATTN_API int attn_decode_noalloc(const void *q, const void *k_cache, const void 
   a.workspace = scratch;
   a.workspace_bytes = kNoAllocScratchBytes;  // plans needing more are rejected
   a.stream = static_cast<cudaStream_t>(stream);
-  a.wait_ns = 1000000000ull;
+  a.wait_ns = attn_host::wait_limit_ns();
+  a.inject = attn_host::inject_hook();
   return attn_host::decode_launch(a);
 }

@@ -38,6 +38,7 @@ struct DecodeArgs {
   size_t workspace_bytes;
   cudaStream_t stream;
   unsigned long long wait_ns;
+  int inject = 0;  // test hook (attn_debug_set)
   // paged cache (k, v are page pools [num_pages, Hkv, page_size, d])
   bool paged = false;
   const int *block_table = nullptr;
@@ -56,6 +57,7 @@ struct BwdArgs {
   size_t workspace_bytes;
   cudaStream_t stream;
   unsigned long long wait_ns;
+  int inject = 0;  // test hook (attn_debug_set)
 };
 
 // Return an attn_status code.
@@ -71,7 +73,19 @@ size_t bwd_workspace_bytes_for(int B, int Hq, int Tq, int d);
 int validate_decode_args(const void *q, const void *k, const void *v, const void *o,
                          const float *lse, int B, int Hq, int Hkv, int Tk, int d,
                          float scale, float *scale_out);
+// Compute capability 10.3 check and SM count of the current device, queried
+// once per device and cached.
 int check_device_sm103(int *num_sms);
+// Device address of a __device__ symbol (the address of its host-side
+// stand-in) on the current device, looked up once per (symbol, device).
+int symbol_address(const void *symbol, void **out);
+// Raises a kernel's dynamic shared-memory limit to `bytes`, once per
+// (kernel, device).
+int ensure_smem_limit(const void *kern, int bytes);
+// The wait limit attn_debug_set chose (1 s unless a test changed it).
+unsigned long long wait_limit_ns();
+// The test hook attn_debug_set chose (0 = none).
+int inject_hook();
 // 3-D bf16 tensor map over a dense (inner, rows, planes) array; the box is
 // box_inner x box_rows x box_planes elements.
 bool encode_tmap_3d_bf16(CUtensorMap *map, const void *base, uint64_t inner,

@@ -10,16 +10,39 @@
 namespace {
 __device__ unsigned int g_prefill_status;
 
-// Work counters of the persistent prefill kernel: one {next item, finished
-// CTAs} pair per launch slot.  A launch takes the next slot in turn, finds it
-// zero and leaves it zero (its last CTA resets it), so up to kWorkSlots
-// launches may be in flight at once on different streams.
-constexpr int kWorkSlots = 64;
-__device__ unsigned int g_prefill_work[2 * kWorkSlots];
+// Work counters of the persistent prefill kernel: per slot two 64-bit words
+// {items taken, CTAs finished}, each (tag << 32) | count.  A launch made
+// outside graph capture gets a fresh tag e and uses slot e % kWorkSlots of
+// the first pool; its first fetch finds an older tag there and restarts the
+// count, so nothing needs resetting afterwards.  A launch captured into a
+// CUDA graph replays with the same tag, so it uses the second pool, and its
+// last CTA frees the slot (tag 0) for the next replay.  A launch whose slot
+// was taken over by a newer one (more than kWorkSlots launches of a pool in
+// flight at once) stops and reports ATTN_ERR_IN_FLIGHT_LIMIT instead of
+// sharing the count.
+constexpr int kWorkSlots = ATTN_FWD_MAX_IN_FLIGHT;
+__device__ unsigned long long g_prefill_work[2 * 2 * kWorkSlots];
 std::atomic<unsigned int> g_launch_seq{0};
+std::atomic<unsigned int> g_graph_seq{0};
+
+// Tag of the next launch of a pool (never 0: 0 marks a free slot).
+unsigned int next_epoch(std::atomic<unsigned int> &seq) {
+  unsigned int e = seq.fetch_add(1) + 1;
+  if (e == 0) e = seq.fetch_add(1) + 1;
+  return e;
+}
+
+// Picks the pool, tag and slot of a launch (graph: captured into a CUDA
+// graph).
+void take_slot(bool graph, unsigned long long *work, attn_dev::PrefillParams &p) {
+  p.graph_mode = graph ? 1 : 0;
+  p.epoch = next_epoch(graph ? g_graph_seq : g_launch_seq);
+  const int slot = (graph ? kWorkSlots : 0) + (int)(p.epoch % kWorkSlots);
+  p.work = work + 2 * slot;
+}
 
 template <int D, bool kWindow>
-int launch_d(const attn_host::PrefillArgs &a, unsigned int *status, unsigned int *work,
+int launch_d(const attn_host::PrefillArgs &a, unsigned int *status, unsigned long long *work,
              int sms) {
   using C = attn_dev::PrefillCfg<D>;
   CUtensorMap tq, tk, tv;
@@ -57,13 +80,16 @@ int launch_d(const attn_host::PrefillArgs &a, unsigned int *status, unsigned int
   const uint64_t items = bhq * (uint64_t)p.n_qt;
   if (items > (uint64_t)INT_MAX) return ATTN_ERR_INVALID_ARG;
   p.n_items = (int)items;
-  p.work = work + 2 * (g_launch_seq.fetch_add(1) % kWorkSlots);
+  {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(a.stream, &cs) != cudaSuccess) return ATTN_ERR_CUDA;
+    take_slot(cs == cudaStreamCaptureStatusActive, work, p);
+  }
   // Persistent: one CTA per SM (each holds all of an SM's tensor memory);
   // CTAs take work items from the slot's counter until the list is done.
   const uint64_t grid = items < (uint64_t)sms ? items : (uint64_t)sms;
   auto kern = attn_dev::prefill_fwd_kernel<D, kWindow, false>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)C::SMEM_BYTES) != cudaSuccess)
+  if (attn_host::ensure_smem_limit((const void *)kern, (int)C::SMEM_BYTES) != ATTN_OK)
     return ATTN_ERR_CUDA;
   kern<<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(tq, tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
@@ -172,8 +198,8 @@ __global__ void __launch_bounds__(kPlanThreads)
 }
 
 template <int D>
-int launch_varlen(const attn_host::PrefillArgs &a, unsigned int *status, unsigned int *work,
-                  int sms) {
+int launch_varlen(const attn_host::PrefillArgs &a, unsigned int *status,
+                  unsigned long long *work, int sms) {
   using C = attn_dev::PrefillCfg<D>;
   const long long capacity = attn_host::varlen_list_capacity(a.B, a.total_q, a.Tq);
   if (capacity < 1 || capacity * a.Hq > (long long)INT_MAX) return ATTN_ERR_INVALID_ARG;
@@ -215,7 +241,11 @@ int launch_varlen(const attn_host::PrefillArgs &a, unsigned int *status, unsigne
   p.cu_k = a.cu_k;
   p.vl_list = static_cast<const int *>(a.workspace);
   p.total_q = a.total_q;
-  p.work = work + 2 * (g_launch_seq.fetch_add(1) % kWorkSlots);
+  {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(a.stream, &cs) != cudaSuccess) return ATTN_ERR_CUDA;
+    take_slot(cs == cudaStreamCaptureStatusActive, work, p);
+  }
   varlen_plan_kernel<<<1, kPlanThreads, 0, a.stream>>>(
       a.cu_q, a.cu_k, a.B, a.total_q, a.total_k, a.Tq, a.Tk, a.causal, a.window,
       static_cast<int *>(a.workspace), capacity, status);
@@ -225,8 +255,7 @@ int launch_varlen(const attn_host::PrefillArgs &a, unsigned int *status, unsigne
   // the sliding window inside each sequence compiles a variant of its own
   auto kern = a.window > 0 ? attn_dev::prefill_fwd_kernel<D, true, true>
                            : attn_dev::prefill_fwd_kernel<D, false, true>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)C::SMEM_BYTES) != cudaSuccess)
+  if (attn_host::ensure_smem_limit((const void *)kern, (int)C::SMEM_BYTES) != ATTN_OK)
     return ATTN_ERR_CUDA;
   kern<<<(unsigned)grid, C::THREADS, C::SMEM_BYTES, a.stream>>>(tq, tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
@@ -252,10 +281,12 @@ int prefill_launch(const PrefillArgs &a) {
   int sms = 0;
   const int rc = check_device_sm103(&sms);
   if (rc != ATTN_OK) return rc;
-  unsigned int *status = nullptr, *work = nullptr;
-  if (cudaGetSymbolAddress(reinterpret_cast<void **>(&status), g_prefill_status) !=
-          cudaSuccess ||
-      cudaGetSymbolAddress(reinterpret_cast<void **>(&work), g_prefill_work) != cudaSuccess)
+  unsigned int *status = nullptr;
+  unsigned long long *work = nullptr;
+  if (symbol_address((const void *)&g_prefill_status, reinterpret_cast<void **>(&status)) !=
+          ATTN_OK ||
+      symbol_address((const void *)&g_prefill_work, reinterpret_cast<void **>(&work)) !=
+          ATTN_OK)
     return ATTN_ERR_CUDA;
   if (a.varlen) {
     switch (a.d) {

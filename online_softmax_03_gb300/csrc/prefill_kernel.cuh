@@ -87,6 +87,7 @@
 namespace attn_dev {
 
 constexpr unsigned int kStatusTimeout = 6;  // ATTN_ERR_DEVICE_TIMEOUT
+constexpr unsigned int kStatusSlotLost = 7;  // ATTN_ERR_IN_FLIGHT_LIMIT
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -100,7 +101,9 @@ struct PrefillParams {
   int n_bh;               // B * Hq
   int head_group;         // heads per scheduling group (K/V working set in L2)
   int n_items;            // n_bh * n_qt
-  unsigned int *work;     // {next item, finished CTAs}: zero on entry, zero on exit
+  unsigned long long *work;  // work slot: {items taken, CTAs finished}, each (tag << 32) | n
+  unsigned int epoch;        // this launch's tag (never 0)
+  int graph_mode;            // 1: captured into a CUDA graph (the last CTA frees the slot)
   int causal;
   int window;             // > 0: causal sliding window of this many keys
   float scale_log2;       // scale * log2(e)
@@ -288,6 +291,57 @@ __device__ __forceinline__ PrefillItem prefill_item(const PrefillParams &p, int 
   return it;
 }
 
+// Work slot of a launch: two words, each (tag << 32) | count, counting the
+// items taken and the CTAs that have finished.  Tag 0 marks a free word; the
+// launch's first increment of a word that is free or carries an older tag
+// claims it (compare-and-swap) and restarts the count.  Every other
+// increment is one atomicAdd: an add that lands on an unclaimed word only
+// moves that word's stale count and is retried after the claim.  Every
+// launch made outside graph capture has a tag of its own, so it leaves its
+// words as they are; a launch captured into a CUDA graph keeps its tag for
+// every replay, so its last CTA frees the words again (those launches use
+// slots of their own).  Returns false if a newer launch owns the word (more
+// launches in flight than there are slots), or if the claim keeps losing
+// for an implausible number of rounds.
+__device__ __forceinline__ bool tagged_increment(unsigned long long *word, unsigned int tag,
+                                                 unsigned int *before) {
+  const unsigned long long mine = (unsigned long long)tag << 32;
+  for (int round = 0; round < 4096; ++round) {
+    const unsigned long long old = atomicAdd(word, 1ull);
+    const unsigned int t = (unsigned int)(old >> 32);
+    if (t == tag) {
+      *before = (unsigned int)old;
+      return true;
+    }
+    if (t != 0 && (int)(t - tag) > 0) return false;  // a newer launch owns it
+    // free or older: claim it, unless another CTA of this launch already has
+    unsigned long long cur = old + 1ull;
+    for (int c = 0; c < 4096; ++c) {
+      const unsigned long long prev = atomicCAS(word, cur, mine | 1ull);
+      if (prev == cur) {
+        *before = 0;
+        return true;
+      }
+      const unsigned int pt = (unsigned int)(prev >> 32);
+      if (pt == tag) break;  // claimed by another CTA: add again
+      if (pt != 0 && (int)(pt - tag) > 0) return false;
+      cur = prev;
+    }
+  }
+  return false;
+}
+
+// Frees the word if the launch with this tag still owns it.
+__device__ __forceinline__ void tagged_release(unsigned long long *word, unsigned int tag) {
+  unsigned long long w = atomicAdd(word, 0ull);
+  for (int round = 0; round < (1 << 20); ++round) {
+    if ((unsigned int)(w >> 32) != tag) return;
+    const unsigned long long prev = atomicCAS(word, w, 0ull);
+    if (prev == w) return;
+    w = prev;
+  }
+}
+
 template <int D, bool kWindow, bool kVarlen>
 __global__ void __launch_bounds__(320, 1)
     prefill_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -398,8 +452,18 @@ __global__ void __launch_bounds__(320, 1)
           ok = false;
           break;
         }
-        int idx = (int)atomicAdd(&p.work[0], 1u);
-        if (idx >= n_items) idx = -1;
+        // The first item of every CTA is its block index (the heaviest items
+        // come first); later ones come from the launch's counter.
+        int idx = -1;
+        if (fetch == 0) {
+          idx = (int)blockIdx.x < n_items ? (int)blockIdx.x : -1;
+        } else {
+          unsigned int taken = 0;
+          if (!tagged_increment(&p.work[0], p.epoch, &taken))
+            atomicMax(p.status, kStatusSlotLost);
+          else if ((long long)taken + gridDim.x < (long long)n_items)
+            idx = (int)(taken + gridDim.x);
+        }
         volatile int *ring = item_ring + k * kRingInts;
         ring[0] = idx;
         VarlenItem vi{};
@@ -811,13 +875,14 @@ __global__ void __launch_bounds__(320, 1)
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
-  if (threadIdx.x == 0) {
-    // Every producer of this launch has stopped fetching once all CTAs have
-    // arrived here, so the last CTA resets the counters for the next launch.
+  if (p.graph_mode && threadIdx.x == 0) {
+    // Every producer of this launch has stopped fetching once all its CTAs
+    // have arrived here, so the last one frees the slot for the next replay.
     __threadfence();
-    if (atomicAdd(&p.work[1], 1u) == gridDim.x - 1) {
-      atomicExch(&p.work[0], 0u);
-      atomicExch(&p.work[1], 0u);
+    unsigned int done = 0;
+    if (tagged_increment(&p.work[1], p.epoch, &done) && done + 1 == gridDim.x) {
+      tagged_release(&p.work[0], p.epoch);
+      tagged_release(&p.work[1], p.epoch);
       __threadfence();
     }
   }

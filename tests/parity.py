@@ -5,6 +5,9 @@ max |dO| <= 2e-2, mean |dO| <= 2e-3, max |dLSE| <= 1e-3.
 """
 from __future__ import annotations
 
+import json
+import os
+
 import numpy as np
 
 import synth
@@ -35,8 +38,20 @@ def assert_close(o_gpu, lse_gpu, o_ref, lse_ref, what="", lse_rel=0.0):
     assert mo <= TOL_MAX_O, f"{what}: max|dO| = {mo:.3e}"
     assert mean_o <= TOL_MEAN_O, f"{what}: mean|dO| = {mean_o:.3e}"
     bound = TOL_MAX_LSE + lse_rel * np.abs(lse_ref)
+    _report(what, mo, mean_o, ml, lse.size)
     assert np.all(dl <= bound), f"{what}: max|dLSE| = {ml:.3e}"
     return mo, mean_o, ml
+
+
+def _report(what, mo, mean_o, ml, rows):
+    """Append the measured errors to the JSON-lines file named by
+    ATTN_PARITY_REPORT (unset: nothing is written)."""
+    path = os.environ.get("ATTN_PARITY_REPORT")
+    if not path:
+        return
+    with open(path, "a") as f:
+        f.write(json.dumps({"case": what, "rows": int(rows), "max_abs_dO": float(mo),
+                            "mean_abs_dO": float(mean_o), "max_abs_dLSE": float(ml)}) + "\n")
 
 
 def oracle_full(q, k, v, causal, scale):

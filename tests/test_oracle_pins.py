@@ -227,6 +227,28 @@ def test_rows_entry_point_matches_dense():
         np.testing.assert_allclose(lrow, lse[rb, rh, ri], rtol=0, atol=1e-14)
 
 
+@pytest.mark.parametrize("window", [1, 3, 7, 30])
+def test_rows_entry_point_matches_dense_with_a_window(window):
+    """The sampled-rows routine under a sliding window equals the dense
+    windowed definition on every row (GQA, Tq < Tk, and windows from one key
+    to past every row), so tests that check rows instead of whole tensors
+    rest on a pinned routine."""
+    q, k, v = _rand((2, 4, 19, 8), 31), _rand((2, 2, 23, 8), 32), _rand((2, 2, 23, 8), 33)
+    o, lse, _ = ora.attention_dense(q, k, v, causal=True, window=window)
+    rb, rh, ri = np.meshgrid(np.arange(2), np.arange(4), np.arange(19), indexing="ij")
+    rb, rh, ri = rb.ravel(), rh.ravel(), ri.ravel()
+    orow, lrow = ora.attention_rows(q, k, v, rb, rh, ri, causal=True, window=window)
+    np.testing.assert_allclose(orow, o[rb, rh, ri], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lrow, lse[rb, rh, ri], rtol=0, atol=1e-14)
+    if window == 1:
+        # one visible key: the value at the query's position (bottom-right
+        # aligned, 23 - 19 = 4 keys ahead) and its single scaled score
+        g = rh // 2
+        np.testing.assert_array_equal(orow, v[rb, g, ri + 4])
+        s = (q[rb, rh, ri] * k[rb, g, ri + 4]).sum(-1) / np.sqrt(8)
+        np.testing.assert_allclose(lrow, s, rtol=0, atol=1e-14)
+
+
 # --- blocked online softmax against dense ------------------------------------
 
 @pytest.mark.parametrize("bq,bk", [(8, 8), (16, 16), (13, 19), (32, 8), (1, 1), (64, 64)])
