@@ -140,7 +140,11 @@ struct PrefillCfg {
   static constexpr uint32_t OFF_BAR = OFF_EPI + 8 * EPI_WARP_BYTES;
   // drain, q_full[2], q_empty[2], s_full[2], p_full[2], o_done[2],
   // item_full[2], item_empty[2], then per stage k_full, v_full, k_empty, v_empty
-  static constexpr int NBAR = 15 + 4 * STAGES;
+  // At D <= 64 tensor memory has room for P beside S: P_t gets a region of
+  // its own, so S_t of the next K/V tile may be written while P_t is formed.
+  static constexpr bool SEP_P = D <= 64;
+  // ..., then s_free[2] and pv_done[2] (SEP_P)
+  static constexpr int NBAR = 19 + 4 * STAGES;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   // tmem slot, abort flag, then the two-entry item ring of kRingInts ints each
   static constexpr uint32_t SMEM_USED = OFF_MISC + 128 + 1024;  // + align slack
@@ -153,9 +157,14 @@ struct PrefillCfg {
   static constexpr int MMA_WARP = 9;
   __host__ __device__ static constexpr uint32_t tm_s(int t) { return t * 128; }
   __host__ __device__ static constexpr uint32_t tm_o(int t) { return 256 + t * D; }
+  // P_t: 64 columns of bf16 pairs (128 keys), after both O regions
+  __host__ __device__ static constexpr uint32_t tm_p(int t) {
+    return SEP_P ? 384 + t * 64 : tm_s(t);
+  }
   static_assert(D % CHUNK == 0, "head dim must be a whole number of boxes");
   static_assert(Q_BYTES % 1024 == 0 && KV_BYTES % 1024 == 0, "1 KiB regions");
   static_assert(256 + 2 * D <= 512, "tensor memory budget");
+  static_assert(!SEP_P || 256 + 2 * D <= 384, "P regions after the O regions");
   static_assert(SMEM_BYTES <= 232448u, "shared memory budget");
   static_assert(EPI_UNITS == 8 || EPI_UNITS == 4, "epilogue swizzle");
   // The 16-byte unit u of staged row r sits at unit epi_swz(u, r) of the row,
@@ -361,6 +370,8 @@ __global__ void __launch_bounds__(320, 1)
   uint64_t *item_full = bars + 11, *item_empty = bars + 13;
   uint64_t *k_full = bars + 15, *v_full = k_full + ST;
   uint64_t *k_empty = v_full + ST, *v_empty = k_empty + ST;
+  // SEP_P: S_t has been loaded (its region may be rewritten); P_t V done
+  uint64_t *s_free = v_empty + ST, *pv_done = s_free + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
   volatile int *item_ring =
@@ -378,6 +389,8 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(&s_full[t], 1);
       mbar_init(&p_full[t], C::BM);
       mbar_init(&o_done[t], 1);
+      mbar_init(&s_free[t], C::BM);
+      mbar_init(&pv_done[t], 1);
     }
     for (int k = 0; k < 2; ++k) {
       mbar_init(&item_full[k], 1);
@@ -581,12 +594,13 @@ __global__ void __launch_bounds__(320, 1)
         const uint64_t vd = adv(v_desc, s * C::KV_BYTES);
 #pragma unroll
         for (int kk = 0; kk < C::BN / 16; ++kk)  // 16 keys = 8 TMEM columns of P
-          mma_bf16_ts_elect(tmem + C::tm_o(t), tmem + C::tm_s(t) + kk * 8, adv(vd, kk * 16 * C::SPAN),
+          mma_bf16_ts_elect(tmem + C::tm_o(t), tmem + C::tm_p(t) + kk * 8, adv(vd, kk * 16 * C::SPAN),
                       IDESC_PV, (acc || kk > 0) ? 1u : 0u);
       };
       bool ok = true;
       int q_cnt0 = 0, q_cnt1 = 0;  // Q_t tiles consumed
       int p_cnt0 = 0, p_cnt1 = 0;  // P_t tiles consumed
+      int f_cnt0 = 0, f_cnt1 = 0;  // S_t loads signalled (SEP_P)
       int kv = 0;                  // K/V tiles consumed (all items)
       for (int fetch = 0; ok;) {
         int idx = -1;
@@ -653,7 +667,46 @@ __global__ void __launch_bounds__(320, 1)
             }
             return true;
           };
-          if (aborted() || !tile_step(0, p_cnt0, q_cnt0) || !tile_step(1, p_cnt1, q_cnt1)) {
+          if constexpr (C::SEP_P) {
+            // S_t of the next K/V tile as soon as the group has loaded S_t(j)
+            // (P_t has a region of its own), then P_t V_j once P_t is ready.
+            auto next_s = [&](const int t, int &f_cnt, int &q_cnt) -> bool {
+              const int lo = kWindow ? it.lo(t) : 0, hi = it.hi(t);
+              if ((!kWindow || lo <= j) && j + 1 < hi) {
+                if (!wait_all(&s_free[t], f_cnt & 1)) return false;
+                ++f_cnt;
+                if (!need_k()) return false;
+                tc_fence_after();  // the group's loads of S_t(j) completed before its arrive
+                issue_s(t, s1);
+                mma_commit_elect(&s_full[t]);
+                if (j + 2 == hi) mma_commit_elect(&q_empty[t]);  // last S_t of the item
+              } else if (kWindow && j + 1 == lo && lo < hi) {
+                if (!need_k() || !start_tile(t, q_cnt, s1, j + 1)) return false;
+              }
+              return true;
+            };
+            auto pv = [&](const int t, int &p_cnt) -> bool {
+              const int lo = kWindow ? it.lo(t) : 0, hi = it.hi(t);
+              if ((!kWindow || lo <= j) && j < hi) {
+                if (!wait_all(&p_full[t], p_cnt & 1)) return false;
+                ++p_cnt;
+                if (!v_ready) {
+                  if (!wait_all(&v_full[s], u & 1)) return false;
+                  v_ready = true;
+                }
+                tc_fence_after();  // P_t was written to tensor memory by the softmax threads
+                issue_pv(t, s, j > lo);
+                mma_commit_elect(j + 1 < hi ? &pv_done[t] : &o_done[t]);
+              }
+              return true;
+            };
+            if (aborted() || !next_s(0, f_cnt0, q_cnt0) || !next_s(1, f_cnt1, q_cnt1) ||
+                !pv(0, p_cnt0) || !pv(1, p_cnt1)) {
+              ok = false;
+              break;
+            }
+          } else if (aborted() || !tile_step(0, p_cnt0, q_cnt0) ||
+                     !tile_step(1, p_cnt1, q_cnt1)) {
             ok = false;
             break;
           }
@@ -676,9 +729,11 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t t_s = tmem + lane_base + C::tm_s(t);
     const uint32_t t_o = tmem + lane_base + C::tm_o(t);
+    const uint32_t t_p = tmem + lane_base + C::tm_p(t);
     const float sl2 = p.scale_log2;
     int s_cnt = 0;  // S_t tiles consumed (all items)
     int o_cnt = 0;  // O_t tiles finished (all items)
+    int v_cnt = 0;  // P_t V products waited for (SEP_P)
     bool ok = true;
 
     for (int fetch = 0; ok;) {
@@ -711,6 +766,13 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_after();
         float s[C::BN];
         tmem_ld128_wait(t_s, s);
+        if constexpr (C::SEP_P) {
+          // S_t(j) is in registers: the next S_t may overwrite its region
+          if (j + 1 < jhi) {
+            tc_fence_before();
+            mbar_arrive(&s_free[t]);
+          }
+        }
 
         const int kbase = j * C::BN;
         const bool need_mask = (kbase + C::BN > Tk) ||
@@ -743,10 +805,9 @@ __global__ void __launch_bounds__(320, 1)
           alpha = ex2_approx(m_used - m_new);  // 0 while nothing was seen
           m_used = m_new;
         }
-        // O_t is stable here (PV_t(j-1) completed before S_t(j) was signalled):
-        // rescale it before any of P_t(j) is published.  Chunks of 16 columns
-        // keep the registers this rare path needs small next to the S row.
-        if (j > jlo && __any_sync(0xffffffffu, resc)) {
+        // Rescaling O_t by alpha: chunks of 16 columns keep the registers this
+        // rare path needs small next to the S row.
+        auto rescale_o = [&]() {
           const float2 al2 = make_float2(alpha, alpha);
 #pragma unroll 1
           for (int cb = 0; cb < D / 16; ++cb) {
@@ -762,7 +823,21 @@ __global__ void __launch_bounds__(320, 1)
             tmem_st16(t_o + cb * 16, ow);
           }
           tmem_st_wait();
+        };
+        if constexpr (C::SEP_P) {
+          // P_t V_(j-1) has read P_t and updated O_t before either is touched
+          if (j > jlo) {
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait(&pv_done[t], v_cnt & 1, wait_ns) && !*abort_flag);
+            if (!ok) break;
+            ++v_cnt;
+            tc_fence_after();
+          }
         }
+        // O_t is stable here (PV_t(j-1) completed before S_t(j) was signalled,
+        // or, with a P region of its own, was waited for above): rescale it
+        // before any of P_t(j) is published.
+        if (j > jlo && __any_sync(0xffffffffu, resc)) rescale_o();
         const float m_ref = (m_used == -INFINITY) ? 0.f : m_used;
         const float2 c2 = make_float2(sl2, sl2);
         const float2 b2 = make_float2(-m_ref, -m_ref);
@@ -783,7 +858,7 @@ __global__ void __launch_bounds__(320, 1)
             acc2[c & 3] = __fadd2_rn(acc2[c & 3], e);
             pw[c] = pack_bf16x2(e.x, e.y);
           }
-          tmem_st16(t_s + q4 * 16, pw);
+          tmem_st16(t_p + q4 * 16, pw);
         }
         tmem_st_wait();
         tc_fence_before();
