@@ -257,6 +257,8 @@ def time_config_rows(dev, stream, peak_burst):
             "tflops": round(flops / (p50 / 1e3) / 1e12, 2),
             "frac_of_burst_peak": round(flops / (p50 / 1e3) / 1e12 / peak_burst, 4),
             "flops_per_launch": flops,
+            "traffic": ncu_traffic(f"prefill_fwd_kernel<{w.d}>/{w.name}",
+                                   source_sha(*PREFILL_SOURCES)),
         }
         del q, k, v, o, lse
     del flush_buf
@@ -712,7 +714,8 @@ def run_reference(args, rank, world):
     print(json.dumps(result), flush=True)
 
 
-PROFILE_WORKLOADS = {w.name: w for w in synth.ALL + (synth.WINDOW_8K,)}
+PROFILE_WORKLOADS = {w.name: w for w in synth.ALL + (synth.WINDOW_8K, synth.PAGED_DECODE,
+                                                     synth.VARLEN)}
 
 
 def run_profile(args):
@@ -731,6 +734,24 @@ def run_profile(args):
     backward = name.endswith(":bwd")
     w = PROFILE_WORKLOADS[name[:-4] if backward else name]
     dev = torch.device("cuda", 0)
+    if w is synth.PAGED_DECODE:
+        pq, pk, pv, tab, lens = synth.make_paged_inputs(
+            w.B, w.Hq, w.Hkv, w.d, synth.PAGED_PAGE_SIZE, [w.Tk] * w.B, w.seed, dev)
+        fn = lambda: binding.decode_paged(pq, pk, pv, tab, lens, max_seq_len=w.Tk,  # noqa
+                                          scale=w.scale)
+    elif w is synth.VARLEN:
+        lens = synth.packed_lengths(synth.VARLEN_TOKENS, w.seed)
+        vq, vk, vv, cq, ck = synth.make_varlen_inputs(lens, lens, w.Hq, w.Hkv, w.d, w.seed, dev)
+        fn = lambda: binding.fwd_varlen(vq, vk, vv, cq, ck, max(lens), max(lens),  # noqa
+                                        causal=True, scale=w.scale)
+    if w is synth.PAGED_DECODE or w is synth.VARLEN:
+        for _ in range(args.launches):
+            fn()
+        torch.cuda.synchronize()
+        assert binding.attn_device_status() == binding.ATTN_OK
+        print(json.dumps({"profile": name, "launches": args.launches,
+                          "device_bytes": torch.cuda.max_memory_allocated()}), flush=True)
+        return
     q, k, v = synth.make_inputs(w, dev)
     if w.decode:
         ws = binding.decode_workspace(k, w.Hq)
@@ -768,7 +789,8 @@ def main():
     ap.add_argument("--no-extra-rows", action="store_true",
                     help="skip the separately timed rows beyond the specified step")
     ap.add_argument("--profile", choices=sorted(PROFILE_WORKLOADS) +
-                    sorted(n + ":bwd" for n in PROFILE_WORKLOADS if "decode" not in n),
+                    sorted(n + ":bwd" for n in PROFILE_WORKLOADS
+                           if "decode" not in n and "varlen" not in n),
                     help="run only this workload's kernels (for ncu captures); "
                          "NAME:bwd runs the backward")
     ap.add_argument("--launches", type=int, default=3)
