@@ -140,6 +140,20 @@ def oracle_prefill_sample(q, k, v, n_heads):
     return flops, dt
 
 
+def oracle_blocked_prefill_sample(q, k, v, n_heads, block=128):
+    """Time the oracle's blocked online-softmax forward (the pages' tiled
+    algorithm, block x block tiles, whole tiles above the diagonal skipped)
+    on the same sample as oracle_prefill_sample."""
+    from oracle import oracle as ora
+
+    qs, ks, vs = (synth.bf16_bits(t[:1, :n_heads]) for t in (q, k, v))
+    t0 = time.perf_counter()
+    ora.attention_blocked(qs, ks, vs, block, block, causal=PREFILL.causal, scale=PREFILL.scale)
+    dt = time.perf_counter() - t0
+    flops = acct.attention_flops(1, n_heads, PREFILL.Tq, PREFILL.Tk, PREFILL.d, PREFILL.causal)
+    return flops, dt
+
+
 def oracle_decode_sample(q, k, v, n_batch):
     from oracle import oracle as ora
 
@@ -164,12 +178,16 @@ DECODE_SAMPLE_BATCH = 8
 
 def cpu_baseline(qp, kp, vp, qd, kd, vd):
     flops, dt = oracle_prefill_sample(qp, kp, vp, PREFILL_SAMPLE_HEADS)
+    bflops, dtb = oracle_blocked_prefill_sample(qp, kp, vp, PREFILL_SAMPLE_HEADS)
     nbytes, dtd = oracle_decode_sample(qd, kd, vd, DECODE_SAMPLE_BATCH)
     return {
         "value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": omp_threads(),
         "kind": "oracle",
         "sample": (f"fp64 dense oracle on {PREFILL_SAMPLE_HEADS} of {PREFILL.B * PREFILL.Hq} "
                    f"heads of the prefill workload ({dt:.2f} s)"),
+        "blocked": {"value": bflops / dtb / 1e12, "unit": "TFLOP/s",
+                    "sample": (f"fp64 blocked online-softmax oracle (128 x 128 tiles) on the "
+                               f"same {PREFILL_SAMPLE_HEADS} heads ({dtb:.2f} s)")},
         "decode": {"value": nbytes / dtd / 1e9, "unit": "GB/s",
                    "sample": (f"fp64 dense oracle on {DECODE_SAMPLE_BATCH} of {DECODE.B} "
                               f"sequences of the decode workload ({dtd:.2f} s)")},

@@ -31,7 +31,8 @@ def _worker(rank, world, port, out):
 def test_max_over_two_gloo_ranks():
     world = 2
     port = _free_port()
-    with mp.Manager() as mgr:
+    # spawn, not fork: earlier tests may have started the oracle's threads
+    with mp.get_context("spawn").Manager() as mgr:
         out = mgr.dict()
         mp.start_processes(_worker, args=(world, port, out), nprocs=world, start_method="spawn")
         res = dict(out)
